@@ -1,0 +1,326 @@
+"""CPU oracle for the MoE layer hot path.  TEST INFRASTRUCTURE ONLY.
+
+Plain, slow, obviously correct restatement of what the layer computes, in
+float64 with bfloat16 rounding applied only at the declared storage points.
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may use it; the product path never does, and this module shares
+no code with the CUDA path.
+
+Source of the method: "Enabling trillion-parameter models on AWS EFA"
+(Licker, Hu, Zaytsev, Chen; 2025).  The page fixes:
+  * section "Introduction": an MoE layer replaces a dense layer with a set of
+    experts plus a small linear routing layer that picks the experts a token is
+    multiplied with; dispatch splits the tokens by expert, and combine, its
+    dual, gathers the processed tokens back and takes their weighted average;
+  * section "Send and receive buffers": T tokens, each routed to R of E experts;
+  * section "Dispatch and combine": per-expert token counts, then a cumulative
+    sum of the counts gives the offsets that pack the tokens of each expert
+    contiguously; the receiver shuffles tokens into the tensor the grouped
+    GEMM consumes, and combine accumulates the weighted tokens at the receiver;
+  * section "MoE all-to-all over EFA": dispatch -> grouped GEMMs multiply the
+    tokens by the expert weights -> combine returns them and averages.
+Readings where the page is silent (all listed in the design notes):
+  * router: logits = x @ W_g + bias in fp32; experts ordered by (logit desc,
+    index asc); the first R are chosen, in that order; the gate weights are the
+    softmax of the chosen logits (renormalised top-R softmax), so they sum to 1;
+  * within an expert, rows are ordered by ascending token index;
+  * expert FFN: SwiGLU, h = silu(x W1^T) * (x W3^T), o = h W2^T;
+  * bf16 round-to-nearest-even at h, o, y (forward) and at do, da, db,
+    dx_perm, dx (backward); a and b are kept for the backward as bf16;
+  * loss L = sum(y * g); no auxiliary loss; the router bias is a constant.
+
+Parity pins for every function live in tests/test_oracle.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 stored fraction bits.
+# ----------------------------------------------------------------------------
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+_BF16_MIN_QUANTUM_EXP = -133      # spacing of bf16 subnormals: 2^(-126-7)
+
+
+def bf16_round(v, enabled: bool = True):
+    """Round float64 values to the nearest bfloat16 value, ties to even.
+
+    Written from the IEEE 754 definition: a finite nonzero value |v| in
+    [2^k, 2^(k+1)) keeps 8 significant bits, so the representable spacing there
+    is 2^(k-7) (never finer than the subnormal spacing 2^-133).  |v|/spacing is
+    rounded to the nearest integer with ties to even (np.rint) and scaled back;
+    both scalings are exact in float64.  Results above the largest finite bf16
+    value overflow to infinity.  With ``enabled=False`` the values pass through
+    unchanged (used to check gradients by finite differences).
+    """
+    v = np.asarray(v, dtype=np.float64)
+    if not enabled:
+        return v.copy()
+    out = v.copy()
+    fin = np.isfinite(v) & (v != 0.0)
+    a = np.abs(v[fin])
+    _, e = np.frexp(a)                       # a = m * 2^e, 0.5 <= m < 1
+    q = np.ldexp(1.0, np.maximum(e - 1 - 7, _BF16_MIN_QUANTUM_EXP))
+    r = np.rint(a / q) * q
+    r[r > BF16_MAX] = np.inf
+    out[fin] = np.copysign(r, v[fin])
+    return out
+
+
+def bf16_to_f64(bits):
+    """bf16 bit patterns (uint16) -> float64 values (exact)."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def values(a):
+    """bf16 bit patterns (uint16) -> float64 values; other arrays -> float64 as is."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return bf16_to_f64(a)
+    return a.astype(np.float64)
+
+
+def f64_to_bf16_bits(v):
+    """float64 values that are already bf16-representable -> uint16 bit patterns."""
+    f = np.asarray(v, dtype=np.float64).astype(np.float32)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# Routing: a small linear layer scores the experts for each token and the best
+# ones are chosen (section "Introduction").
+# ----------------------------------------------------------------------------
+def gate_logits(x, w_gate, bias=None, rounding=True):
+    """logits[t,e] = sum_k x[t,k] * W_g[k,e] + bias[e]; float64 sums, stored fp32.
+
+    With ``rounding=False`` the float64 sums are returned unrounded.
+    """
+    x = values(x)
+    l = x @ np.asarray(w_gate, dtype=np.float64)
+    if bias is not None:
+        l = l + np.asarray(bias, dtype=np.float64)[None, :]
+    return l.astype(np.float32) if rounding else l
+
+
+def route_topk(logits, R):
+    """Top-R expert choice and gate weights for each token.
+
+    Experts are ordered by (fp32 logit descending, expert index ascending); the
+    first R are taken, in that order (idx[t, 0] is the best expert).  The gate
+    weights are the softmax of the chosen logits,
+        w_r = exp(l_{i_r} - l_{i_0}) / sum_s exp(l_{i_s} - l_{i_0}),
+    so they are positive and sum to 1 (combine is a weighted average).
+    Returns idx int32 [T,R] and w [T,R] (computed in float64; stored float32
+    when the logits are float32, kept float64 when they are float64).
+    """
+    l = np.asarray(logits)
+    assert l.dtype in (np.float32, np.float64)
+    T, E = l.shape
+    assert 1 <= R <= E
+    key_index = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((key_index, -l), axis=-1)     # primary: -logit, then index
+    idx = order[:, :R].astype(np.int32)
+    sel = np.take_along_axis(l, idx, axis=1).astype(np.float64)
+    ex = np.exp(sel - sel[:, :1])
+    w = ex / ex.sum(axis=1, keepdims=True)
+    return idx, w.astype(l.dtype)
+
+
+# ----------------------------------------------------------------------------
+# Dispatch (section "Dispatch and combine": per-expert counts, cumulative sum
+# for contiguous offsets, shuffle into the grouped-GEMM input).
+# ----------------------------------------------------------------------------
+def dispatch_plan(idx, E):
+    """counts[E], offsets[E+1], row_slot[N], slot_row[N] for N = T*R slots.
+
+    A slot is s = t*R + r.  counts[e] = #{s : idx_s = e}; offsets is their
+    exclusive cumulative sum (offsets[E] = N).  Within expert e the rows
+    offsets[e] .. offsets[e+1]-1 hold its slots in ascending token order (a
+    token names an expert at most once, so ascending slot order is the same).
+    row_slot[row] = slot; slot_row[slot] = row (mutually inverse).
+    """
+    flat = np.asarray(idx, dtype=np.int64).reshape(-1)
+    assert flat.size == 0 or (flat.min() >= 0 and flat.max() < E)
+    counts = np.bincount(flat, minlength=E).astype(np.int32)
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    row_slot = np.argsort(flat, kind="stable").astype(np.int32)
+    slot_row = np.empty_like(row_slot)
+    slot_row[row_slot] = np.arange(flat.size, dtype=np.int32)
+    return counts, offsets, row_slot, slot_row
+
+
+def permute_rows(x, row_slot, R):
+    """x_perm[row] = x[token of row_slot[row]] (a copy; bit patterns stay bit patterns)."""
+    return np.asarray(x)[np.asarray(row_slot) // R].copy()
+
+
+# ----------------------------------------------------------------------------
+# Grouped SwiGLU expert FFN: after dispatch, grouped GEMMs apply each expert's
+# weights to the tokens routed to it (section "MoE all-to-all over EFA").
+# ----------------------------------------------------------------------------
+def silu(a):
+    return a / (1.0 + np.exp(-a))
+
+
+def expert_ffn(x_perm, offsets, W1, W3, W2, rounding=True):
+    """Per expert e over rows offsets[e]..offsets[e+1]-1 of x_perm:
+
+        a = x W1[e]^T, b = x W3[e]^T      (float64)
+        h = bf16(silu(a) * b)
+        o = bf16(h W2[e]^T)
+
+    W1, W3: [E, f, d]; W2: [E, d, f] (bf16 bit patterns or float64 values; an
+    expert's weights are decoded only when its rows are processed).
+    Returns a, b (float64), h, o (float64 holding bf16 values).
+    """
+    E = len(offsets) - 1
+    N = int(offsets[-1])
+    f = W1.shape[1]
+    d = W1.shape[2]
+    a = np.zeros((N, f))
+    b = np.zeros((N, f))
+    h = np.zeros((N, f))
+    o = np.zeros((N, d))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r0 == r1:
+            continue
+        xe = values(x_perm[r0:r1])
+        ae = xe @ values(W1[e]).T
+        be = xe @ values(W3[e]).T
+        he = bf16_round(silu(ae) * be, rounding)
+        oe = bf16_round(he @ values(W2[e]).T, rounding)
+        a[r0:r1], b[r0:r1], h[r0:r1], o[r0:r1] = ae, be, he, oe
+    return a, b, h, o
+
+
+# ----------------------------------------------------------------------------
+# Combine: each token's expert outputs come back to it and are averaged with
+# the gate weights (section "Introduction"); the sum is taken at the token's
+# side (section "Dispatch and combine").
+# ----------------------------------------------------------------------------
+def combine(o, slot_row, w, T, R, rounding=True):
+    """y[t] = bf16( sum_{r=0..R-1} w[t,r] * o[slot_row[t*R+r]] ), summed in r order.
+
+    ``o`` holds float64 values; ``w`` None means unweighted (all ones).
+    """
+    o = np.asarray(o, dtype=np.float64)
+    y = np.zeros((T, o.shape[1]))
+    sr = np.asarray(slot_row).reshape(T, R)
+    for r in range(R):
+        wr = 1.0 if w is None else np.asarray(w, dtype=np.float64)[:, r:r + 1]
+        y = y + wr * o[sr[:, r]]
+    return bf16_round(y, rounding)
+
+
+# ----------------------------------------------------------------------------
+# Whole layer.
+# ----------------------------------------------------------------------------
+def layer_fwd(x, w_gate, bias, W1, W3, W2, R, rounding=True,
+              forced_idx=None, forced_w=None):
+    """Forward pass of the MoE layer: route -> dispatch -> expert FFN -> combine.
+
+    ``forced_idx``/``forced_w`` replace the router's choice (used to compare the
+    later stages with a GPU run whose routing is fixed).  Returns a dict of all
+    intermediates; bf16 tensors are float64 arrays holding bf16 values.
+    """
+    x = np.asarray(x)
+    T = x.shape[0]
+    E = W1.shape[0]
+    logits = gate_logits(x, w_gate, bias, rounding)
+    if forced_idx is None:
+        idx, w = route_topk(logits, R)
+    else:
+        idx, w = np.asarray(forced_idx, np.int32), np.asarray(forced_w)
+    counts, offsets, row_slot, slot_row = dispatch_plan(idx, E)
+    x_perm = permute_rows(x, row_slot, R)
+    a, b, h, o = expert_ffn(x_perm, offsets, W1, W3, W2, rounding)
+    y = combine(o, slot_row, w, T, R, rounding)
+    return dict(logits=logits, idx=idx, w=w, counts=counts, offsets=offsets,
+                row_slot=row_slot, slot_row=slot_row, x_perm=x_perm, a=a, b=b, h=h, o=o, y=y)
+
+
+def layer_bwd(fwd, x, w_gate, W1, W3, W2, dy, R, rounding=True):
+    """Backward pass for L = sum(y * g) with dy = g (bf16 bits or float64 values).
+
+    Per token t and slot r (row = slot_row[t*R+r], expert e = idx[t,r]):
+        dw[t,r]   = <dy_t, o_row>
+        do_row    = bf16(w[t,r] * dy_t)
+    Per expert e (rows of e), with a_s = bf16(a), b_s = bf16(b) as saved:
+        dh        = do W2[e]                                  (no rounding)
+        da        = bf16(dh * b_s * silu'(a_s)),  silu'(a) = s(a) (1 + a (1 - s(a)))
+        db        = bf16(dh * silu(a_s))
+        dx_perm   = bf16(da W1[e] + db W3[e])
+        dW2[e]    = do^T h,  dW1[e] = da^T x_perm,  dW3[e] = db^T x_perm
+    Router (softmax over the chosen logits; unchosen logits get no gradient):
+        dlogits[t, idx[t,q]] = w_q (dw_q - sum_r w_r dw_r)
+        dW_g      = x^T dlogits
+        dx_t      = bf16( sum_r dx_perm[row(t,r)] + dlogits_t W_g^T )
+    Returns dict with dx, dW_gate, dW1, dW3, dW2 (float64) and intermediates.
+    """
+    x = values(x)
+    dy = values(dy)
+    T = x.shape[0]
+    E = W1.shape[0]
+    idx, w = fwd["idx"], fwd["w"].astype(np.float64)
+    offsets, slot_row = fwd["offsets"], fwd["slot_row"]
+    sr = np.asarray(slot_row).reshape(T, R)
+    o = fwd["o"]
+    N = o.shape[0]
+    d = o.shape[1]
+    f = fwd["h"].shape[1]
+
+    dw = np.zeros((T, R))
+    do = np.zeros((N, d))
+    for r in range(R):
+        rows = sr[:, r]
+        dw[:, r] = np.sum(dy * o[rows], axis=1)
+        do[rows] = bf16_round(w[:, r:r + 1] * dy, rounding)
+
+    a_s = bf16_round(fwd["a"], rounding)
+    b_s = bf16_round(fwd["b"], rounding)
+    h = fwd["h"]
+    x_perm = values(fwd["x_perm"])
+    dx_perm = np.zeros((N, d))
+    da = np.zeros((N, f))
+    db = np.zeros((N, f))
+    dW1 = np.zeros((E, f, d))
+    dW3 = np.zeros((E, f, d))
+    dW2 = np.zeros((E, d, f))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r0 == r1:
+            continue
+        w1 = values(W1[e])
+        w3 = values(W3[e])
+        w2 = values(W2[e])
+        dh = do[r0:r1] @ w2
+        sg = 1.0 / (1.0 + np.exp(-a_s[r0:r1]))
+        dsilu = sg * (1.0 + a_s[r0:r1] * (1.0 - sg))
+        da_e = bf16_round(dh * b_s[r0:r1] * dsilu, rounding)
+        db_e = bf16_round(dh * a_s[r0:r1] * sg, rounding)
+        dx_perm[r0:r1] = bf16_round(da_e @ w1 + db_e @ w3, rounding)
+        dW2[e] = do[r0:r1].T @ h[r0:r1]
+        dW1[e] = da_e.T @ x_perm[r0:r1]
+        dW3[e] = db_e.T @ x_perm[r0:r1]
+        da[r0:r1], db[r0:r1] = da_e, db_e
+
+    wdw = np.sum(w * dw, axis=1, keepdims=True)
+    dsel = w * (dw - wdw)
+    dlogits = np.zeros((T, E))
+    np.put_along_axis(dlogits, np.asarray(idx, np.int64), dsel, axis=1)
+    wg = np.asarray(w_gate, dtype=np.float64)
+    dW_gate = x.T @ dlogits
+    dx = np.zeros((T, d))
+    for r in range(R):
+        dx = dx + dx_perm[sr[:, r]]
+    dx = bf16_round(dx + dlogits @ wg.T, rounding)
+    return dict(dx=dx, dW_gate=dW_gate, dW1=dW1, dW3=dW3, dW2=dW2, dw=dw, do=do,
+                da=da, db=db, dx_perm=dx_perm, dlogits=dlogits)
+
+
+def loss(y, g):
+    """L = sum(y * g) in float64."""
+    return float(np.sum(np.asarray(y, np.float64) * np.asarray(g, np.float64)))

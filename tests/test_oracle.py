@@ -1,0 +1,367 @@
+"""Pins for the CPU oracle, against facts that do not come from the oracle itself.
+
+Each test ties one oracle function to something independent of it: the IEEE
+definition of bf16 rounding (hand-derived cases and torch's own conversion),
+brute-force enumeration of expert subsets, closed-form router weights, a
+textbook triple loop for the SwiGLU FFN, torch fp64 autograd and central finite
+differences for the backward, and the exact identity round trip of
+dispatch + combine.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16_bits_of(vals):
+    return torch.tensor(np.asarray(vals, dtype=np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------- bf16 rounding
+def test_bf16_golden_cases():
+    with open(os.path.join(GOLD, "bf16_rounding.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for src, dst, note in cases:
+        v = eval(src, {"inf": math.inf})
+        want = eval(dst, {"inf": math.inf})
+        got = float(O.bf16_round(np.array([v]))[0])
+        assert got == want, (src, dst, got, note)
+
+
+def test_bf16_matches_torch_conversion_on_fp32_values():
+    # torch rounds fp32 -> bf16 to nearest even; every fp32 value is exact in
+    # float64, so the oracle's direct rounding must agree bit for bit.
+    r = _rng(1)
+    parts = [
+        r.standard_normal(200000).astype(np.float32),
+        (r.standard_normal(50000) * 1e30).astype(np.float32),
+        (r.standard_normal(50000) * 1e-38).astype(np.float32),       # subnormal range
+        r.integers(0, 2 ** 32, 200000, dtype=np.uint64).astype(np.uint32).view(np.float32),
+    ]
+    f = np.concatenate(parts)
+    f = f[np.isfinite(f)]
+    # exact ties: random bf16 values plus half an ulp
+    base = _bf16_bits_of(r.standard_normal(20000)).astype(np.uint32) << 16
+    ties = (base | 0x8000).view(np.float32)
+    f = np.concatenate([f, ties])
+    want = torch.tensor(f).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.bf16_round(f.astype(np.float64))
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), f[~same][:10]
+
+
+def test_bf16_bits_roundtrip():
+    bits = np.arange(0, 2 ** 16, dtype=np.uint32).astype(np.uint16)
+    v = O.bf16_to_f64(bits)
+    fin = np.isfinite(v)
+    assert np.array_equal(O.bf16_round(v[fin]), v[fin])
+    assert np.array_equal(O.f64_to_bf16_bits(v[fin]), bits[fin])
+
+
+# ---------------------------------------------------------------- gate logits
+def test_gate_logits_exact_sum_brute_force():
+    r = _rng(2)
+    T, d, E = 5, 37, 6
+    x = _bf16_bits_of(r.standard_normal((T, d)))
+    wg = (r.standard_normal((d, E)) * 0.3).astype(np.float32)
+    bias = r.standard_normal(E).astype(np.float32)
+    got = O.gate_logits(x, wg, bias)
+    xv = O.bf16_to_f64(x)
+    for t in range(T):
+        for e in range(E):
+            # products of a bf16 and an fp32 value are exact in float64
+            s = math.fsum([xv[t, k] * float(wg[k, e]) for k in range(d)] + [float(bias[e])])
+            assert got[t, e] == np.float32(s)
+
+
+# ---------------------------------------------------------------- routing
+def _brute_topk(l, R):
+    """The unique R-subset whose members all beat every non-member under
+    (value desc, index asc); listed in that order."""
+    E = len(l)
+
+    def beats(i, j):
+        return l[i] > l[j] or (l[i] == l[j] and i < j)
+
+    found = []
+    for S in itertools.combinations(range(E), R):
+        rest = [j for j in range(E) if j not in S]
+        if all(beats(i, j) for i in S for j in rest):
+            found.append(S)
+    assert len(found) == 1
+    S = list(found[0])
+    for a in range(R):                       # selection sort by the same order
+        for b in range(a + 1, R):
+            if beats(S[b], S[a]):
+                S[a], S[b] = S[b], S[a]
+    return S
+
+
+@pytest.mark.parametrize("E,R", [(4, 1), (5, 2), (6, 3), (8, 2), (8, 8)])
+def test_route_brute_force_with_ties(E, R):
+    r = _rng(3 + E * 10 + R)
+    T = 64
+    logits = r.integers(-2, 3, (T, E)).astype(np.float32)    # many exact ties
+    idx, w = O.route_topk(logits, R)
+    for t in range(T):
+        S = _brute_topk([float(v) for v in logits[t]], R)
+        assert list(idx[t]) == S
+        ex = np.array([math.exp(float(logits[t, i]) - float(logits[t, S[0]])) for i in S])
+        np.testing.assert_allclose(w[t], ex / ex.sum(), rtol=1e-6)
+
+
+def test_route_golden_closed_forms():
+    with open(os.path.join(GOLD, "route_cases.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for c in cases:
+        l = np.array([c["logits"]], dtype=np.float32)
+        idx, w = O.route_topk(l, c["R"])
+        assert list(idx[0]) == c["idx"], c["note"]
+        np.testing.assert_allclose(w[0], c["w"], rtol=2e-7, atol=1e-8, err_msg=c["note"])
+
+
+def test_route_full_softmax_when_R_equals_E():
+    from scipy.special import softmax
+    r = _rng(4)
+    logits = (r.standard_normal((50, 7)) * 3).astype(np.float32)
+    idx, w = O.route_topk(logits, 7)
+    full = softmax(logits.astype(np.float64), axis=1)
+    np.testing.assert_allclose(w, np.take_along_axis(full, idx.astype(np.int64), 1), rtol=1e-6)
+
+
+def test_route_invariants():
+    r = _rng(5)
+    logits = r.standard_normal((500, 64)).astype(np.float32)
+    idx, w = O.route_topk(logits, 6)
+    assert all(len(set(row)) == 6 for row in idx.tolist())
+    np.testing.assert_allclose(w.astype(np.float64).sum(1), 1.0, atol=1e-6)
+    assert (np.diff(w, axis=1) <= 0).all()
+    assert (w > 0).all()
+    idx1, w1 = O.route_topk(logits, 1)
+    assert (w1 == 1.0).all() and np.array_equal(idx1[:, 0], logits.argmax(1))
+
+
+# ---------------------------------------------------------------- dispatch
+def test_dispatch_plan_brute_force():
+    r = _rng(6)
+    T, E, R = 97, 11, 3
+    idx = np.stack([r.choice(E, R, replace=False) for _ in range(T)]).astype(np.int32)
+    counts, offsets, row_slot, slot_row = O.dispatch_plan(idx, E)
+    rows = []
+    for e in range(E):                      # stable counting sort by hand
+        for t in range(T):
+            for q in range(R):
+                if idx[t, q] == e:
+                    rows.append(t * R + q)
+    assert list(row_slot) == rows
+    assert counts.sum() == T * R and offsets[-1] == T * R and offsets[0] == 0
+    assert all(offsets[e + 1] - offsets[e] == counts[e] for e in range(E))
+    assert np.array_equal(slot_row[row_slot], np.arange(T * R))
+    assert np.array_equal(row_slot[slot_row], np.arange(T * R))
+    for e in range(E):
+        seg = row_slot[offsets[e]:offsets[e + 1]]
+        assert (idx.reshape(-1)[seg] == e).all()
+        assert (np.diff(seg // R) > 0).all()          # ascending tokens
+
+
+def test_permute_rows_bit_copy():
+    r = _rng(7)
+    T, E, R, d = 40, 5, 2, 16
+    x = _bf16_bits_of(r.standard_normal((T, d)))
+    idx = np.stack([r.choice(E, R, replace=False) for _ in range(T)]).astype(np.int32)
+    _, _, row_slot, _ = O.dispatch_plan(idx, E)
+    xp = O.permute_rows(x, row_slot, R)
+    for row in range(T * R):
+        assert np.array_equal(xp[row], x[row_slot[row] // R])
+
+
+def test_dispatch_empty_experts_and_all_rows_one_expert():
+    idx = np.zeros((9, 1), dtype=np.int32)
+    counts, offsets, row_slot, slot_row = O.dispatch_plan(idx, 4)
+    assert list(counts) == [9, 0, 0, 0] and list(offsets) == [0, 9, 9, 9, 9]
+    assert list(row_slot) == list(range(9))
+    counts, offsets, row_slot, _ = O.dispatch_plan(np.zeros((0, 2), np.int32), 3)
+    assert list(offsets) == [0, 0, 0, 0] and row_slot.size == 0
+
+
+# ---------------------------------------------------------------- expert FFN
+def _textbook_swiglu(x, w1, w3, w2):
+    """Dense SwiGLU by triple loops: o = (silu(x w1^T) * (x w3^T)) w2^T, no rounding."""
+    M, d = len(x), len(x[0])
+    f = len(w1)
+    o = [[0.0] * d for _ in range(M)]
+    for m in range(M):
+        h = []
+        for j in range(f):
+            a = sum(x[m][k] * w1[j][k] for k in range(d))
+            b = sum(x[m][k] * w3[j][k] for k in range(d))
+            h.append(a / (1.0 + math.exp(-a)) * b)
+        for i in range(d):
+            o[m][i] = sum(h[j] * w2[i][j] for j in range(f))
+    return o
+
+
+def test_expert_ffn_single_expert_is_dense_swiglu():
+    r = _rng(8)
+    M, d, f = 3, 8, 5
+    x = r.standard_normal((M, d))
+    w1 = r.standard_normal((1, f, d)) * 0.5
+    w3 = r.standard_normal((1, f, d)) * 0.5
+    w2 = r.standard_normal((1, d, f)) * 0.5
+    _, _, _, o = O.expert_ffn(x, np.array([0, M]), w1, w3, w2, rounding=False)
+    want = _textbook_swiglu(x.tolist(), w1[0].tolist(), w3[0].tolist(), w2[0].tolist())
+    np.testing.assert_allclose(o, want, rtol=1e-12, atol=1e-12)
+
+
+def test_expert_ffn_matches_torch_per_expert_with_rounding():
+    r = _rng(9)
+    E, d, f = 3, 24, 16
+    counts = [5, 0, 7]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    N = offsets[-1]
+    xb = _bf16_bits_of(r.standard_normal((N, d)))
+    W1 = _bf16_bits_of(r.standard_normal((E, f, d)) * 0.2)
+    W3 = _bf16_bits_of(r.standard_normal((E, f, d)) * 0.2)
+    W2 = _bf16_bits_of(r.standard_normal((E, d, f)) * 0.2)
+    a, b, h, o = O.expert_ffn(xb, offsets, W1, W3, W2)
+    tx = torch.tensor(O.bf16_to_f64(xb))
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        s = slice(offsets[e], offsets[e + 1])
+        ta = tx[s] @ torch.tensor(O.bf16_to_f64(W1[e])).T
+        tb = tx[s] @ torch.tensor(O.bf16_to_f64(W3[e])).T
+        th = (torch.nn.functional.silu(ta) * tb).to(torch.bfloat16).to(torch.float64)
+        to = (th @ torch.tensor(O.bf16_to_f64(W2[e])).T).to(torch.bfloat16).to(torch.float64)
+        np.testing.assert_allclose(a[s], ta.numpy(), rtol=1e-12, atol=1e-12)
+        # torch rounds float64 -> bf16 through its own path; allow the rare
+        # one-ulp double-rounding difference only
+        np.testing.assert_allclose(h[s], th.numpy(), rtol=2 ** -7, atol=0)
+        np.testing.assert_allclose(o[s], to.numpy(), rtol=2 ** -7, atol=0)
+        assert np.mean(h[s] == th.numpy()) > 0.99 and np.mean(o[s] == to.numpy()) > 0.99
+
+
+# ---------------------------------------------------------------- combine
+def test_identity_experts_roundtrip_is_exact():
+    # combine(dispatch(x)) == x because the gate weights sum to 1
+    r = _rng(10)
+    T, d, E, R = 300, 64, 16, 4
+    x = _bf16_bits_of(r.standard_normal((T, d)))
+    logits = r.standard_normal((T, E)).astype(np.float32)
+    idx, w = O.route_topk(logits, R)
+    _, _, row_slot, slot_row = O.dispatch_plan(idx, E)
+    xp = O.permute_rows(x, row_slot, R)
+    y = O.combine(O.bf16_to_f64(xp), slot_row, w, T, R)
+    assert np.array_equal(y, O.bf16_to_f64(x))
+
+
+def test_combine_equal_outputs_and_unweighted():
+    T, R, d = 6, 3, 5
+    o = np.full((T * R, d), 0.375)
+    slot_row = np.arange(T * R)[::-1].copy()
+    w = np.full((T, R), 1.0 / 3, dtype=np.float32)
+    np.testing.assert_array_equal(O.combine(o, slot_row, w, T, R), np.full((T, d), 0.375))
+    np.testing.assert_array_equal(O.combine(o, slot_row, None, T, R), np.full((T, d), 1.125))
+
+
+# ---------------------------------------------------------------- backward
+def _tiny_layer(seed, T=6, d=8, E=4, R=2, f=6):
+    r = _rng(seed)
+    x = r.standard_normal((T, d))
+    wg = r.standard_normal((d, E)) * 0.3
+    bias = np.arange(E)[::-1] * 4.0          # wide router margins: routing is stable
+    W1 = r.standard_normal((E, f, d)) * 0.4
+    W3 = r.standard_normal((E, f, d)) * 0.4
+    W2 = r.standard_normal((E, d, f)) * 0.4
+    g = r.standard_normal((T, d))
+    return x, wg, bias, W1, W3, W2, g, R
+
+
+def _loss(params, R):
+    x, wg, bias, W1, W3, W2, g = params
+    fw = O.layer_fwd(x, wg, bias, W1, W3, W2, R, rounding=False)
+    return O.loss(fw["y"], g), fw
+
+
+def test_backward_matches_finite_differences():
+    x, wg, bias, W1, W3, W2, g, R = _tiny_layer(11)
+    # a ragged routing with an unused expert: bias ranks experts 0 > 1 > 2 > 3
+    L0, fw = _loss((x, wg, bias, W1, W3, W2, g), R)
+    bw = O.layer_bwd(fw, x, wg, W1, W3, W2, g, R, rounding=False)
+    r = _rng(12)
+    grads = {"x": bw["dx"], "wg": bw["dW_gate"], "W1": bw["dW1"], "W3": bw["dW3"],
+             "W2": bw["dW2"]}
+    base = {"x": x, "wg": wg, "W1": W1, "W3": W3, "W2": W2}
+    eps = 1e-6
+    for name, val in base.items():
+        for _ in range(3):
+            v = r.standard_normal(val.shape)
+            p = dict(base)
+            p[name] = val + eps * v
+            Lp, fp = _loss((p["x"], p["wg"], bias, p["W1"], p["W3"], p["W2"], g), R)
+            p[name] = val - eps * v
+            Lm, fm = _loss((p["x"], p["wg"], bias, p["W1"], p["W3"], p["W2"], g), R)
+            assert np.array_equal(fp["idx"], fw["idx"]) and np.array_equal(fm["idx"], fw["idx"])
+            fd = (Lp - Lm) / (2 * eps)
+            an = float(np.sum(grads[name] * v))
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_backward_matches_torch_autograd():
+    x, wg, bias, W1, W3, W2, g, R = _tiny_layer(13, T=9, d=10, E=5, R=3, f=7)
+    fw = O.layer_fwd(x, wg, bias, W1, W3, W2, R, rounding=False)
+    bw = O.layer_bwd(fw, x, wg, W1, W3, W2, g, R, rounding=False)
+    idx = torch.tensor(fw["idx"], dtype=torch.int64)
+    tx, twg = torch.tensor(x, requires_grad=True), torch.tensor(wg, requires_grad=True)
+    tW1, tW3, tW2 = (torch.tensor(a, requires_grad=True) for a in (W1, W3, W2))
+    logits = tx @ twg + torch.tensor(bias)
+    wsel = torch.softmax(torch.gather(logits, 1, idx), dim=1)
+    y = torch.zeros_like(tx)
+    for q in range(R):
+        e = idx[:, q]
+        a = torch.einsum("td,tfd->tf", tx, tW1[e])
+        b = torch.einsum("td,tfd->tf", tx, tW3[e])
+        o = torch.einsum("tf,tdf->td", torch.nn.functional.silu(a) * b, tW2[e])
+        y = y + wsel[:, q:q + 1] * o
+    (y * torch.tensor(g)).sum().backward()
+    np.testing.assert_allclose(bw["dx"], tx.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(bw["dW_gate"], twg.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(bw["dW1"], tW1.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(bw["dW3"], tW3.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(bw["dW2"], tW2.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_backward_zero_row_expert_has_zero_weight_grad():
+    x, wg, bias, W1, W3, W2, g, R = _tiny_layer(14)
+    fw = O.layer_fwd(x, wg, bias, W1, W3, W2, R, rounding=False)
+    bw = O.layer_bwd(fw, x, wg, W1, W3, W2, g, R, rounding=False)
+    unused = [e for e in range(W1.shape[0]) if fw["counts"][e] == 0]
+    assert unused, "bias should leave the lowest-ranked experts unused"
+    for e in unused:
+        assert not bw["dW1"][e].any() and not bw["dW3"][e].any() and not bw["dW2"][e].any()
+        assert not bw["dW_gate"][:, e].any()
+
+
+def test_backward_rounding_points_applied():
+    # with rounding on, every declared bf16 storage point holds bf16 values
+    x, wg, bias, W1, W3, W2, g, R = _tiny_layer(15)
+    xb = O.bf16_round(x)
+    fw = O.layer_fwd(xb, wg, bias, W1, W3, W2, R)
+    bw = O.layer_bwd(fw, xb, wg, W1, W3, W2, O.bf16_round(g), R)
+    for key in ("y", "h", "o"):
+        assert np.array_equal(fw[key], O.bf16_round(fw[key]))
+    for key in ("dx", "do", "da", "db", "dx_perm"):
+        assert np.array_equal(bw[key], O.bf16_round(bw[key]))
