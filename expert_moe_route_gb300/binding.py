@@ -1,0 +1,260 @@
+"""Thin ctypes binding of libmoe.so (include/moe.h), same names as the C ABI.
+
+Only argument marshalling lives here: torch tensors supply device pointers and
+the current CUDA stream; every step of the MoE layer runs in the library's
+CUDA kernels.  There is no fallback: if the library cannot be built or loaded,
+importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_LOGITS_IN = 0x1
+MOE_CHECK = 0x2
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CUDA"}
+
+# the C ABI's exported symbols (checked against include/moe.h by the tests)
+SYMBOLS = ("moe_status_string", "moe_version", "moe_route", "moe_dispatch", "moe_grouped_ffn",
+           "moe_combine", "moe_layer_fwd", "moe_layer_bwd")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_u = ctypes.c_uint
+_szp = ctypes.POINTER(ctypes.c_size_t)
+
+
+class moe_layer_t(ctypes.Structure):
+    _fields_ = [("T", _i), ("d", _i), ("E", _i), ("R", _i), ("f", _i), ("w_gate", _vp),
+                ("bias", _vp), ("W1", _vp), ("W3", _vp), ("W2", _vp)]
+
+
+class moe_saved_t(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("logits", "topk_idx", "topk_w", "counts", "offsets", "row_slot",
+                                   "slot_row", "x_perm", "a", "b", "h", "o")]
+
+
+def _declare(lib):
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_status_string.argtypes = [_i]
+    lib.moe_version.restype = _i
+    lib.moe_version.argtypes = []
+    lib.moe_route.restype = _i
+    lib.moe_route.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _u, _vp]
+    lib.moe_dispatch.restype = _i
+    lib.moe_dispatch.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _szp, _u,
+                                 _vp]
+    lib.moe_grouped_ffn.restype = _i
+    lib.moe_grouped_ffn.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _vp, _szp, _u, _vp]
+    lib.moe_combine.restype = _i
+    lib.moe_combine.argtypes = [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]
+    lib.moe_layer_fwd.restype = _i
+    lib.moe_layer_fwd.argtypes = [ctypes.POINTER(moe_layer_t), _vp, _vp,
+                                  ctypes.POINTER(moe_saved_t), _vp, _szp, _u, _vp]
+    lib.moe_layer_bwd.restype = _i
+    lib.moe_layer_bwd.argtypes = [ctypes.POINTER(moe_layer_t), _vp, ctypes.POINTER(moe_saved_t),
+                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _szp, _u, _vp]
+
+
+_LIB = None
+
+
+def lib():
+    """The loaded library (built in-tree on first use)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        handle = ctypes.CDLL(path)
+        _declare(handle)
+        _LIB = handle
+    return _LIB
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+# ---------------------------------------------------------------- marshalling
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(st, where):
+    if st != MOE_OK:
+        raise MoeError(st, where)
+
+
+def _dt(t, dtype, name):
+    if t is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# ---------------------------------------------------------------- entry points
+def moe_route(x, w_gate, bias, logits, topk_idx, topk_w, flags=0, stream=None):
+    T, E = logits.shape
+    R = topk_idx.shape[1]
+    d = x.shape[1] if x is not None else 0
+    _dt(x, torch.bfloat16, "x"); _dt(w_gate, torch.float32, "w_gate"); _dt(bias, torch.float32, "bias")
+    _dt(logits, torch.float32, "logits"); _dt(topk_idx, torch.int32, "topk_idx")
+    _dt(topk_w, torch.float32, "topk_w")
+    st = lib().moe_route(_p(x), _p(w_gate), _p(bias), T, d, E, R, _p(logits), _p(topk_idx),
+                         _p(topk_w), flags, _stream(stream))
+    _check(st, "moe_route")
+
+
+def dispatch_ws_bytes(T, d, E, R) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_dispatch(None, None, T, d, E, R, None, None, None, None, None, None,
+                              ctypes.byref(n), 0, None), "moe_dispatch(ws query)")
+    return n.value
+
+
+def moe_dispatch(x, topk_idx, E, counts, offsets, row_slot, slot_row, x_perm, ws, flags=0,
+                 stream=None):
+    T, R = topk_idx.shape
+    d = x.shape[1] if x is not None else (x_perm.shape[1] if x_perm is not None else 8)
+    _dt(x, torch.bfloat16, "x"); _dt(x_perm, torch.bfloat16, "x_perm")
+    for name, t in (("topk_idx", topk_idx), ("counts", counts), ("offsets", offsets),
+                    ("row_slot", row_slot), ("slot_row", slot_row)):
+        _dt(t, torch.int32, name)
+    n = ctypes.c_size_t(ws.numel())
+    st = lib().moe_dispatch(_p(x), _p(topk_idx), T, d, E, R, _p(counts), _p(offsets),
+                            _p(row_slot), _p(slot_row), _p(x_perm), _p(ws), ctypes.byref(n),
+                            flags, _stream(stream))
+    _check(st, "moe_dispatch")
+
+
+def grouped_ffn_ws_bytes(N, d, f, E) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_grouped_ffn(None, None, N, d, f, E, None, None, None, None, None, None, None,
+                                 None, ctypes.byref(n), 0, None), "moe_grouped_ffn(ws query)")
+    return n.value
+
+
+def moe_grouped_ffn(x_perm, offsets, W1, W3, W2, h, out, ws, a_save=None, b_save=None, flags=0,
+                    stream=None):
+    N, d = x_perm.shape
+    E, f, _ = W1.shape
+    for name, t in (("x_perm", x_perm), ("W1", W1), ("W3", W3), ("W2", W2), ("h", h),
+                    ("out", out), ("a_save", a_save), ("b_save", b_save)):
+        _dt(t, torch.bfloat16, name)
+    _dt(offsets, torch.int32, "offsets")
+    n = ctypes.c_size_t(ws.numel())
+    st = lib().moe_grouped_ffn(_p(x_perm), _p(offsets), N, d, f, E, _p(W1), _p(W3), _p(W2),
+                               _p(a_save), _p(b_save), _p(h), _p(out), _p(ws), ctypes.byref(n),
+                               flags, _stream(stream))
+    _check(st, "moe_grouped_ffn")
+
+
+def moe_combine(expert_out, slot_row, topk_w, y, R, stream=None):
+    T, d = y.shape
+    _dt(expert_out, torch.bfloat16, "expert_out"); _dt(y, torch.bfloat16, "y")
+    _dt(slot_row, torch.int32, "slot_row"); _dt(topk_w, torch.float32, "topk_w")
+    st = lib().moe_combine(_p(expert_out), _p(slot_row), _p(topk_w), T, d, R, _p(y),
+                           _stream(stream))
+    _check(st, "moe_combine")
+
+
+# ---------------------------------------------------------------- layer
+class Layer:
+    """Parameters of one MoE layer (device tensors) and their C struct."""
+
+    def __init__(self, w_gate, bias, W1, W3, W2, R, T):
+        self.w_gate, self.bias, self.W1, self.W3, self.W2 = w_gate, bias, W1, W3, W2
+        self.E, self.f, self.d = W1.shape
+        self.R, self.T = R, T
+        self.c = moe_layer_t(T, self.d, self.E, R, self.f, _p(w_gate), _p(bias), _p(W1), _p(W3),
+                             _p(W2))
+
+    def with_tokens(self, T):
+        return Layer(self.w_gate, self.bias, self.W1, self.W3, self.W2, self.R, T)
+
+
+class Saved:
+    """Caller-owned forward intermediates (allocated here with torch)."""
+
+    def __init__(self, layer: Layer, device, train=True):
+        T, d, E, R, f = layer.T, layer.d, layer.E, layer.R, layer.f
+        N = T * R
+        z = dict(device=device)
+        self.logits = torch.empty((T, E), dtype=torch.float32, **z)
+        self.topk_idx = torch.empty((T, R), dtype=torch.int32, **z)
+        self.topk_w = torch.empty((T, R), dtype=torch.float32, **z)
+        self.counts = torch.empty((E,), dtype=torch.int32, **z)
+        self.offsets = torch.empty((E + 1,), dtype=torch.int32, **z)
+        self.row_slot = torch.empty((N,), dtype=torch.int32, **z)
+        self.slot_row = torch.empty((N,), dtype=torch.int32, **z)
+        self.x_perm = torch.empty((N, d), dtype=torch.bfloat16, **z)
+        self.a = torch.empty((N, f), dtype=torch.bfloat16, **z) if train else None
+        self.b = torch.empty((N, f), dtype=torch.bfloat16, **z) if train else None
+        self.h = torch.empty((N, f), dtype=torch.bfloat16, **z)
+        self.o = torch.empty((N, d), dtype=torch.bfloat16, **z)
+        self.c = moe_saved_t(*[_p(getattr(self, n)) for n, _ in moe_saved_t._fields_])
+
+
+def layer_fwd_ws_bytes(layer: Layer) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_layer_fwd(ctypes.byref(layer.c), None, None, None, None, ctypes.byref(n), 0,
+                               None), "moe_layer_fwd(ws query)")
+    return n.value
+
+
+def layer_bwd_ws_bytes(layer: Layer) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_layer_bwd(ctypes.byref(layer.c), None, None, None, None, None, None, None,
+                               None, None, ctypes.byref(n), 0, None), "moe_layer_bwd(ws query)")
+    return n.value
+
+
+def workspace(nbytes: int, device="cuda"):
+    """A device byte buffer for the workspace arguments (torch allocates it)."""
+    return torch.empty((max(int(nbytes), 256),), dtype=torch.uint8, device=device)
+
+
+def moe_layer_fwd(layer: Layer, x, y, saved: Saved, ws, flags=0, stream=None):
+    n = ctypes.c_size_t(ws.numel())
+    st = lib().moe_layer_fwd(ctypes.byref(layer.c), _p(x), _p(y), ctypes.byref(saved.c), _p(ws),
+                             ctypes.byref(n), flags, _stream(stream))
+    _check(st, "moe_layer_fwd")
+
+
+def moe_layer_bwd(layer: Layer, x, saved: Saved, dy, dx, dW_gate, dW1, dW3, dW2, ws, flags=0,
+                  stream=None):
+    n = ctypes.c_size_t(ws.numel())
+    st = lib().moe_layer_bwd(ctypes.byref(layer.c), _p(x), ctypes.byref(saved.c), _p(dy), _p(dx),
+                             _p(dW_gate), _p(dW1), _p(dW3), _p(dW2), _p(ws), ctypes.byref(n),
+                             flags, _stream(stream))
+    _check(st, "moe_layer_bwd")
+
+
+def status_string(st: int) -> str:
+    return lib().moe_status_string(st).decode()
+
+
+def loaded_path() -> str:
+    return os.path.realpath(_build.LIB)

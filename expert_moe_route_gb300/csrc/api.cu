@@ -1,0 +1,294 @@
+// C ABI of the MoE layer hot path (declared in include/moe.h): argument
+// checks, workspace layout, kernel sequencing on the caller's stream.
+#include <stdio.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kErrBytes = 256;   // device error word, at the start of every workspace
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+inline cudaStream_t S(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+moe_status_t shape_check(int T, int d, int E, int R) {
+  if (T < 0 || d <= 0 || E <= 0 || R <= 0) return MOE_ERR_INVALID_ARG;
+  if (R > E) return MOE_ERR_INVALID_ARG;
+  if (R > 32 || E > 1024 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((long long)T * R >= (1LL << 31) || (long long)T * d >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool init_once() {
+  static int done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev < 0 || dev >= 64) return false;
+  if (!done[dev]) {
+    if (dispatch_set_smem_limits() != cudaSuccess) return false;
+    done[dev] = 1;
+  }
+  return true;
+}
+
+// Optionally wait for the stream and translate the device error word.
+moe_status_t finish(cudaError_t launched, const int* err_dev, unsigned flags, cudaStream_t s) {
+  if (launched != cudaSuccess) return MOE_ERR_CUDA;
+  if (!(flags & MOE_CHECK)) return MOE_OK;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!err_dev) return MOE_OK;
+  int h = 0;
+  if (cudaMemcpy(&h, err_dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (h & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (h & kErrBadRouting) return MOE_ERR_BAD_ROUTING;
+  return MOE_OK;
+}
+
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    void* p = base ? base + off : nullptr;
+    off += align_up(bytes, 256);
+    return p;
+  }
+};
+
+#define MOE_TRY(expr)                        \
+  do {                                       \
+    cudaError_t e_ = (expr);                 \
+    if (e_ != cudaSuccess) return finish(e_, nullptr, 0, nullptr); \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_BAD_ROUTING: return "MOE_ERR_BAD_ROUTING";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+  }
+  return "unknown moe_status_t";
+}
+
+int moe_version(void) { return 100; }
+
+moe_status_t moe_route(const uint16_t* x, const float* w_gate, const float* bias, int T, int d,
+                       int E, int R, float* logits, int32_t* topk_idx, float* topk_w,
+                       unsigned flags, moe_stream_t stream) {
+  const bool logits_in = flags & MOE_LOGITS_IN;
+  if (logits_in) {
+    if (T < 0 || E <= 0 || R <= 0 || R > E) return MOE_ERR_INVALID_ARG;
+    if (R > 32 || E > 1024) return MOE_ERR_UNSUPPORTED;
+  } else {
+    moe_status_t st = shape_check(T, d, E, R);
+    if (st != MOE_OK) return st;
+  }
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!logits_in) {
+    if (!x || !w_gate) return MOE_ERR_INVALID_ARG;
+    if (!al16(x)) return MOE_ERR_UNSUPPORTED;
+  }
+  if (!init_once()) return MOE_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  if (!logits_in) MOE_TRY(launch_gate_logits(x, w_gate, bias, T, d, E, logits, s));
+  return finish(launch_topk(logits, T, E, R, topk_idx, topk_w, s), nullptr, flags, s);
+}
+
+moe_status_t moe_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int R,
+                          int32_t* counts, int32_t* offsets, int32_t* row_slot, int32_t* slot_row,
+                          uint16_t* x_perm, void* ws, size_t* ws_bytes, unsigned flags,
+                          moe_stream_t stream) {
+  moe_status_t st = shape_check(T, d, E, R);
+  if (st != MOE_OK) return st;
+  if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t need = kErrBytes + dispatch_ws_bytes(T, E);
+  if (!ws) {
+    *ws_bytes = need;
+    return MOE_OK;
+  }
+  if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
+  if (!counts || !offsets || (T > 0 && (!topk_idx || !row_slot || !slot_row)))
+    return MOE_ERR_INVALID_ARG;
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (x && (!al16(x) || !al16(x_perm))) return MOE_ERR_UNSUPPORTED;
+  if (!init_once()) return MOE_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  int* err = static_cast<int*>(ws);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  cudaError_t e = launch_dispatch(x, topk_idx, T, d, E, R, counts, offsets, row_slot, slot_row,
+                                  x_perm, static_cast<uint8_t*>(ws) + kErrBytes, err, s);
+  return finish(e, err, flags, s);
+}
+
+moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
+                             int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                             uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
+                             void* ws, size_t* ws_bytes, unsigned flags, moe_stream_t stream) {
+  if (N < 0 || d <= 0 || f <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 8 || f % 8 || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t need = kErrBytes + tiles_ws_bytes(N, E);
+  if (!ws) {
+    *ws_bytes = need;
+    return MOE_OK;
+  }
+  if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
+  if (!offsets || !W1 || !W3 || !W2) return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!x_perm || !h || !out)) return MOE_ERR_INVALID_ARG;
+  if ((a_save == nullptr) != (b_save == nullptr)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {x_perm, W1, W3, W2, a_save, b_save, h, out};
+  for (const void* p : ps)
+    if (p && !al16(p)) return MOE_ERR_UNSUPPORTED;
+  if (!init_once()) return MOE_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  int* err = static_cast<int*>(ws);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  cudaError_t e = launch_ffn_fwd(x_perm, offsets, N, d, f, E, W1, W3, W2, a_save, b_save, h, out,
+                                 static_cast<uint8_t*>(ws) + kErrBytes, err, s);
+  return finish(e, err, flags, s);
+}
+
+moe_status_t moe_combine(const uint16_t* expert_out, const int32_t* slot_row, const float* topk_w,
+                         int T, int d, int R, uint16_t* y, moe_stream_t stream) {
+  if (T < 0 || d <= 0 || R <= 0) return MOE_ERR_INVALID_ARG;
+  if (R > 32 || d % 8) return MOE_ERR_UNSUPPORTED;
+  if ((long long)T * R >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!expert_out || !slot_row || !y) return MOE_ERR_INVALID_ARG;
+  if (!al16(expert_out) || !al16(y)) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = S(stream);
+  return finish(launch_combine(expert_out, slot_row, topk_w, T, d, R, y, s), nullptr, 0, s);
+}
+
+static moe_status_t check_layer(const moe_layer_t* L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = shape_check(L->T, L->d, L->E, L->R);
+  if (st != MOE_OK) return st;
+  if (L->f <= 0) return MOE_ERR_INVALID_ARG;
+  if (L->f % 8) return MOE_ERR_UNSUPPORTED;
+  if (!L->w_gate || !L->W1 || !L->W3 || !L->W2) return MOE_ERR_INVALID_ARG;
+  if (!al16(L->W1) || !al16(L->W3) || !al16(L->W2)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static size_t layer_fwd_ws(const moe_layer_t* L) {
+  const int N = L->T * L->R;
+  return kErrBytes + align_up(dispatch_ws_bytes(L->T, L->E), 256) + tiles_ws_bytes(N, L->E);
+}
+
+moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
+                           const moe_saved_t* sv, void* ws, size_t* ws_bytes, unsigned flags,
+                           moe_stream_t stream) {
+  moe_status_t st = check_layer(L);
+  if (st != MOE_OK) return st;
+  if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t need = layer_fwd_ws(L);
+  if (!ws) {
+    *ws_bytes = need;
+    return MOE_OK;
+  }
+  if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
+  if (!sv || !x || !y) return MOE_ERR_INVALID_ARG;
+  if (!sv->logits || !sv->topk_idx || !sv->topk_w || !sv->counts || !sv->offsets ||
+      !sv->row_slot || !sv->slot_row || !sv->x_perm || !sv->h || !sv->o)
+    return MOE_ERR_INVALID_ARG;
+  if ((sv->a == nullptr) != (sv->b == nullptr)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {x, y, sv->x_perm, sv->a, sv->b, sv->h, sv->o};
+  for (const void* p : ps)
+    if (p && !al16(p)) return MOE_ERR_UNSUPPORTED;
+  if (L->T == 0) return MOE_OK;
+  if (!init_once()) return MOE_ERR_CUDA;
+  const int T = L->T, d = L->d, E = L->E, R = L->R, f = L->f, N = T * R;
+  cudaStream_t s = S(stream);
+  Carve c(ws);
+  int* err = static_cast<int*>(c.take(kErrBytes));
+  void* dws = c.take(dispatch_ws_bytes(T, E));
+  void* tws = c.take(tiles_ws_bytes(N, E));
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  MOE_TRY(launch_gate_logits(x, L->w_gate, L->bias, T, d, E, sv->logits, s));
+  MOE_TRY(launch_topk(sv->logits, T, E, R, sv->topk_idx, sv->topk_w, s));
+  MOE_TRY(launch_dispatch(x, sv->topk_idx, T, d, E, R, sv->counts, sv->offsets, sv->row_slot,
+                          sv->slot_row, sv->x_perm, dws, err, s));
+  MOE_TRY(launch_ffn_fwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
+                         sv->h, sv->o, tws, err, s));
+  return finish(launch_combine(sv->o, sv->slot_row, sv->topk_w, T, d, R, y, s), err, flags, s);
+}
+
+static size_t layer_bwd_ws(const moe_layer_t* L) {
+  const size_t T = L->T, d = L->d, E = L->E, R = L->R, f = L->f, N = T * R;
+  size_t n = kErrBytes;
+  n += tiles_ws_bytes((int)N, (int)E);
+  n += align_up(N * d * 2, 256);        // do
+  n += align_up(N * 2 * f * 2, 256);    // [da | db]
+  n += align_up(N * d * 2, 256);        // dx_perm
+  n += align_up(N * 4, 256);            // dlogits per slot (token order)
+  n += align_up(N * 4, 256);            // dlogits per row
+  n += align_up(E * d * 4, 256);        // W_g^T
+  return n;
+}
+
+moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_saved_t* sv,
+                           const uint16_t* dy, uint16_t* dx, float* dW_gate, float* dW1,
+                           float* dW3, float* dW2, void* ws, size_t* ws_bytes, unsigned flags,
+                           moe_stream_t stream) {
+  moe_status_t st = check_layer(L);
+  if (st != MOE_OK) return st;
+  if (L->d % 64 || L->f % 64) return MOE_ERR_UNSUPPORTED;
+  if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t need = layer_bwd_ws(L);
+  if (!ws) {
+    *ws_bytes = need;
+    return MOE_OK;
+  }
+  if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
+  if (!sv || !x || !dy || !dx || !dW_gate || !dW1 || !dW3 || !dW2) return MOE_ERR_INVALID_ARG;
+  if (!sv->a || !sv->b || !sv->h || !sv->o || !sv->x_perm || !sv->topk_idx || !sv->topk_w ||
+      !sv->offsets || !sv->slot_row)
+    return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {x, dy, dx, dW_gate, dW1, dW3, dW2, sv->a, sv->b, sv->h, sv->o, sv->x_perm};
+  for (const void* p : ps)
+    if (!al16(p)) return MOE_ERR_UNSUPPORTED;
+  if (!init_once()) return MOE_ERR_CUDA;
+  const int T = L->T, d = L->d, E = L->E, R = L->R, f = L->f, N = T * R;
+  cudaStream_t s = S(stream);
+  Carve c(ws);
+  int* err = static_cast<int*>(c.take(kErrBytes));
+  void* tws = c.take(tiles_ws_bytes(N, E));
+  uint16_t* dO = static_cast<uint16_t*>(c.take((size_t)N * d * 2));
+  uint16_t* dab = static_cast<uint16_t*>(c.take((size_t)N * 2 * f * 2));
+  uint16_t* dxp = static_cast<uint16_t*>(c.take((size_t)N * d * 2));
+  float* dsel_tok = static_cast<float*>(c.take((size_t)N * 4));
+  float* dsel_row = static_cast<float*>(c.take((size_t)N * 4));
+  float* wgT = static_cast<float*>(c.take((size_t)E * d * 4));
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  if (N == 0) {
+    MOE_TRY(cudaMemsetAsync(dW_gate, 0, sizeof(float) * d * E, s));
+    MOE_TRY(cudaMemsetAsync(dW1, 0, sizeof(float) * E * f * d, s));
+    MOE_TRY(cudaMemsetAsync(dW3, 0, sizeof(float) * E * f * d, s));
+    return finish(cudaMemsetAsync(dW2, 0, sizeof(float) * E * f * d, s), err, flags, s);
+  }
+  MOE_TRY(launch_bwd_route(dy, sv->o, sv->slot_row, sv->topk_w, T, d, R, dO, dsel_tok, dsel_row, s));
+  MOE_TRY(launch_ffn_bwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
+                         sv->h, dO, dab, dxp, dW1, dW3, dW2, tws, err, s));
+  MOE_TRY(launch_dwg(sv->x_perm, sv->offsets, dsel_row, d, E, dW_gate, s));
+  MOE_TRY(launch_wg_transpose(L->w_gate, d, E, wgT, s));
+  return finish(launch_dx_combine(dxp, sv->slot_row, sv->topk_idx, dsel_tok, wgT, T, d, E, R, dx, s),
+                err, flags, s);
+}
+
+}  // extern "C"

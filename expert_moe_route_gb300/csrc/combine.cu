@@ -1,0 +1,68 @@
+// Combine: each token's R expert outputs come back to it and are averaged with
+// the gate weights ("Enabling trillion-parameter models on AWS EFA", sections
+// "Introduction" and "Dispatch and combine": accumulation at the receiving
+// side).  y[t] = bf16( sum_r w[t,r] * o[slot_row[t*R+r]] ), fp32 in r order.
+//
+// One warp per token.  The warp stages the token's rows and weights in shared
+// memory once, then each lane handles 16-byte vectors (8 bf16) of the hidden
+// dimension: it issues the R row loads of a vector before accumulating them
+// in order, so R independent 16-byte loads are in flight per lane.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+constexpr int CW = 8;   // warps per block
+
+__global__ void __launch_bounds__(CW * 32) combine_kernel(const uint16_t* __restrict__ o,
+                                                          const int32_t* __restrict__ slot_row,
+                                                          const float* __restrict__ w, int T,
+                                                          int d, int R, int N,
+                                                          uint16_t* __restrict__ y) {
+  __shared__ int rows_s[CW][32];
+  __shared__ float w_s[CW][32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nv = d / 8;
+  for (int t = blockIdx.x * CW + wid; t < T; t += gridDim.x * CW) {
+    if (lane < R) {
+      const int row = slot_row[(size_t)t * R + lane];
+      rows_s[wid][lane] = ((unsigned)row < (unsigned)N) ? row : -1;
+      w_s[wid][lane] = w ? w[(size_t)t * R + lane] : 1.f;
+    }
+    __syncwarp();
+    for (int v = lane; v < nv; v += 32) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int r0 = 0; r0 < R; r0 += 4) {
+        uint4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int row = (r0 + u < R) ? rows_s[wid][r0 + u] : -1;
+          q[u] = row >= 0 ? ldg_nc_v4(o + (size_t)row * d + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (r0 + u >= R) break;
+          const float wr = w_s[wid][r0 + u];
+          float f[8];
+          unpack8(q[u], f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] = fmaf(wr, f[j], acc[j]);
+        }
+      }
+      reinterpret_cast<uint4*>(y + (size_t)t * d)[v] = pack8(acc);
+    }
+    __syncwarp();
+  }
+}
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const float* w, int T,
+                           int d, int R, uint16_t* y, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = ceil_div(T, CW) < 152 * 8 ? ceil_div(T, CW) : 152 * 8;
+  combine_kernel<<<blocks, CW * 32, 0, s>>>(o, slot_row, w, T, d, R, T * R, y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,241 @@
+// Dispatch: group the T*R routed slots by expert into contiguous rows.
+// ("Enabling trillion-parameter models on AWS EFA", section "Dispatch and
+// combine": per-expert token counts, a cumulative sum of the counts for the
+// offsets that pack each expert's tokens contiguously, and the shuffle of the
+// tokens into the tensor the grouped GEMM reads.)
+//
+// Four kernels, all deterministic (no atomic decides an order):
+//   1. expert_hist:  per block of CHUNK tokens, a shared-memory histogram of its
+//      slots' experts -> blk_counts[e][b]; also flags out-of-range or repeated
+//      expert indices.
+//   2. expert_scan:  one CTA scans blk_counts in (expert, block) order ->
+//      blk_base[e][b] = offsets[e] + rows of e in earlier blocks; counts, offsets.
+//   3. slot_rank:    per block, warps walk their slots in order; __match_any_sync
+//      gives each slot its rank among equal experts of its 32-slot group, so
+//      row = blk_base + earlier warps + earlier groups + rank (stable order).
+//   4. permute_rows: one warp per token reads x[t] once (16-byte vectors) and
+//      writes it to its R rows of x_perm.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+constexpr int CHUNK = 256;     // tokens per block in hist / rank
+constexpr int DWARPS = 8;      // warps per block in hist / rank
+
+__global__ void __launch_bounds__(256) expert_hist_kernel(const int32_t* __restrict__ idx, int T,
+                                                          int E, int R, int nblk,
+                                                          int32_t* __restrict__ blk_counts,
+                                                          int* __restrict__ err) {
+  extern __shared__ int32_t cnt[];
+  const int b = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int t0 = b * CHUNK;
+  const int t1 = min(T, t0 + CHUNK);
+  const int s0 = t0 * R, s1 = t1 * R;
+  bool bad = false;
+  for (int s = s0 + threadIdx.x; s < s1; s += blockDim.x) {
+    const int e = idx[s];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+    else bad = true;
+  }
+  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {  // repeated expert in a token
+    const int32_t* row = idx + (size_t)t * R;
+    for (int i = 1; i < R; ++i) {
+      const int ei = row[i];
+      for (int j = 0; j < i; ++j) bad |= (row[j] == ei);
+    }
+  }
+  if (bad) atomicOr(err, kErrBadRouting);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blk_counts[(size_t)e * nblk + b] = cnt[e];
+}
+
+// Exclusive scan of L = E*nblk counts by one 1024-thread CTA, 4 values per thread per pass.
+__global__ void __launch_bounds__(1024) expert_scan_kernel(const int32_t* __restrict__ blk_counts,
+                                                            int E, int nblk,
+                                                            int32_t* __restrict__ blk_base,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const long long L = (long long)E * nblk;
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+  for (long long base = 0; base < L; base += 4096) {
+    int v[4];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long i = base + tid * 4 + j;
+      v[j] = i < L ? blk_counts[i] : 0;
+      sum += v[j];
+    }
+    int incl = sum;  // inclusive warp scan of per-thread sums
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int ws = warp_sums[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, ws, off);
+        if (lane >= off) ws += o;
+      }
+      warp_sums[lane] = ws;  // inclusive over warps
+    }
+    __syncthreads();
+    const int carry = carry_s;
+    int run = carry + (wid > 0 ? warp_sums[wid - 1] : 0) + incl - sum;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long i = base + tid * 4 + j;
+      if (i < L) blk_base[i] = run;
+      run += v[j];
+    }
+    __syncthreads();
+    if (tid == 0) carry_s = carry + warp_sums[31];
+    __syncthreads();
+  }
+  const int total = carry_s;
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int first = blk_base[(size_t)e * nblk];
+    const int next = (e + 1 < E) ? blk_base[(size_t)(e + 1) * nblk] : total;
+    offsets[e] = first;
+    counts[e] = next - first;
+  }
+  if (tid == 0) offsets[E] = total;
+}
+
+__global__ void __launch_bounds__(256) slot_rank_kernel(const int32_t* __restrict__ idx, int T,
+                                                        int E, int R, int nblk,
+                                                        const int32_t* __restrict__ blk_base,
+                                                        int32_t* __restrict__ row_slot,
+                                                        int32_t* __restrict__ slot_row) {
+  extern __shared__ int32_t sm[];
+  int32_t* wcnt = sm;                       // [DWARPS][E]
+  int32_t* keys = sm + DWARPS * E;          // [CHUNK*R]
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int t0 = b * CHUNK;
+  const int t1 = min(T, t0 + CHUNK);
+  const int s0 = t0 * R, ns = (t1 - t0) * R;
+  for (int i = threadIdx.x; i < DWARPS * E; i += blockDim.x) wcnt[i] = 0;
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    const int e = idx[s0 + i];
+    keys[i] = ((unsigned)e < (unsigned)E) ? e : -1;
+  }
+  __syncthreads();
+  // this warp's contiguous range of slots, in slot order
+  const int per_warp = ceil_div(ns, DWARPS * 32) * 32;
+  const int w0 = wid * per_warp;
+  const int w1 = min(ns, w0 + per_warp);
+  int32_t* my = wcnt + wid * E;
+  for (int g = w0; g < w1; g += 32) {  // pass 1: per-warp counts
+    const int i = g + lane;
+    const int e = i < w1 ? keys[i] : -1;
+    const unsigned peers = __match_any_sync(kFull, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {  // warp bases for this block
+    int run = blk_base[(size_t)e * nblk + b];
+#pragma unroll
+    for (int w = 0; w < DWARPS; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int g = w0; g < w1; g += 32) {  // pass 2: rows
+    const int i = g + lane;
+    const int e = i < w1 ? keys[i] : -1;
+    const unsigned peers = __match_any_sync(kFull, e);
+    int row = -1;
+    if (e >= 0) row = my[e] + __popc(peers & lt);
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+    __syncwarp();
+    if (i < w1) {
+      slot_row[s0 + i] = row;
+      if (row >= 0) row_slot[row] = s0 + i;
+    }
+  }
+}
+
+// One warp per token; lanes move 16-byte vectors of x[t] to the token's R rows.
+__global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __restrict__ x, int T,
+                                                           int d, int R, int N,
+                                                           const int32_t* __restrict__ slot_row,
+                                                           uint16_t* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x / 32;
+  const int nv = d / 8;
+  for (int t = blockIdx.x * warps + threadIdx.x / 32; t < T; t += gridDim.x * warps) {
+    int my_row = lane < R ? slot_row[(size_t)t * R + lane] : -1;
+    if ((unsigned)my_row >= (unsigned)N) my_row = -1;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    for (int base = 0; base < nv; base += 32 * 4) {  // warp-uniform trip count
+      const int v0 = base + lane;
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < nv) q[u] = ldg_nc_v4(src + v0 + 32 * u);
+      for (int r = 0; r < R; ++r) {
+        const int row = __shfl_sync(kFull, my_row, r);
+        if (row < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * d);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v0 + 32 * u < nv) dst[v0 + 32 * u] = q[u];
+      }
+    }
+  }
+}
+}  // namespace
+
+size_t dispatch_ws_bytes(int T, int E) {
+  const int nblk = ceil_div(T > 0 ? T : 1, CHUNK);
+  return align_up((size_t)2 * E * nblk * sizeof(int32_t), 256);
+}
+
+cudaError_t launch_dispatch(const uint16_t* x, const int32_t* idx, int T, int d, int E, int R,
+                            int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                            int32_t* slot_row, uint16_t* x_perm, void* ws, int* err,
+                            cudaStream_t s) {
+  const int nblk = ceil_div(T > 0 ? T : 1, CHUNK);
+  int32_t* blk_counts = static_cast<int32_t*>(ws);
+  int32_t* blk_base = blk_counts + (size_t)E * nblk;
+  if (T == 0) {
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+    if (e != cudaSuccess) return e;
+    return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
+  }
+  expert_hist_kernel<<<nblk, 256, E * sizeof(int32_t), s>>>(idx, T, E, R, nblk, blk_counts, err);
+  expert_scan_kernel<<<1, 1024, 0, s>>>(blk_counts, E, nblk, blk_base, counts, offsets);
+  const size_t rank_smem = sizeof(int32_t) * ((size_t)DWARPS * E + (size_t)CHUNK * R);
+  slot_rank_kernel<<<nblk, 256, rank_smem, s>>>(idx, T, E, R, nblk, blk_base, row_slot, slot_row);
+  if (x != nullptr && x_perm != nullptr) {
+    const int blocks = ceil_div(T, 8) < 152 * 8 ? ceil_div(T, 8) : 152 * 8;
+    permute_rows_kernel<<<blocks, 256, 0, s>>>(x, T, d, R, T * R, slot_row, x_perm);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t dispatch_set_smem_limits() {
+  const int max_rank_smem = sizeof(int32_t) * (DWARPS * 1024 + CHUNK * 32);
+  return cudaFuncSetAttribute(slot_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              max_rank_smem);
+}
+
+}  // namespace moe

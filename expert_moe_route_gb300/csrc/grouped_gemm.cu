@@ -1,0 +1,592 @@
+// Grouped per-expert GEMMs on the 5th-generation tensor cores (tcgen05).
+// ("Enabling trillion-parameter models on AWS EFA", section "MoE all-to-all
+// over EFA": after dispatch, grouped GEMMs multiply each expert's tokens by its
+// weights; the expert FFN here is SwiGLU.)
+//
+// One persistent, warp-specialised kernel template serves all six contractions
+// of the layer:
+//   GATEUP  [a|b] = x_perm W1[e]^T | x_perm W3[e]^T, epilogue h = bf16(silu(a) b)
+//   DOWN    o = bf16(h W2[e]^T)
+//   DH      dh = do W2[e], epilogue da = bf16(dh b silu'(a)), db = bf16(dh silu(a))
+//   DX      dx_perm = bf16([da|db] [W1[e]; W3[e]])
+//   WG2     dW2[e] = do^T h                     (K = the expert's rows, ragged)
+//   WG13    [dW1[e]; dW3[e]] = [da|db]^T x_perm (K ragged)
+// Roles (192 threads): warp 0 issues TMA loads into a 4-stage shared-memory
+// ring, warp 1 owns TMEM and issues tcgen05.mma (128 x 256 x 16, bf16 in, fp32
+// accumulate), warps 2-5 drain the accumulator (tcgen05.ld) and run the
+// epilogue.  Two 256-column TMEM accumulators let the epilogue of one tile
+// overlap the main loop of the next.  Every wait is bounded (kWaitLimitNs);
+// a timeout sets the error word and all roles return after their in-flight
+// copies and MMAs have drained.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+constexpr int BM = 128, BK = 64, BN = 256, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // every mode moves exactly this per k-block
+constexpr int ATOM_BYTES = 64 * BK * 2;         // MN-major block: 64 elements x 64 k-rows
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+
+enum Mode : int { GATEUP = 0, DOWN = 1, DH = 2, DX = 3, WG2 = 4, WG13 = 5 };
+
+template <int M> struct Traits {
+  static constexpr bool a_mn = (M == WG2 || M == WG13);
+  static constexpr bool b_mn = (M == DH || M == DX || M == WG2 || M == WG13);
+  static constexpr bool wgrad = (M == WG2 || M == WG13);
+};
+
+struct alignas(8) SharedCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Item {
+  int e, row0, row_end, mt, nt, kblocks, krow0;
+};
+
+__device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int item, Item& it) {
+  if (mode == WG2 || mode == WG13) {
+    const int per_e = g.n_tiles_m * g.n_tiles_n;
+    it.e = item / per_e;
+    const int rem = item % per_e;
+    it.mt = rem / g.n_tiles_n;
+    it.nt = rem % g.n_tiles_n;
+    it.krow0 = g.offsets[it.e];
+    const int rows = g.offsets[it.e + 1] - it.krow0;
+    it.kblocks = ceil_div(rows, BK);
+    it.row0 = it.row_end = 0;
+    return true;
+  }
+  const int mi = item / g.n_tiles_n;
+  it.nt = item % g.n_tiles_n;
+  const int2 tl = g.tiles[mi];
+  it.row0 = tl.x;
+  it.e = tl.y;
+  it.row_end = g.offsets[it.e + 1];
+  it.mt = 0;
+  it.krow0 = 0;
+  it.kblocks = g.kblocks;
+  return true;
+}
+
+__device__ __forceinline__ int total_items(const GemmArgs& g, int mode) {
+  if (mode == WG2 || mode == WG13) return g.E * g.n_tiles_m * g.n_tiles_n;
+  return (*g.tile_count) * g.n_tiles_n;
+}
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.f + expf(-a)); }
+
+__device__ __forceinline__ void store_bf16x16(uint16_t* dst, const float* v, int ncols_left) {
+  // ncols_left: columns still inside the row (multiple of 8)
+  if (ncols_left >= 8) reinterpret_cast<uint4*>(dst)[0] = pack8(v);
+  if (ncols_left >= 16) reinterpret_cast<uint4*>(dst)[1] = pack8(v + 8);
+}
+
+__device__ __forceinline__ void store_f32x16(float* dst, const float* v, int ncols_left) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (ncols_left >= 4 * (q + 1))
+      reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ GemmArgs g) {
+  using Tr = Traits<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t tile_base = (raw_addr + 1023u) & ~1023u;       // 1024-B aligned stages
+  uint8_t* tile_ptr = smem_raw + (tile_base - raw_addr);
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(tile_ptr + STAGES * STAGE_BYTES);
+  volatile int* abort_flag = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&ctl->tfull[a]), 1);
+      mbar_init(smem_u32(&ctl->tempty[a]), 4);
+    }
+    mbar_init(smem_u32(&ctl->mma_done), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (MODE == GATEUP || MODE == DX) tma_prefetch_desc(&tmB2);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+  const int total = total_items(g, MODE);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it_count = 0;   // k-blocks issued so far (all items)
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        Item it;
+        decode_item(g, MODE, item, it);
+        for (int kb = 0; kb < it.kblocks; ++kb, ++it_count) {
+          const int s = it_count % STAGES;
+          const uint32_t ph = (it_count / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, g.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&ctl->full[s]);
+          const uint32_t sa = tile_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(bar, STAGE_BYTES);
+          const int kx = kb * BK;
+          if (MODE == GATEUP) {
+            tma_load_2d(sa, &tmA, bar, kx, it.row0);
+            const int brow = it.e * g.f + it.nt * 128;
+            tma_load_2d(sb, &tmB, bar, kx, brow);
+            tma_load_2d(sb + B_BYTES / 2, &tmB2, bar, kx, brow);
+          } else if (MODE == DOWN) {
+            tma_load_2d(sa, &tmA, bar, kx, it.row0);
+            tma_load_2d(sb, &tmB, bar, kx, it.e * g.d + it.nt * BN);
+          } else if (MODE == DH) {
+            tma_load_2d(sa, &tmA, bar, kx, it.row0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(sb + j * ATOM_BYTES, &tmB, bar, it.nt * BN + j * 64, it.e * g.d + kx);
+          } else if (MODE == DX) {
+            tma_load_2d(sa, &tmA, bar, kx, it.row0);
+            const bool first = kx < g.f;
+            const int krow = it.e * g.f + (first ? kx : kx - g.f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(sb + j * ATOM_BYTES, first ? &tmB : &tmB2, bar, it.nt * BN + j * 64, krow);
+          } else {  // WG2 / WG13: both operands MN-major, K = rows of expert e
+            const int krow = it.krow0 + kx;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d(sa + j * ATOM_BYTES, &tmA, bar, it.mt * BM + j * 64, krow);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(sb + j * ATOM_BYTES, &tmB, bar, it.nt * BN + j * 64, krow);
+          }
+        }
+      }
+      if (!ok) {
+        // drain: the last (up to STAGES) issued loads must land before the CTA exits
+        const uint32_t n = it_count < (uint32_t)STAGES ? it_count : (uint32_t)STAGES;
+        int dummy = 0;
+        for (uint32_t q = 0; q < n; ++q) {
+          const uint32_t c = it_count - 1 - q;
+          volatile int never = 0;
+          mbar_wait_bounded(smem_u32(&ctl->full[c % STAGES]), (c / STAGES) & 1u, &never, &dummy);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, Tr::a_mn, Tr::b_mn);
+    uint32_t it_count = 0;
+    int j = 0;
+    bool ok = true;
+    bool issued_any = false;
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++j) {
+      Item it;
+      decode_item(g, MODE, item, it);
+      const int acc = j & 1;
+      const uint32_t aph = (j >> 1) & 1u;
+      ok = mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, g.err);
+      ok = __all_sync(kFull, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < it.kblocks; ++kb, ++it_count) {
+        const int s = it_count % STAGES;
+        const uint32_t ph = (it_count / STAGES) & 1u;
+        ok = mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, g.err);
+        ok = __all_sync(kFull, ok);
+        if (!ok) break;
+        const uint32_t sa = tile_base + s * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+        if (Tr::wgrad) {
+          const int rem = (g.offsets[it.e + 1] - it.krow0) - kb * BK;
+          if (rem < BK) {  // rows past the expert belong to the next one: zero them
+            const int zrows = BK - rem;
+            const int per_atom = zrows * 8;   // 16-byte chunks
+            for (int q = lane; q < 6 * per_atom; q += 32) {
+              const int atom = q / per_atom, w = q % per_atom;
+              const int row = rem + w / 8, chunk = w % 8;
+              uint8_t* p = tile_ptr + s * STAGE_BYTES + atom * ATOM_BYTES + row * 128 + chunk * 16;
+              *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = Tr::a_mn ? smem_desc_sw128(sa + kk * 2048, ATOM_BYTES, 1024)
+                                         : smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, ATOM_BYTES, 1024)
+                                         : smem_desc_sw128(sb + kk * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&ctl->empty[s]));   // frees the stage when these MMAs finish
+          issued_any = true;
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (it.kblocks > 0) tc_commit(smem_u32(&ctl->tfull[acc]));
+        else mbar_arrive(smem_u32(&ctl->tfull[acc]));
+      }
+      __syncwarp();
+    }
+    // drain outstanding MMAs before TMEM is released
+    if (lane == 0 && issued_any) {
+      tc_commit(smem_u32(&ctl->mma_done));
+      volatile int never = 0;
+      int dummy = 0;
+      mbar_wait_bounded(smem_u32(&ctl->mma_done), 0, &never, &dummy);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;              // TMEM lane quadrant this warp may access
+    const int r_local = q * 32 + lane;   // accumulator row owned by this thread
+    int j = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
+      Item it;
+      decode_item(g, MODE, item, it);
+      const int acc = j & 1;
+      const uint32_t aph = (j >> 1) & 1u;
+      bool ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag, g.err);
+      ok = __all_sync(kFull, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      if (MODE == GATEUP) {
+        const int row = it.row0 + r_local;
+        const bool valid = row < it.row_end;
+        for (int c = 0; c < 128; c += 16) {
+          float a[16], b[16];
+          tmem_ld16(t_row + c, a);
+          tmem_ld16(t_row + 128 + c, b);
+          tmem_ld_wait();
+          const int col = it.nt * 128 + c;
+          if (valid && col < g.f) {
+            float h[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) h[u] = silu_f(a[u]) * b[u];
+            const size_t off = (size_t)row * g.f + col;
+            store_bf16x16(g.out_bf16 + off, h, g.f - col);
+            if (g.save_a) {
+              store_bf16x16(g.save_a + off, a, g.f - col);
+              store_bf16x16(g.save_b + off, b, g.f - col);
+            }
+          }
+        }
+      } else if (MODE == DOWN || MODE == DX) {
+        const int row = it.row0 + r_local;
+        const bool valid = row < it.row_end;
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_ld_wait();
+          const int col = it.nt * BN + c;
+          if (valid && col < g.d) store_bf16x16(g.out_bf16 + (size_t)row * g.d + col, v, g.d - col);
+        }
+      } else if (MODE == DH) {
+        const int row = it.row0 + r_local;
+        const bool valid = row < it.row_end;
+        for (int c = 0; c < BN; c += 16) {
+          float dh[16];
+          tmem_ld16(t_row + c, dh);
+          tmem_ld_wait();
+          const int col = it.nt * BN + c;
+          if (valid && col < g.f) {
+            const size_t off = (size_t)row * g.f + col;
+            float a[16], b[16], da[16], db[16];
+            const uint4* pa = reinterpret_cast<const uint4*>(g.in_a + off);
+            const uint4* pb = reinterpret_cast<const uint4*>(g.in_b + off);
+            unpack8(pa[0], a);
+            unpack8(pb[0], b);
+            if (g.f - col >= 16) {
+              unpack8(pa[1], a + 8);
+              unpack8(pb[1], b + 8);
+            } else {
+#pragma unroll
+              for (int u = 8; u < 16; ++u) a[u] = b[u] = 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const float sg = 1.f / (1.f + expf(-a[u]));
+              da[u] = dh[u] * b[u] * (sg * (1.f + a[u] * (1.f - sg)));
+              db[u] = dh[u] * a[u] * sg;
+            }
+            const size_t o2 = (size_t)row * (2 * g.f) + col;
+            store_bf16x16(g.out_bf16 + o2, da, g.f - col);
+            store_bf16x16(g.out_bf16 + o2 + g.f, db, g.f - col);
+          }
+        }
+      } else {  // WG2 / WG13: fp32 weight gradients
+        const int m = it.mt * BM + r_local;
+        const int mrows = (MODE == WG2) ? g.d : 2 * g.f;
+        const int ncols = (MODE == WG2) ? g.f : g.d;
+        float* dst_row = nullptr;
+        if (m < mrows) {
+          if (MODE == WG2) dst_row = g.out_f32 + ((size_t)it.e * g.d + m) * g.f;
+          else if (m < g.f) dst_row = g.out_f32 + ((size_t)it.e * g.f + m) * g.d;
+          else dst_row = g.out_f32b + ((size_t)it.e * g.f + (m - g.f)) * g.d;
+        }
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          if (it.kblocks > 0) {
+            tmem_ld16(t_row + c, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) v[u] = 0.f;
+          }
+          const int col = it.nt * BN + c;
+          if (dst_row && col < ncols) store_f32x16(dst_row + col, v, ncols - col);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// Ragged M tiles: expert e's rows [offsets[e], offsets[e+1]) split into 128-row
+// tiles; tiles[i] = {first row, expert}, ordered by expert then row.
+__global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
+                                                           int E, int2* __restrict__ tiles,
+                                                           int32_t* __restrict__ tile_count) {
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int carry = 0;
+  for (int e0 = 0; e0 < E; e0 += 1024) {
+    const int e = e0 + tid;
+    int r0 = 0, n = 0;
+    if (e < E) {
+      r0 = offsets[e];
+      n = ceil_div(offsets[e + 1] - r0, BM);
+    }
+    int incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int ws = warp_sums[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, ws, off);
+        if (lane >= off) ws += o;
+      }
+      warp_sums[lane] = ws;
+    }
+    __syncthreads();
+    const int start = carry + (wid > 0 ? warp_sums[wid - 1] : 0) + incl - n;
+    for (int i = 0; i < n; ++i) tiles[start + i] = make_int2(r0 + i * BM, e);
+    carry += warp_sums[31];
+    __syncthreads();
+  }
+  if (tid == 0) *tile_count = carry;
+}
+}  // namespace
+
+// ------------------------------------------------------------------ host side
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 matrix [rows, cols] (row pitch = cols elements), box {64 cols, box_rows}, 128-B swizzle.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (n[dev] == 0) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
+  return n[dev] > 0 ? n[dev] : 148;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
+                        const GemmArgs& g, long long max_items, cudaStream_t s) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  if (max_items <= 0) return cudaSuccess;
+  const int grid = (int)std::min<long long>(sm_count(), max_items);
+  grouped_gemm_kernel<MODE><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, b2, g);
+  return cudaGetLastError();
+}
+}  // namespace
+
+size_t tiles_ws_bytes(int N, int E) {
+  return align_up(sizeof(int2) * ((size_t)ceil_div(N, BM) + E) + 16, 256);
+}
+
+cudaError_t launch_build_tiles(const int32_t* offsets, int E, void* ws, cudaStream_t s) {
+  int32_t* count = static_cast<int32_t*>(ws);
+  int2* tiles = reinterpret_cast<int2*>(static_cast<uint8_t*>(ws) + 16);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(offsets, E, tiles, count);
+  return cudaGetLastError();
+}
+
+// x_perm [N,d] -> h [N,f] (and a, b); h -> out [N,d].
+cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
+                           int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                           uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
+                           void* tiles_ws, int* err, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  cudaError_t e = launch_build_tiles(offsets, E, tiles_ws, s);
+  if (e != cudaSuccess) return e;
+  GemmArgs g{};
+  g.E = E; g.N = N; g.d = d; g.f = f;
+  g.offsets = offsets;
+  g.tile_count = static_cast<const int32_t*>(tiles_ws);
+  g.tiles = reinterpret_cast<const int2*>(static_cast<const uint8_t*>(tiles_ws) + 16);
+  g.err = err;
+  const long long max_m_tiles = ceil_div(N, BM) + E;
+  CUtensorMap ma, mb, mb2;
+  // gate-up: A = x_perm, B = W1 / W3 rows (128 per tile each)
+  if (!make_map(&ma, x_perm, N, d, BM) || !make_map(&mb, W1, (long long)E * f, d, 128) ||
+      !make_map(&mb2, W3, (long long)E * f, d, 128))
+    return cudaErrorInvalidValue;
+  g.kblocks = ceil_div(d, BK);
+  g.n_tiles_n = ceil_div(f, 128);
+  g.out_bf16 = h; g.save_a = a_save; g.save_b = b_save;
+  e = launch_mode<GATEUP>(ma, mb, mb2, g, max_m_tiles * g.n_tiles_n, s);
+  if (e != cudaSuccess) return e;
+  // down: A = h, B = W2 rows (256 per tile)
+  if (!make_map(&ma, h, N, f, BM) || !make_map(&mb, W2, (long long)E * d, f, BN))
+    return cudaErrorInvalidValue;
+  g.kblocks = ceil_div(f, BK);
+  g.n_tiles_n = ceil_div(d, BN);
+  g.out_bf16 = out; g.save_a = g.save_b = nullptr;
+  return launch_mode<DOWN>(ma, mb, mb, g, max_m_tiles * g.n_tiles_n, s);
+}
+
+// Backward contractions.  d % 64 == 0 and f % 64 == 0 are required.
+cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
+                           int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                           const uint16_t* a_s, const uint16_t* b_s, const uint16_t* h,
+                           const uint16_t* dO, uint16_t* dab, uint16_t* dx_perm, float* dW1,
+                           float* dW3, float* dW2, void* tiles_ws, int* err, cudaStream_t s) {
+  cudaError_t e;
+  GemmArgs g{};
+  g.E = E; g.N = N; g.d = d; g.f = f;
+  g.offsets = offsets;
+  g.tile_count = static_cast<const int32_t*>(tiles_ws);
+  g.tiles = reinterpret_cast<const int2*>(static_cast<const uint8_t*>(tiles_ws) + 16);
+  g.err = err;
+  CUtensorMap ma, mb, mb2;
+  if (N > 0) {
+    e = launch_build_tiles(offsets, E, tiles_ws, s);
+    if (e != cudaSuccess) return e;
+    const long long max_m_tiles = ceil_div(N, BM) + E;
+    // dh = do W2[e] (B MN-major: W2 viewed [E*d, f]); epilogue -> dab = [da | db]
+    if (!make_map(&ma, dO, N, d, BM) || !make_map(&mb, W2, (long long)E * d, f, 64))
+      return cudaErrorInvalidValue;
+    g.kblocks = d / BK;
+    g.n_tiles_n = ceil_div(f, BN);
+    g.out_bf16 = dab; g.in_a = a_s; g.in_b = b_s;
+    e = launch_mode<DH>(ma, mb, mb, g, max_m_tiles * g.n_tiles_n, s);
+    if (e != cudaSuccess) return e;
+    // dx_perm = [da | db] [W1[e]; W3[e]] (B MN-major: W1, W3 viewed [E*f, d])
+    if (!make_map(&ma, dab, N, 2LL * f, BM) || !make_map(&mb, W1, (long long)E * f, d, 64) ||
+        !make_map(&mb2, W3, (long long)E * f, d, 64))
+      return cudaErrorInvalidValue;
+    g.kblocks = 2 * f / BK;
+    g.n_tiles_n = ceil_div(d, BN);
+    g.out_bf16 = dx_perm;
+    e = launch_mode<DX>(ma, mb, mb2, g, max_m_tiles * g.n_tiles_n, s);
+    if (e != cudaSuccess) return e;
+  }
+  // dW2[e] = do^T h: A = do [N, d] MN-major, B = h [N, f] MN-major
+  const long long rows = N > 0 ? N : 1;
+  if (!make_map(&ma, dO, rows, d, 64) || !make_map(&mb, h, rows, f, 64)) return cudaErrorInvalidValue;
+  g.n_tiles_m = ceil_div(d, BM);
+  g.n_tiles_n = ceil_div(f, BN);
+  g.out_f32 = dW2;
+  e = launch_mode<WG2>(ma, mb, mb, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
+  if (e != cudaSuccess) return e;
+  // [dW1[e]; dW3[e]] = [da | db]^T x_perm: A = dab [N, 2f], B = x_perm [N, d]
+  if (!make_map(&ma, dab, rows, 2LL * f, 64) || !make_map(&mb, x_perm, rows, d, 64))
+    return cudaErrorInvalidValue;
+  g.n_tiles_m = ceil_div(2 * f, BM);
+  g.n_tiles_n = ceil_div(d, BN);
+  g.out_f32 = dW1; g.out_f32b = dW3;
+  return launch_mode<WG13>(ma, mb, mb, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,66 @@
+// Internal launchers shared by the C-ABI implementation (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Arguments of the grouped tcgen05 GEMM kernel (one struct for all modes).
+struct GemmArgs {
+  int E, N, d, f;
+  const int32_t* offsets;     // [E+1] expert row offsets
+  const int2* tiles;          // ragged 128-row tiles {first row, expert}
+  const int32_t* tile_count;  // number of valid entries in tiles
+  int kblocks;                // 64-deep k-blocks per tile (row-ragged modes)
+  int n_tiles_n;              // output column tiles
+  int n_tiles_m;              // output row tiles per expert (weight-gradient modes)
+  uint16_t* out_bf16;
+  uint16_t* save_a;
+  uint16_t* save_b;
+  const uint16_t* in_a;
+  const uint16_t* in_b;
+  float* out_f32;
+  float* out_f32b;
+  int* err;
+};
+
+cudaError_t launch_gate_logits(const uint16_t* x, const float* wg, const float* bias, int T, int d,
+                               int E, float* logits, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int T, int E, int R, int32_t* idx, float* w,
+                        cudaStream_t s);
+
+size_t dispatch_ws_bytes(int T, int E);
+cudaError_t launch_dispatch(const uint16_t* x, const int32_t* idx, int T, int d, int E, int R,
+                            int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                            int32_t* slot_row, uint16_t* x_perm, void* ws, int* err,
+                            cudaStream_t s);
+cudaError_t dispatch_set_smem_limits();
+
+cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const float* w, int T,
+                           int d, int R, uint16_t* y, cudaStream_t s);
+
+size_t tiles_ws_bytes(int N, int E);
+cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
+                           int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                           uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
+                           void* tiles_ws, int* err, cudaStream_t s);
+cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
+                           int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                           const uint16_t* a_s, const uint16_t* b_s, const uint16_t* h,
+                           const uint16_t* dO, uint16_t* dab, uint16_t* dx_perm, float* dW1,
+                           float* dW3, float* dW2, void* tiles_ws, int* err, cudaStream_t s);
+
+// backward of routing / dispatch / combine
+cudaError_t launch_bwd_route(const uint16_t* dy, const uint16_t* o, const int32_t* slot_row,
+                             const float* w, int T, int d, int R, uint16_t* dO, float* dsel_tok,
+                             float* dsel_row, cudaStream_t s);
+cudaError_t launch_wg_transpose(const float* wg, int d, int E, float* wgT, cudaStream_t s);
+cudaError_t launch_dwg(const uint16_t* x_perm, const int32_t* offsets, const float* dsel_row,
+                       int d, int E, float* dW_gate, cudaStream_t s);
+cudaError_t launch_dx_combine(const uint16_t* dx_perm, const int32_t* slot_row,
+                              const int32_t* idx, const float* dsel_tok, const float* wgT, int T,
+                              int d, int E, int R, uint16_t* dx, cudaStream_t s);
+
+}  // namespace moe

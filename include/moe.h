@@ -1,0 +1,199 @@
+/*
+ * moe.h -- C ABI of the GB300 MoE layer hot path (route, dispatch, grouped
+ * SwiGLU expert FFN, combine, and the layer's forward and backward).
+ *
+ * Method: "Enabling trillion-parameter models on AWS EFA" (Licker, Hu,
+ * Zaytsev, Chen; 2025).  Section "Introduction": an MoE layer routes each token
+ * to a few experts with a small linear router; dispatch groups tokens by
+ * expert and combine, its dual, brings the expert outputs back and takes their
+ * weighted average.  Section "Send and receive buffers": T tokens, each routed
+ * to R of E experts.  Section "Dispatch and combine": per-expert counts and a
+ * cumulative sum give the offsets that pack each expert's tokens contiguously
+ * for the grouped GEMM.  Here everything runs on one GPU; the page's
+ * network send/receive halves have no counterpart.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates device memory and never synchronises, unless MOE_CHECK is
+ *    passed (then the call waits for its own work and reads the device error
+ *    word back).  Work is enqueued on `stream` (a cudaStream_t; NULL means the
+ *    legacy default stream).
+ *  - bf16 tensors cross the ABI as raw uint16_t bit patterns.  All tensors are
+ *    dense row-major; every pointer must be 16-byte aligned and d, f must be
+ *    multiples of 8 (rows move as 16-byte vectors), else MOE_ERR_UNSUPPORTED.
+ *  - Shapes: T tokens, hidden size d, E experts, top-R routing, expert FFN
+ *    width f, N = T*R routed rows.  A "slot" is s = t*R + r (token t, choice r).
+ *    Limits: 1 <= R <= 32, R <= E <= 1024, T*R < 2^31.
+ *  - Weight layout (nn.Linear [out, in]): W1, W3 bf16 [E, f, d]; W2 bf16
+ *    [E, d, f]; the router weight W_g is fp32 [d, E], its bias fp32 [E].
+ *  - Workspace: calls that need scratch memory take (ws, ws_bytes).  With
+ *    ws == NULL the call only writes the required size to *ws_bytes and
+ *    returns MOE_OK.  Otherwise *ws_bytes must be at least that size and ws
+ *    256-byte aligned; the workspace must not be shared by calls that may run
+ *    concurrently.
+ *  - Errors: host-side argument checks return MOE_ERR_INVALID_ARG /
+ *    MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE before anything is enqueued; a
+ *    failed launch returns MOE_ERR_CUDA.  Kernels that detect bad routing
+ *    (expert index outside [0,E) or repeated within a token) or a stalled
+ *    pipeline wait set bits in a device error word inside the workspace and
+ *    never trap; with MOE_CHECK the call returns MOE_ERR_BAD_ROUTING or
+ *    MOE_ERR_TIMEOUT from it.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, negative or inconsistent size */
+  MOE_ERR_UNSUPPORTED = 2,   /* misaligned pointer, d or f not a multiple of 8, limits */
+  MOE_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned */
+  MOE_ERR_BAD_ROUTING = 4,   /* device saw an expert index outside [0,E) or a repeat */
+  MOE_ERR_TIMEOUT = 5,       /* a bounded pipeline wait gave up (kernel returned early) */
+  MOE_ERR_CUDA = 6           /* a CUDA runtime call or launch failed */
+} moe_status_t;
+
+typedef void* moe_stream_t;  /* cudaStream_t */
+
+/* flags */
+#define MOE_LOGITS_IN 0x1u   /* moe_route: `logits` is an input; skip the gate projection */
+#define MOE_CHECK 0x2u       /* wait for the call's work and report device-side errors */
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+/*
+ * moe_route -- the router: a small linear layer scores the experts and the R
+ * best are chosen for each token (section "Introduction").
+ *   logits[t,e] = sum_k x[t,k] * W_g[k,e] + bias[e]        (fp32 accumulation)
+ *   idx[t,0..R-1] = the R experts of largest logit, ordered by (logit desc,
+ *                   expert index asc): ties go to the lower index
+ *   w[t,r] = exp(l_{idx[t,r]} - l_{idx[t,0]}) / sum_s exp(l_{idx[t,s]} - l_{idx[t,0]})
+ *            (softmax over the chosen experts: the weights sum to 1)
+ * x: bf16 [T,d]; w_gate: fp32 [d,E]; bias: fp32 [E] or NULL.
+ * logits: fp32 [T,E], written (or read, with MOE_LOGITS_IN: then x, w_gate
+ * and bias are ignored and may be NULL).  topk_idx: int32 [T,R]; topk_w: fp32
+ * [T,R].  Logits must be finite.  No workspace.
+ */
+moe_status_t moe_route(const uint16_t* x, const float* w_gate, const float* bias,
+                       int T, int d, int E, int R, float* logits,
+                       int32_t* topk_idx, float* topk_w, unsigned flags, moe_stream_t stream);
+
+/*
+ * moe_dispatch -- group the routed tokens by expert (section "Dispatch and
+ * combine": per-expert counts, their cumulative sum as offsets, tokens packed
+ * contiguously per expert into the grouped-GEMM input).
+ *   counts[e]  = #{slots s : topk_idx[s] == e}
+ *   offsets    = exclusive prefix sum of counts, offsets[E] = T*R
+ *   rows offsets[e] .. offsets[e+1]-1 belong to expert e, in ascending token order
+ *   row_slot[row] = s,  slot_row[s] = row  (inverse maps)
+ *   x_perm[row]   = x[row_slot[row] / R]   (bit copy)
+ * x: bf16 [T,d] (may be NULL together with x_perm: plan only); topk_idx:
+ * int32 [T,R]; counts int32 [E]; offsets int32 [E+1]; row_slot, slot_row
+ * int32 [T*R]; x_perm bf16 [T*R, d].  Needs a workspace (per-block expert
+ * histograms and the error word).  Deterministic: the result does not depend
+ * on scheduling.
+ */
+moe_status_t moe_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int R,
+                          int32_t* counts, int32_t* offsets, int32_t* row_slot, int32_t* slot_row,
+                          uint16_t* x_perm, void* ws, size_t* ws_bytes, unsigned flags,
+                          moe_stream_t stream);
+
+/*
+ * moe_grouped_ffn -- the grouped GEMMs that apply each expert's weights to its
+ * rows (section "MoE all-to-all over EFA"), as a SwiGLU FFN.  For every expert
+ * e and row i in [offsets[e], offsets[e+1]):
+ *   a = x_perm[i] W1[e]^T,  b = x_perm[i] W3[e]^T      (fp32 accumulation)
+ *   h[i]   = bf16(silu(a) * b),   silu(a) = a / (1 + exp(-a))
+ *   out[i] = bf16(h[i] W2[e]^T)
+ * x_perm: bf16 [N,d]; offsets: int32 [E+1] on the device with offsets[E] == N;
+ * W1, W3: bf16 [E,f,d]; W2: bf16 [E,d,f]; h: bf16 [N,f] (written, kept for the
+ * backward); a_save, b_save: bf16 [N,f] or NULL (bf16(a), bf16(b) for the
+ * backward); out: bf16 [N,d].  Needs a workspace (tile list, error word).
+ */
+moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
+                             int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                             uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
+                             void* ws, size_t* ws_bytes, unsigned flags, moe_stream_t stream);
+
+/*
+ * moe_combine -- bring each token's R expert outputs back and take their
+ * gate-weighted sum (sections "Introduction" and "Dispatch and combine"):
+ *   y[t] = bf16( sum_{r=0..R-1} topk_w[t,r] * expert_out[slot_row[t*R+r]] )
+ * accumulated in fp32 in r order (bitwise reproducible).  topk_w NULL means
+ * unweighted.  expert_out: bf16 [T*R,d]; slot_row: int32 [T*R]; y: bf16 [T,d].
+ * Rows outside [0, T*R) contribute nothing.  No workspace.
+ */
+moe_status_t moe_combine(const uint16_t* expert_out, const int32_t* slot_row, const float* topk_w,
+                         int T, int d, int R, uint16_t* y, moe_stream_t stream);
+
+/* Layer parameters (device pointers, caller-owned). */
+typedef struct {
+  int T, d, E, R, f;
+  const float* w_gate;  /* fp32 [d,E] */
+  const float* bias;    /* fp32 [E] or NULL */
+  const uint16_t* W1;   /* bf16 [E,f,d] */
+  const uint16_t* W3;   /* bf16 [E,f,d] */
+  const uint16_t* W2;   /* bf16 [E,d,f] */
+} moe_layer_t;
+
+/* Forward intermediates (caller-owned device buffers, written by the forward,
+ * read by the backward).  N = T*R. */
+typedef struct {
+  float* logits;       /* fp32 [T,E] */
+  int32_t* topk_idx;   /* int32 [T,R] */
+  float* topk_w;       /* fp32 [T,R] */
+  int32_t* counts;     /* int32 [E] */
+  int32_t* offsets;    /* int32 [E+1] */
+  int32_t* row_slot;   /* int32 [N] */
+  int32_t* slot_row;   /* int32 [N] */
+  uint16_t* x_perm;    /* bf16 [N,d] */
+  uint16_t* a;         /* bf16 [N,f] or NULL (inference: nothing saved for the backward) */
+  uint16_t* b;         /* bf16 [N,f] or NULL (must be NULL iff a is) */
+  uint16_t* h;         /* bf16 [N,f] */
+  uint16_t* o;         /* bf16 [N,d] expert outputs */
+} moe_saved_t;
+
+/*
+ * moe_layer_fwd -- y = combine(FFN(dispatch(x, route(x)))): route, dispatch,
+ * grouped SwiGLU FFN and combine, as the entry points above define them.
+ * x: bf16 [T,d]; y: bf16 [T,d]; saved: all intermediates (a and b may be NULL).
+ */
+moe_status_t moe_layer_fwd(const moe_layer_t* layer, const uint16_t* x, uint16_t* y,
+                           const moe_saved_t* saved, void* ws, size_t* ws_bytes, unsigned flags,
+                           moe_stream_t stream);
+
+/*
+ * moe_layer_bwd -- gradients of a loss L given dy = dL/dy (bf16 [T,d]), from
+ * the intermediates of moe_layer_fwd (which must have saved a and b):
+ *   dw[t,r]  = <dy_t, o_row>,  do_row = bf16(w[t,r] dy_t)      (row = slot_row[t*R+r])
+ *   per expert: dh = do W2[e];  da = bf16(dh * b * silu'(a)),  db = bf16(dh * silu(a))
+ *               dx_perm = bf16(da W1[e] + db W3[e])
+ *               dW2[e] = do^T h,  dW1[e] = da^T x_perm,  dW3[e] = db^T x_perm
+ *   router:  dlogits[t, idx[t,q]] = w_q (dw_q - sum_r w_r dw_r), 0 for unchosen experts
+ *            dW_gate = x^T dlogits
+ *   dx_t = bf16( sum_r dx_perm[row(t,r)] + dlogits_t W_g^T )
+ * (a, b as saved in bf16; silu'(a) = s(a)(1 + a(1 - s(a))), s the logistic
+ * function.)  x: bf16 [T,d]; dx: bf16 [T,d]; dW_gate: fp32 [d,E]; dW1, dW3:
+ * fp32 [E,f,d]; dW2: fp32 [E,d,f] -- all overwritten (experts with no rows get
+ * zero gradients).  The router bias is treated as a constant.
+ */
+moe_status_t moe_layer_bwd(const moe_layer_t* layer, const uint16_t* x, const moe_saved_t* saved,
+                           const uint16_t* dy, uint16_t* dx, float* dW_gate, float* dW1,
+                           float* dW3, float* dW2, void* ws, size_t* ws_bytes, unsigned flags,
+                           moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,57 @@
+"""Shared test helpers: tolerances, conversions, seeded routing for GPU tests."""
+import numpy as np
+import torch
+
+# Floating-point parity bar for bf16 outputs with fp32 accumulation, normwise
+# per tensor: max|got-ref| / max|ref| <= 1e-2 and sum|got-ref| / sum|ref| <= 1e-3.
+MAX_REL = 1e-2
+MEAN_REL = 1e-3
+
+
+def f64(t):
+    """A torch tensor (any device/dtype) as a float64 numpy array."""
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def bits(t):
+    """A bf16 torch tensor as numpy uint16 bit patterns."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def rel_errors(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    diff = np.abs(got - ref)
+    mx = float(diff.max() / max(np.abs(ref).max(), 1e-30)) if ref.size else 0.0
+    mean = float(diff.sum() / max(np.abs(ref).sum(), 1e-30)) if ref.size else 0.0
+    return mx, mean
+
+
+def assert_close(got, ref, name, max_rel=MAX_REL, mean_rel=MEAN_REL):
+    mx, mean = rel_errors(got, ref)
+    assert np.isfinite(np.asarray(got, np.float64)).all(), f"{name}: non-finite values"
+    assert mx <= max_rel and mean <= mean_rel, f"{name}: max_rel={mx:.3e} mean_rel={mean:.3e}"
+    return mx, mean
+
+
+def near_tie_tokens(logits, R, rel=1e-5):
+    """Tokens whose R-th and (R+1)-th largest logits are closer than rel*max|logit|."""
+    l = np.asarray(logits, np.float64)
+    T, E = l.shape
+    if R >= E:
+        return np.zeros(T, dtype=bool)
+    s = -np.sort(-l, axis=1)
+    gap = s[:, R - 1] - s[:, R]
+    return gap <= rel * np.abs(l).max()
+
+
+def random_routing(T, E, R, seed, skew=0.0):
+    """Seeded distinct-expert routing (host), weights positive and summing to 1."""
+    g = np.random.default_rng(seed)
+    p = np.arange(1, E + 1, dtype=np.float64) ** (-skew)
+    p /= p.sum()
+    keys = np.log(p)[None, :] - np.log(-np.log(g.random((T, E)).clip(1e-300, 1.0)))
+    idx = np.argsort(-keys, axis=1)[:, :R].astype(np.int32)
+    u = g.random((T, R)) + 0.5
+    w = (u / u.sum(1, keepdims=True)).astype(np.float32)
+    return idx, w

@@ -1,0 +1,101 @@
+"""The C ABI library builds, loads and exports what include/moe.h declares;
+host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from expert_moe_route_gb300 import binding as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "moe.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_six_entry_points():
+    names = declared_functions()
+    for n in ("moe_route", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_layer_fwd",
+              "moe_layer_bwd"):
+        assert n in names
+    assert set(names) == set(B.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = B.lib()
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert lib.moe_version() == 100
+    assert B.status_string(0) == "MOE_OK" and B.status_string(4) == "MOE_ERR_BAD_ROUTING"
+
+
+def test_library_is_in_tree():
+    assert os.path.realpath(B.library_path()).startswith(
+        os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+
+def _st(fn, *args):
+    return fn(*args)
+
+
+def test_host_argument_checks():
+    lib = B.lib()
+    n = ctypes.c_size_t(0)
+    # workspace queries need no device
+    assert lib.moe_dispatch(None, None, 100, 64, 8, 2, None, None, None, None, None, None,
+                            ctypes.byref(n), 0, None) == 0 and n.value > 0
+    # bad shapes
+    assert lib.moe_dispatch(None, None, 100, 64, 8, 9, None, None, None, None, None, None,
+                            ctypes.byref(n), 0, None) == 1          # R > E
+    assert lib.moe_dispatch(None, None, 100, 60, 8, 2, None, None, None, None, None, None,
+                            ctypes.byref(n), 0, None) == 2          # d % 8 != 0
+    assert lib.moe_dispatch(None, None, 100, 64, 2000, 2, None, None, None, None, None, None,
+                            ctypes.byref(n), 0, None) == 2          # E > 1024
+    assert lib.moe_dispatch(None, None, -1, 64, 8, 2, None, None, None, None, None, None,
+                            ctypes.byref(n), 0, None) == 1
+    # too-small or misaligned workspace
+    small = ctypes.c_size_t(16)
+    assert lib.moe_dispatch(None, None, 100, 64, 8, 2, None, None, None, None, None,
+                            ctypes.c_void_p(4096), ctypes.byref(small), 0, None) == 3
+    big = ctypes.c_size_t(1 << 20)
+    assert lib.moe_dispatch(None, None, 100, 64, 8, 2, None, None, None, None, None,
+                            ctypes.c_void_p(4096 + 16), ctypes.byref(big), 0, None) == 3
+    # route: R > 32 unsupported, R > E invalid
+    assert lib.moe_route(None, None, None, 4, 64, 64, 33, None, None, None, 0, None) == 2
+    assert lib.moe_route(None, None, None, 4, 64, 4, 5, None, None, None, 0, None) == 1
+    # combine: misaligned output
+    assert lib.moe_combine(ctypes.c_void_p(4096), ctypes.c_void_p(8192), None, 4, 64, 2,
+                           ctypes.c_void_p(4098), None) == 2
+    # grouped ffn: f % 8
+    assert lib.moe_grouped_ffn(None, None, 10, 64, 60, 4, None, None, None, None, None, None,
+                               None, None, ctypes.byref(n), 0, None) == 2
+
+
+def test_layer_ws_query_and_bwd_shape_limits():
+    lib = B.lib()
+    L = B.moe_layer_t(256, 512, 8, 2, 1024, 8, 0, 16, 32, 48)
+    n = ctypes.c_size_t(0)
+    assert lib.moe_layer_fwd(ctypes.byref(L), None, None, None, None, ctypes.byref(n), 0, None) == 0
+    assert n.value > 0
+    assert lib.moe_layer_bwd(ctypes.byref(L), None, None, None, None, None, None, None, None,
+                             None, ctypes.byref(n), 0, None) == 0
+    L2 = B.moe_layer_t(256, 520, 8, 2, 1024, 8, 0, 16, 32, 48)   # d % 64 != 0: no backward
+    assert lib.moe_layer_bwd(ctypes.byref(L2), None, None, None, None, None, None, None, None,
+                             None, ctypes.byref(n), 0, None) == 2
+
+
+def test_no_cpu_fallback_without_gpu():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    # with no device the library reports a CUDA error instead of computing on the host
+    lib = B.lib()
+    n = ctypes.c_size_t(1 << 20)
+    st = lib.moe_combine(ctypes.c_void_p(4096), ctypes.c_void_p(8192), None, 4, 64, 2,
+                         ctypes.c_void_p(1 << 20), None)
+    assert st == 6
