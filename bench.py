@@ -1,0 +1,521 @@
+"""Benchmark of the MoE layer hot path on GB300 (one JSON line on rank 0).
+
+Default workload: the MoE layer training step (forward + backward) with
+T=16384 tokens, d=4096, E=128 experts, top-8 routing, SwiGLU width f=1536 --
+one pass of every step of the path (route, dispatch, grouped SwiGLU FFN,
+combine, and their backward).  Other workloads: --workload large | large_hot |
+mid | tiny (forward only) and dispatch (dispatch + combine with identity
+experts, --tokens T).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+value = tokens per second of the whole job (all ranks); each rank runs an
+independent replica of the workload (the path has no cross-GPU exchange), so
+scaling is weak.  The timed region is K back-to-back steps between CUDA events
+on the launching stream, after W warm-up steps, bracketed by a barrier and a
+device synchronisation; the max over ranks is reported.  Each step streams
+more than L2 (5 GB of expert weights for the default workload), so no flush
+is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s on 1 GB300; grouped-GEMM % BF16 TC peak; dispatch/combine GB/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="train",
+                   choices=["train", "large", "large_hot", "mid", "tiny", "dispatch",
+                            "dispatch_zipf"])
+    p.add_argument("--tokens", type=int, default=None, help="override T")
+    p.add_argument("--cpu-tokens", type=int, default=None,
+                   help="tokens in the CPU oracle sample (default per workload)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            pk = json.load(fh)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [c.strip() for c in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sms.append(float(f[1]))
+                    maxs.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxs) if maxs else None, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ---------------------------------------------------------------- work model
+def stage_work(wl):
+    """Algorithmic work of one launch of each traced stage: (kind, amount).
+
+    kind "tflop": FLOPs of real rows only (no padding); "gb": bytes that must
+    move to or from HBM at least once (reads of inputs + writes of outputs).
+    """
+    T, d, E, R, f = wl.T, wl.d, wl.E, wl.R, wl.f
+    N = T * R
+    w = {
+        "gate": ("alu", 2.0 * T * d * E),
+        "topk": ("gb", 4.0 * T * E + 8.0 * N),
+        "dispatch": ("gb", 2.0 * T * d + 2.0 * N * d + 4.0 * N * 3),
+        "combine": ("gb", 2.0 * N * d + 8.0 * N + 2.0 * T * d),
+    }
+    if f:
+        w.update({
+            "gateup": ("tflop", 4.0 * N * d * f),
+            "down": ("tflop", 2.0 * N * d * f),
+            "bwd_route": ("gb", 2.0 * T * d + 2.0 * N * d + 2.0 * N * d + 12.0 * N),
+            "bwd_dh": ("tflop", 2.0 * N * d * f),
+            "bwd_dx": ("tflop", 4.0 * N * d * f),
+            "bwd_wg2": ("tflop", 2.0 * N * d * f),
+            "bwd_wg13": ("tflop", 4.0 * N * d * f),
+            "bwd_dwg": ("gb", 2.0 * N * d + 4.0 * N + 4.0 * d * E),
+            "bwd_dxc": ("gb", 2.0 * N * d + 2.0 * T * d + 8.0 * E * d),
+        })
+    return w
+
+
+def alu_peak_tflops(sm_mhz):
+    """FP32 FMA peak: 152 SMs x 128 lanes x 2 FLOP per cycle."""
+    return 152 * 128 * 2 * (sm_mhz or 2070.0) * 1e6 / 1e12
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, device):
+    import torch
+
+    from expert_moe_route_gb300 import binding as B
+    from expert_moe_route_gb300 import synth
+
+    over = {} if args.tokens is None else {"T": args.tokens}
+    wl = synth.workload(args.workload, **over)
+    identity = wl.f == 0
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs, resident in HBM before timing
+    if identity:
+        r = synth.drawn_routing(wl, device=device)
+        x, idx, w = r["x"], r["topk_idx"], r["topk_w"]
+        N = wl.T * wl.R
+        counts = torch.empty(wl.E, dtype=torch.int32, device=device)
+        offsets = torch.empty(wl.E + 1, dtype=torch.int32, device=device)
+        row_slot = torch.empty(N, dtype=torch.int32, device=device)
+        slot_row = torch.empty(N, dtype=torch.int32, device=device)
+        x_perm = torch.empty((N, wl.d), dtype=torch.bfloat16, device=device)
+        y = torch.empty_like(x)
+        ws = B.workspace(B.dispatch_ws_bytes(wl.T, wl.d, wl.E, wl.R), device)
+
+        def step(xin=None, yout=None):
+            B.moe_dispatch(x if xin is None else xin, idx, wl.E, counts, offsets, row_slot,
+                           slot_row, x_perm, ws)
+            B.moe_combine(x_perm, slot_row, w, y if yout is None else yout, wl.R)
+        train = False
+        host_in = [("x", x)]
+        host_out = [("y", y)]
+    else:
+        big = wl.E * wl.f * wl.d > (1 << 28)
+        inp = synth.layer_inputs(wl, device=device, weight_device=device if big else "cpu")
+        train = wl.train
+        layer = B.Layer(inp["w_gate"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], wl.R, wl.T)
+        saved = B.Saved(layer, device, train=train)
+        x = inp["x"]
+        y = torch.empty_like(x)
+        fws = B.workspace(B.layer_fwd_ws_bytes(layer), device)
+        if train:
+            g = inp["g"]
+            dx = torch.empty_like(x)
+            dWg = torch.empty((wl.d, wl.E), dtype=torch.float32, device=device)
+            dW1 = torch.empty((wl.E, wl.f, wl.d), dtype=torch.float32, device=device)
+            dW3 = torch.empty_like(dW1)
+            dW2 = torch.empty((wl.E, wl.d, wl.f), dtype=torch.float32, device=device)
+            bws = B.workspace(B.layer_bwd_ws_bytes(layer), device)
+
+        def step(xin=None, yout=None, gin=None, dxout=None):
+            xx = x if xin is None else xin
+            B.moe_layer_fwd(layer, xx, y if yout is None else yout, saved, fws)
+            if train:
+                B.moe_layer_bwd(layer, xx, saved, g if gin is None else gin,
+                                dx if dxout is None else dxout, dWg, dW1, dW3, dW2, bws)
+        host_in = [("x", x)] + ([("g", inp["g"])] if train else [])
+        host_out = [("y", y)] + ([("dx", dx)] if train else [])
+
+    # ---- one checked step (device error word) before timing
+    if identity:
+        step()
+    else:
+        B.moe_layer_fwd(layer, x, y, saved, fws, flags=B.MOE_CHECK)
+        if train:
+            B.moe_layer_bwd(layer, x, saved, g, dx, dWg, dW1, dW3, dW2, bws, flags=B.MOE_CHECK)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region
+    traces = [B.StageTrace() for _ in range(args.steps)]
+    world_barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = B.kernel_launches()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        traces[k].arm()
+        step()
+    B.StageTrace.disarm()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = B.kernel_launches() - launches0
+    clk = clocks.stop()
+    world_barrier(world)
+    ms_total = t0.elapsed_time(t1)
+    ms_total = world_max(ms_total, world, device)
+    ms_step = ms_total / args.steps
+    tokens_per_step = wl.T
+    value = tokens_per_step * world * args.steps / (ms_total / 1e3)
+
+    # ---- per-stage device time, averaged over the timed steps
+    stage_ms = {}
+    for tr in traces:
+        for name, ms in tr.elapsed_ms().items():
+            stage_ms[name] = stage_ms.get(name, 0.0) + ms / args.steps
+    pk, pk_src = load_peaks()
+    work = stage_work(wl)
+    stages = {}
+    for name, ms in stage_ms.items():
+        if name not in work or ms <= 0:
+            continue
+        kind, amount = work[name]
+        if kind == "tflop":
+            ach = amount / (ms / 1e3) / 1e12
+            stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 1),
+                            "frac": round(ach / pk["bf16_tflops_sustained"], 4)}
+        elif kind == "gb":
+            ach = amount / (ms / 1e3) / 1e9
+            stages[name] = {"ms": round(ms, 4), "gbs": round(ach, 1),
+                            "frac": round(ach / pk["hbm_gbs"], 4)}
+        else:
+            ach = amount / (ms / 1e3) / 1e12
+            stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 2),
+                            "frac": round(ach / alu_peak_tflops(clk.get("sm_mhz")), 4)}
+    dom = max(stages, key=lambda n: stages[n]["ms"])
+    kind, amount = work[dom]
+    traffic = None
+    try:
+        with open(PROFILE_TRAFFIC) as fh:
+            tr = json.load(fh).get(wl.name, {}).get(dom)
+            traffic = tr.get("bytes_per_launch") if tr else None
+    except (OSError, ValueError):
+        traffic = None
+    if kind == "tflop":
+        roof = {"bound": "tensor", "kernel": dom, "achieved": stages[dom]["tflops"],
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": stages[dom]["frac"], "traffic": traffic,
+                "peak_source": f"{pk_src} bf16 sustained (kernel timed inside a long step)"}
+    elif kind == "gb":
+        roof = {"bound": "hbm", "kernel": dom, "achieved": stages[dom]["gbs"],
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": stages[dom]["frac"],
+                "traffic": traffic, "peak_source": f"{pk_src} HBM copy"}
+    else:
+        roof = {"bound": "alu", "kernel": dom, "achieved": stages[dom]["tflops"],
+                "peak": round(alu_peak_tflops(clk.get("sm_mhz")), 1), "unit": "TFLOP/s",
+                "frac": stages[dom]["frac"], "traffic": traffic,
+                "peak_source": "FP32 FMA: 152 SMs x 128 lanes x 2 x median SM clock"}
+    gemm = [n for n in stages if work[n][0] == "tflop"]
+    gemm_ms = sum(stages[n]["ms"] for n in gemm)
+    gemm_fl = sum(work[n][1] for n in gemm)
+    summary = {}
+    if gemm_ms > 0:
+        tf = gemm_fl / (gemm_ms / 1e3) / 1e12
+        summary["grouped_gemm_tflops"] = round(tf, 1)
+        summary["grouped_gemm_frac_of_bf16_peak"] = round(tf / pk["bf16_tflops_sustained"], 4)
+    for n in ("dispatch", "combine"):
+        if n in stages:
+            summary[f"{n}_gbs"] = stages[n]["gbs"]
+            summary[f"{n}_frac_of_hbm"] = stages[n]["frac"]
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin_in = {n: t.detach().cpu().pin_memory() for n, t in host_in}
+        pin_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in host_out}
+        dev_in = {n: torch.empty_like(t) for n, t in host_in}
+        dev_out = {n: torch.empty_like(t) for n, t in host_out}
+        bi = sum(t.numel() * t.element_size() for t in pin_in.values())
+        bo = sum(t.numel() * t.element_size() for t in pin_out.values())
+
+        def e2e_step():
+            for n, t in pin_in.items():
+                dev_in[n].copy_(t, non_blocking=True)
+            if identity:
+                step(xin=dev_in["x"], yout=dev_out["y"])
+            elif train:
+                step(xin=dev_in["x"], yout=dev_out["y"], gin=dev_in["g"], dxout=dev_out["dx"])
+            else:
+                step(xin=dev_in["x"], yout=dev_out["y"])
+            for n, t in pin_out.items():
+                t.copy_(dev_out[n], non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        world_barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = world_max(e0.elapsed_time(e1), world, device)
+        e2e = {"value": round(tokens_per_step * world * args.steps / (ems / 1e3), 1),
+               "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "ms_per_step": round(ems / args.steps, 4)}
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 (fp32 accumulation)",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": {"workload": synth.describe(wl) + (" fwd+bwd" if train else " fwd"),
+                   "parallelism": f"replicas x{world} (no cross-GPU exchange)",
+                   "global_batch_tokens": wl.T * world,
+                   "l2": "inputs larger than L2 every step (no flush)"},
+        "roofline": roof,
+        "summary": summary,
+        "stages": stages,
+        "clocks": clk,
+        "gpu_launches": launches,
+        "e2e": e2e,
+    }
+    return result, wl
+
+
+class LazyExperts:
+    """[E, ...] weight tensor whose expert slices are copied to the host on access."""
+
+    def __init__(self, t, bits):
+        self.t, self.bits, self.shape = t, bits, tuple(t.shape)
+
+    def __getitem__(self, e):
+        return self.bits(self.t[e])
+
+
+def cpu_oracle_sample(wl, device, n_tokens, steps=1):
+    """Times the CPU oracle (fwd, and bwd for training) on the first n_tokens tokens."""
+    import numpy as np
+    import torch
+
+    from expert_moe_route_gb300 import synth
+    from oracle import moe_oracle as O
+
+    def bits(t):
+        return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    n = min(n_tokens, wl.T)
+    if wl.f == 0:
+        r = synth.drawn_routing(wl)
+        x = bits(r["x"])[:n]
+        idx = r["topk_idx"].numpy()[:n]
+        w = r["topk_w"].numpy()[:n]
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            _, _, row_slot, slot_row = O.dispatch_plan(idx, wl.E)
+            xp = O.permute_rows(x, row_slot, wl.R)
+            O.combine(O.bf16_to_f64(xp), slot_row, w, n, wl.R)
+        dt = time.perf_counter() - t0
+    else:
+        big = wl.E * wl.f * wl.d > (1 << 28)
+        use_dev = device if (big and torch.cuda.is_available()) else "cpu"
+        inp = synth.layer_inputs(wl, device=use_dev)
+        x = bits(inp["x"])[:n]
+        # expert weights stay where they were drawn; the oracle reads one expert at a time
+        W1, W3, W2 = (LazyExperts(inp[k], bits) for k in ("W1", "W3", "W2"))
+        wg = inp["w_gate"].cpu().numpy()
+        bias = None if inp["bias"] is None else inp["bias"].cpu().numpy()
+        g = bits(inp["g"])[:n] if wl.train else None
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            fw = O.layer_fwd(x, wg, bias, W1, W3, W2, wl.R)
+            if wl.train:
+                O.layer_bwd(fw, x, wg, W1, W3, W2, g, wl.R)
+        dt = time.perf_counter() - t0
+    return n * steps / dt, dt, n
+
+
+def world_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def world_max(v, world, device):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def default_cpu_tokens(wl):
+    if wl.f == 0:
+        return 4096
+    return {"train": 192, "large": 16, "large_hot": 16, "mid": 512, "tiny": 256}.get(wl.name, 128)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from expert_moe_route_gb300 import synth
+        over = {} if args.tokens is None else {"T": args.tokens}
+        wl = synth.workload(args.workload, **over)
+        n = args.cpu_tokens or (8 if wl.f else 1024)
+        device = "cuda:0"
+        try:
+            import torch
+            if not torch.cuda.is_available():
+                device = "cpu"
+        except ImportError:
+            device = "cpu"
+        for _ in range(args.warmup):
+            cpu_oracle_sample(wl, device, n)
+        rates = []
+        t_all = 0.0
+        for _ in range(args.steps):
+            rate, dt, _ = cpu_oracle_sample(wl, device, n)
+            rates.append(rate)
+            t_all += dt
+        value = n * args.steps / t_all
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(1e3 * t_all / args.steps, 2), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64 (bf16 storage points)",
+                "data": "synthetic (seeded)", "impl": "reference",
+                "config": {"workload": synth.describe(wl) + (" fwd+bwd" if wl.train else " fwd"),
+                           "parallelism": "host cores"},
+                "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                                 "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": f"each step: the oracle on the first {n} of {wl.T} tokens "
+                                           f"of the workload (full d, E, R, f and weights)"},
+                "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    device = f"cuda:{torch.cuda.current_device()}"
+    result, wl = run_ours(args, rank, world, device)
+    if rank == 0 and not args.no_cpu_baseline:
+        n = args.cpu_tokens or default_cpu_tokens(wl)
+        rate, dt, n = cpu_oracle_sample(wl, device, n)
+        result["cpu_baseline"] = {
+            "value": round(rate, 2), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"the oracle ({'fwd+bwd' if wl.train else 'fwd'}) on the first {n} of "
+                      f"{wl.T} tokens (full d, E, R, f and weights), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -21,8 +21,13 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
           4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CUDA"}
 
 # the C ABI's exported symbols (checked against include/moe.h by the tests)
-SYMBOLS = ("moe_status_string", "moe_version", "moe_route", "moe_dispatch", "moe_grouped_ffn",
-           "moe_combine", "moe_layer_fwd", "moe_layer_bwd")
+SYMBOLS = ("moe_status_string", "moe_version", "moe_trace_events", "moe_kernel_launches",
+           "moe_route", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_layer_fwd",
+           "moe_layer_bwd")
+
+# moe_stage_t
+STAGES = ("gate", "topk", "dispatch", "gateup", "down", "combine", "bwd_route", "bwd_dh", "bwd_dx",
+          "bwd_wg2", "bwd_wg13", "bwd_dwg", "bwd_dxc")
 
 
 class MoeError(RuntimeError):
@@ -52,6 +57,10 @@ def _declare(lib):
     lib.moe_status_string.argtypes = [_i]
     lib.moe_version.restype = _i
     lib.moe_version.argtypes = []
+    lib.moe_trace_events.restype = _i
+    lib.moe_trace_events.argtypes = [ctypes.POINTER(_vp)]
+    lib.moe_kernel_launches.restype = ctypes.c_ulonglong
+    lib.moe_kernel_launches.argtypes = []
     lib.moe_route.restype = _i
     lib.moe_route.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _u, _vp]
     lib.moe_dispatch.restype = _i
@@ -250,6 +259,40 @@ def moe_layer_bwd(layer: Layer, x, saved: Saved, dy, dx, dW_gate, dW1, dW3, dW2,
                              _p(dW_gate), _p(dW1), _p(dW3), _p(dW2), _p(ws), ctypes.byref(n),
                              flags, _stream(stream))
     _check(st, "moe_layer_bwd")
+
+
+class StageTrace:
+    """CUDA events recorded by the library around each layer stage (moe_trace_events).
+
+    ``arm()`` makes the library record into this trace's events until
+    ``disarm()``; ``elapsed_ms()`` (after the work completed) gives each
+    stage's device time, or None for stages that did not run.
+    """
+
+    def __init__(self):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(STAGES))]
+        self._arr = (_vp * len(self.events))(*[e.cuda_event for e in self.events])
+        self.used = False
+
+    def arm(self):
+        for e in self.events:    # make every event "recorded" so unused stages read as 0
+            e.record()
+        _check(lib().moe_trace_events(self._arr), "moe_trace_events")
+        self.used = True
+
+    @staticmethod
+    def disarm():
+        _check(lib().moe_trace_events(None), "moe_trace_events")
+
+    def elapsed_ms(self):
+        out = {}
+        for i, name in enumerate(STAGES):
+            out[name] = self.events[2 * i].elapsed_time(self.events[2 * i + 1])
+        return out
+
+
+def kernel_launches() -> int:
+    return int(lib().moe_kernel_launches())
 
 
 def status_string(st: int) -> str:

@@ -2,8 +2,24 @@
 // checks, workspace layout, kernel sequencing on the caller's stream.
 #include <stdio.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace moe {
+static std::atomic<unsigned long long> g_launches{0};
+static std::atomic<void* const*> g_trace{nullptr};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+void trace_begin(int stage, cudaStream_t s) {
+  void* const* ev = g_trace.load(std::memory_order_relaxed);
+  if (ev) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[2 * stage]), s);
+}
+void trace_end(int stage, cudaStream_t s) {
+  void* const* ev = g_trace.load(std::memory_order_relaxed);
+  if (ev) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[2 * stage + 1]), s);
+}
+}  // namespace moe
 
 using namespace moe;
 
@@ -61,6 +77,14 @@ struct Carve {
   }
 };
 
+// Records the stage-boundary events of moe_trace_events, when enabled.
+struct Stage {
+  cudaStream_t s;
+  int i;
+  Stage(cudaStream_t s_, int stage) : s(s_), i(stage) { trace_begin(i, s); }
+  ~Stage() { trace_end(i, s); }
+};
+
 #define MOE_TRY(expr)                        \
   do {                                       \
     cudaError_t e_ = (expr);                 \
@@ -85,6 +109,13 @@ const char* moe_status_string(moe_status_t st) {
 }
 
 int moe_version(void) { return 100; }
+
+moe_status_t moe_trace_events(void* const* events) {
+  g_trace.store(events, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+unsigned long long moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 moe_status_t moe_route(const uint16_t* x, const float* w_gate, const float* bias, int T, int d,
                        int E, int R, float* logits, int32_t* topk_idx, float* topk_w,
@@ -220,13 +251,27 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   void* dws = c.take(dispatch_ws_bytes(T, E));
   void* tws = c.take(tiles_ws_bytes(N, E));
   MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
-  MOE_TRY(launch_gate_logits(x, L->w_gate, L->bias, T, d, E, sv->logits, s));
-  MOE_TRY(launch_topk(sv->logits, T, E, R, sv->topk_idx, sv->topk_w, s));
-  MOE_TRY(launch_dispatch(x, sv->topk_idx, T, d, E, R, sv->counts, sv->offsets, sv->row_slot,
-                          sv->slot_row, sv->x_perm, dws, err, s));
+  {
+    Stage st_(s, MOE_STAGE_GATE);
+    MOE_TRY(launch_gate_logits(x, L->w_gate, L->bias, T, d, E, sv->logits, s));
+  }
+  {
+    Stage st_(s, MOE_STAGE_TOPK);
+    MOE_TRY(launch_topk(sv->logits, T, E, R, sv->topk_idx, sv->topk_w, s));
+  }
+  {
+    Stage st_(s, MOE_STAGE_DISPATCH);
+    MOE_TRY(launch_dispatch(x, sv->topk_idx, T, d, E, R, sv->counts, sv->offsets, sv->row_slot,
+                            sv->slot_row, sv->x_perm, dws, err, s));
+  }
   MOE_TRY(launch_ffn_fwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
                          sv->h, sv->o, tws, err, s));
-  return finish(launch_combine(sv->o, sv->slot_row, sv->topk_w, T, d, R, y, s), err, flags, s);
+  cudaError_t e;
+  {
+    Stage st_(s, MOE_STAGE_COMBINE);
+    e = launch_combine(sv->o, sv->slot_row, sv->topk_w, T, d, R, y, s);
+  }
+  return finish(e, err, flags, s);
 }
 
 static size_t layer_bwd_ws(const moe_layer_t* L) {
@@ -282,13 +327,25 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
     MOE_TRY(cudaMemsetAsync(dW3, 0, sizeof(float) * E * f * d, s));
     return finish(cudaMemsetAsync(dW2, 0, sizeof(float) * E * f * d, s), err, flags, s);
   }
-  MOE_TRY(launch_bwd_route(dy, sv->o, sv->slot_row, sv->topk_w, T, d, R, dO, dsel_tok, dsel_row, s));
+  {
+    Stage st_(s, MOE_STAGE_BWD_ROUTE);
+    MOE_TRY(launch_bwd_route(dy, sv->o, sv->slot_row, sv->topk_w, T, d, R, dO, dsel_tok, dsel_row,
+                             s));
+  }
   MOE_TRY(launch_ffn_bwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
                          sv->h, dO, dab, dxp, dW1, dW3, dW2, tws, err, s));
-  MOE_TRY(launch_dwg(sv->x_perm, sv->offsets, dsel_row, d, E, dW_gate, s));
-  MOE_TRY(launch_wg_transpose(L->w_gate, d, E, wgT, s));
-  return finish(launch_dx_combine(dxp, sv->slot_row, sv->topk_idx, dsel_tok, wgT, T, d, E, R, dx, s),
-                err, flags, s);
+  {
+    Stage st_(s, MOE_STAGE_BWD_DWG);
+    MOE_TRY(launch_dwg(sv->x_perm, sv->offsets, dsel_row, d, E, dW_gate, s));
+  }
+  cudaError_t e;
+  {
+    Stage st_(s, MOE_STAGE_BWD_DXC);
+    e = launch_wg_transpose(L->w_gate, d, E, wgT, s);
+    if (e == cudaSuccess)
+      e = launch_dx_combine(dxp, sv->slot_row, sv->topk_idx, dsel_tok, wgT, T, d, E, R, dx, s);
+  }
+  return finish(e, err, flags, s);
 }
 
 }  // extern "C"

@@ -175,12 +175,14 @@ cudaError_t launch_bwd_route(const uint16_t* dy, const uint16_t* o, const int32_
   if (T == 0) return cudaSuccess;
   bwd_route_kernel<<<grid_for(T, BW), BW * 32, 0, s>>>(dy, o, slot_row, w, T, d, R, T * R, dO,
                                                       dsel_tok, dsel_row);
+  count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_wg_transpose(const float* wg, int d, int E, float* wgT, cudaStream_t s) {
   dim3 grid(ceil_div(d, 32), ceil_div(E, 32));
   wg_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(wg, d, E, wgT);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -188,6 +190,7 @@ cudaError_t launch_dwg(const uint16_t* x_perm, const int32_t* offsets, const flo
                        int d, int E, float* dW_gate, cudaStream_t s) {
   dim3 grid(ceil_div(d, 256), E);
   dwg_kernel<<<grid, 256, 0, s>>>(x_perm, offsets, dsel_row, d, E, dW_gate);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -197,6 +200,7 @@ cudaError_t launch_dx_combine(const uint16_t* dx_perm, const int32_t* slot_row,
   if (T == 0) return cudaSuccess;
   dx_combine_kernel<<<grid_for(T, BW), BW * 32, 0, s>>>(dx_perm, slot_row, idx, dsel_tok, wgT, T,
                                                        d, E, R, T * R, dx);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -62,6 +62,7 @@ cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const flo
   if (T == 0) return cudaSuccess;
   const int blocks = ceil_div(T, CW) < 152 * 8 ? ceil_div(T, CW) : 152 * 8;
   combine_kernel<<<blocks, CW * 32, 0, s>>>(o, slot_row, w, T, d, R, T * R, y);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -225,9 +225,11 @@ cudaError_t launch_dispatch(const uint16_t* x, const int32_t* idx, int T, int d,
   expert_scan_kernel<<<1, 1024, 0, s>>>(blk_counts, E, nblk, blk_base, counts, offsets);
   const size_t rank_smem = sizeof(int32_t) * ((size_t)DWARPS * E + (size_t)CHUNK * R);
   slot_rank_kernel<<<nblk, 256, rank_smem, s>>>(idx, T, E, R, nblk, blk_base, row_slot, slot_row);
+  count_launches(3);
   if (x != nullptr && x_perm != nullptr) {
     const int blocks = ceil_div(T, 8) < 152 * 8 ? ceil_div(T, 8) : 152 * 8;
     permute_rows_kernel<<<blocks, 256, 0, s>>>(x, T, d, R, T * R, slot_row, x_perm);
+    count_launches(1);
   }
   return cudaGetLastError();
 }

@@ -487,6 +487,7 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   if (max_items <= 0) return cudaSuccess;
   const int grid = (int)std::min<long long>(sm_count(), max_items);
   grouped_gemm_kernel<MODE><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, b2, g);
+  count_launches(1);
   return cudaGetLastError();
 }
 }  // namespace
@@ -499,6 +500,7 @@ cudaError_t launch_build_tiles(const int32_t* offsets, int E, void* ws, cudaStre
   int32_t* count = static_cast<int32_t*>(ws);
   int2* tiles = reinterpret_cast<int2*>(static_cast<uint8_t*>(ws) + 16);
   build_tiles_kernel<<<1, 1024, 0, s>>>(offsets, E, tiles, count);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -508,6 +510,7 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
                            void* tiles_ws, int* err, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
+  trace_begin(MOE_STAGE_GATEUP, s);
   cudaError_t e = launch_build_tiles(offsets, E, tiles_ws, s);
   if (e != cudaSuccess) return e;
   GemmArgs g{};
@@ -526,6 +529,7 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.n_tiles_n = ceil_div(f, 128);
   g.out_bf16 = h; g.save_a = a_save; g.save_b = b_save;
   e = launch_mode<GATEUP>(ma, mb, mb2, g, max_m_tiles * g.n_tiles_n, s);
+  trace_end(MOE_STAGE_GATEUP, s);
   if (e != cudaSuccess) return e;
   // down: A = h, B = W2 rows (256 per tile)
   if (!make_map(&ma, h, N, f, BM) || !make_map(&mb, W2, (long long)E * d, f, BN))
@@ -533,7 +537,10 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.kblocks = ceil_div(f, BK);
   g.n_tiles_n = ceil_div(d, BN);
   g.out_bf16 = out; g.save_a = g.save_b = nullptr;
-  return launch_mode<DOWN>(ma, mb, mb, g, max_m_tiles * g.n_tiles_n, s);
+  trace_begin(MOE_STAGE_DOWN, s);
+  e = launch_mode<DOWN>(ma, mb, mb, g, max_m_tiles * g.n_tiles_n, s);
+  trace_end(MOE_STAGE_DOWN, s);
+  return e;
 }
 
 // Backward contractions.  d % 64 == 0 and f % 64 == 0 are required.
@@ -551,6 +558,7 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.err = err;
   CUtensorMap ma, mb, mb2;
   if (N > 0) {
+    trace_begin(MOE_STAGE_BWD_DH, s);
     e = launch_build_tiles(offsets, E, tiles_ws, s);
     if (e != cudaSuccess) return e;
     const long long max_m_tiles = ceil_div(N, BM) + E;
@@ -561,6 +569,7 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
     g.n_tiles_n = ceil_div(f, BN);
     g.out_bf16 = dab; g.in_a = a_s; g.in_b = b_s;
     e = launch_mode<DH>(ma, mb, mb, g, max_m_tiles * g.n_tiles_n, s);
+    trace_end(MOE_STAGE_BWD_DH, s);
     if (e != cudaSuccess) return e;
     // dx_perm = [da | db] [W1[e]; W3[e]] (B MN-major: W1, W3 viewed [E*f, d])
     if (!make_map(&ma, dab, N, 2LL * f, BM) || !make_map(&mb, W1, (long long)E * f, d, 64) ||
@@ -569,7 +578,9 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
     g.kblocks = 2 * f / BK;
     g.n_tiles_n = ceil_div(d, BN);
     g.out_bf16 = dx_perm;
+    trace_begin(MOE_STAGE_BWD_DX, s);
     e = launch_mode<DX>(ma, mb, mb2, g, max_m_tiles * g.n_tiles_n, s);
+    trace_end(MOE_STAGE_BWD_DX, s);
     if (e != cudaSuccess) return e;
   }
   // dW2[e] = do^T h: A = do [N, d] MN-major, B = h [N, f] MN-major
@@ -578,7 +589,9 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.n_tiles_m = ceil_div(d, BM);
   g.n_tiles_n = ceil_div(f, BN);
   g.out_f32 = dW2;
+  trace_begin(MOE_STAGE_BWD_WG2, s);
   e = launch_mode<WG2>(ma, mb, mb, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
+  trace_end(MOE_STAGE_BWD_WG2, s);
   if (e != cudaSuccess) return e;
   // [dW1[e]; dW3[e]] = [da | db]^T x_perm: A = dab [N, 2f], B = x_perm [N, d]
   if (!make_map(&ma, dab, rows, 2LL * f, 64) || !make_map(&mb, x_perm, rows, d, 64))
@@ -586,7 +599,10 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.n_tiles_m = ceil_div(2 * f, BM);
   g.n_tiles_n = ceil_div(d, BN);
   g.out_f32 = dW1; g.out_f32b = dW3;
-  return launch_mode<WG13>(ma, mb, mb, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
+  trace_begin(MOE_STAGE_BWD_WG13, s);
+  e = launch_mode<WG13>(ma, mb, mb, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
+  trace_end(MOE_STAGE_BWD_WG13, s);
+  return e;
 }
 
 }  // namespace moe

@@ -7,6 +7,12 @@
 
 namespace moe {
 
+// Adds n to the process-wide count of kernels launched by the library.
+void count_launches(int n);
+// Record the caller's trace events around stage `stage` (moe_stage_t), if tracing is on.
+void trace_begin(int stage, cudaStream_t s);
+void trace_end(int stage, cudaStream_t s);
+
 // Arguments of the grouped tcgen05 GEMM kernel (one struct for all modes).
 struct GemmArgs {
   int E, N, d, f;

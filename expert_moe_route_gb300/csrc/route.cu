@@ -144,6 +144,7 @@ cudaError_t launch_gate_logits(const uint16_t* x, const float* wg, const float* 
   if (T == 0) return cudaSuccess;
   dim3 grid(ceil_div(E, GL_BN), ceil_div(T, GL_BM));
   gate_logits_kernel<<<grid, 256, 0, s>>>(x, wg, bias, T, d, E, logits);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -160,6 +161,7 @@ cudaError_t launch_topk(const float* logits, int T, int E, int R, int32_t* idx, 
   else if (epl <= 16) MOE_TOPK(16);
   else MOE_TOPK(32);
 #undef MOE_TOPK
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -65,6 +65,37 @@ typedef void* moe_stream_t;  /* cudaStream_t */
 #define MOE_LOGITS_IN 0x1u   /* moe_route: `logits` is an input; skip the gate projection */
 #define MOE_CHECK 0x2u       /* wait for the call's work and report device-side errors */
 
+/* Stages of moe_layer_fwd / moe_layer_bwd, for moe_trace_events. */
+typedef enum {
+  MOE_STAGE_GATE = 0,      /* router projection (logits) */
+  MOE_STAGE_TOPK,          /* softmax top-R */
+  MOE_STAGE_DISPATCH,      /* histogram, scan, stable rank, row copies */
+  MOE_STAGE_GATEUP,        /* tile list + grouped x W1^T | x W3^T with the SwiGLU epilogue */
+  MOE_STAGE_DOWN,          /* grouped h W2^T */
+  MOE_STAGE_COMBINE,       /* weighted gather-sum */
+  MOE_STAGE_BWD_ROUTE,     /* dw, do, router logit gradient */
+  MOE_STAGE_BWD_DH,        /* tile list + grouped do W2 with the SwiGLU backward epilogue */
+  MOE_STAGE_BWD_DX,        /* grouped [da|db] [W1;W3] */
+  MOE_STAGE_BWD_WG2,       /* dW2 = do^T h per expert */
+  MOE_STAGE_BWD_WG13,      /* [dW1;dW3] = [da|db]^T x_perm per expert */
+  MOE_STAGE_BWD_DWG,       /* router weight gradient */
+  MOE_STAGE_BWD_DXC,       /* W_g transpose + dx gather-sum */
+  MOE_STAGE_COUNT
+} moe_stage_t;
+
+/*
+ * moe_trace_events -- per-stage timing (utility; the page has no counterpart).
+ * events: NULL to disable, else 2*MOE_STAGE_COUNT cudaEvent_t handles created
+ * by the caller on the current device; while set, moe_layer_fwd and
+ * moe_layer_bwd record events[2*i] on their stream just before stage i and
+ * events[2*i+1] just after it.  The pointer is kept (not copied) until the
+ * next call; one setting is shared by all threads of the process.
+ */
+moe_status_t moe_trace_events(void* const* events);
+
+/* Number of CUDA kernels this library has launched in this process (utility). */
+unsigned long long moe_kernel_launches(void);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(moe_status_t status);
 

@@ -93,14 +93,17 @@ def test_layer_forward(lib, name, T):
     inp = synth.layer_inputs(wl)
     _, _, saved, y = _layer_run(lib, wl, inp, train=False)
     ref = _oracle_fwd(inp, wl)
+    assert_close(f64(saved.logits), ref["logits"], "logits", max_rel=3e-5, mean_rel=1e-5)
     tie = near_tie_tokens(ref["logits"], wl.R)
-    assert not tie.any(), "near-tied routing in this seed; parity of y would be ambiguous"
-    assert np.array_equal(saved.topk_idx.cpu().numpy(), ref["idx"])
-    assert np.array_equal(saved.offsets.cpu().numpy(), ref["offsets"])
-    assert np.array_equal(saved.slot_row.cpu().numpy(), ref["slot_row"])
-    assert_close(f64(saved.h), ref["h"], "h")
-    assert_close(f64(saved.o), ref["o"], "o")
-    assert_close(f64(y), ref["y"], "y")
+    same = (saved.topk_idx.cpu().numpy() == ref["idx"]).all(axis=1)
+    assert (same | tie).all(), "routing differs on a token without a near tie"
+    if same.all():
+        assert np.array_equal(saved.offsets.cpu().numpy(), ref["offsets"])
+        assert np.array_equal(saved.slot_row.cpu().numpy(), ref["slot_row"])
+        assert_close(f64(saved.h), ref["h"], "h")
+        assert_close(f64(saved.o), ref["o"], "o")
+    # a token's output depends only on its own routing: compare every token routed alike
+    assert_close(f64(y)[same], ref["y"][same], "y")
 
 
 @pytest.mark.parametrize("name,T,E,f", [("tiny", None, None, None), ("train", 512, None, None),
@@ -123,14 +126,21 @@ def test_layer_backward(lib, name, T, E, f):
     ws = lib.workspace(lib.layer_bwd_ws_bytes(layer))
     lib.moe_layer_bwd(layer, dev["x"], saved, dy, dx, dWg, dW1, dW3, dW2, ws, flags=lib.MOE_CHECK)
     ref = _oracle_fwd(inp, wl)
-    assert not near_tie_tokens(ref["logits"], wl.R).any()
-    assert np.array_equal(saved.topk_idx.cpu().numpy(), ref["idx"])
+    gidx = saved.topk_idx.cpu().numpy()
+    same = (gidx == ref["idx"]).all(axis=1)
+    assert (same | near_tie_tokens(ref["logits"], wl.R)).all(), "routing differs without a near tie"
     rb = O.layer_bwd(ref, bits(inp["x"]), inp["w_gate"].numpy(), bits(inp["W1"]), bits(inp["W3"]),
                      bits(inp["W2"]), bits(inp["g"]), wl.R)
-    assert_close(f64(dx), rb["dx"], "dx")
-    assert_close(f64(dWg), rb["dW_gate"], "dW_gate")
-    assert_close(f64(dW1), rb["dW1"], "dW1")
-    assert_close(f64(dW3), rb["dW3"], "dW3")
-    assert_close(f64(dW2), rb["dW2"], "dW2")
+    # a token routed differently (near tie) changes only its own dx and the weight
+    # gradients of the experts it touched on either side
+    touched = np.zeros(wl.E, dtype=bool)
+    touched[np.unique(np.concatenate([gidx[~same].ravel(), ref["idx"][~same].ravel()]))] = True
+    keep = ~touched
+    assert_close(f64(dx)[same], rb["dx"][same], "dx")
+    assert_close(f64(dWg)[:, keep], rb["dW_gate"][:, keep], "dW_gate")
+    assert_close(f64(dW1)[keep], rb["dW1"][keep], "dW1")
+    assert_close(f64(dW3)[keep], rb["dW3"][keep], "dW3")
+    assert_close(f64(dW2)[keep], rb["dW2"][keep], "dW2")
     for e in np.nonzero(ref["counts"] == 0)[0]:
-        assert not dW1[e].any() and not dW2[e].any() and not dWg[:, e].any()
+        if keep[e]:
+            assert not dW1[e].any() and not dW2[e].any() and not dWg[:, e].any()
