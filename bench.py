@@ -256,9 +256,15 @@ def run_ours(args, rank, world, device):
             stage_ms[name] = stage_ms.get(name, 0.0) + ms / args.steps
     pk, pk_src = load_peaks()
     work = stage_work(wl)
+    if identity:
+        ran = ("dispatch", "combine")
+    elif train:
+        ran = tuple(work)
+    else:
+        ran = ("gate", "topk", "dispatch", "gateup", "down", "combine")
     stages = {}
     for name, ms in stage_ms.items():
-        if name not in work or ms <= 0:
+        if name not in ran or ms <= 0:
             continue
         kind, amount = work[name]
         if kind == "tflop":

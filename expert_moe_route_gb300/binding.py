@@ -271,14 +271,15 @@ class StageTrace:
 
     def __init__(self):
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(STAGES))]
-        self._arr = (_vp * len(self.events))(*[e.cuda_event for e in self.events])
-        self.used = False
+        self._arr = None
 
     def arm(self):
-        for e in self.events:    # make every event "recorded" so unused stages read as 0
+        # torch creates an event's CUDA handle at its first record(): record every
+        # event once (unused stages then read as ~0) before handing the handles over
+        for e in self.events:
             e.record()
+        self._arr = (_vp * len(self.events))(*[e.cuda_event for e in self.events])
         _check(lib().moe_trace_events(self._arr), "moe_trace_events")
-        self.used = True
 
     @staticmethod
     def disarm():

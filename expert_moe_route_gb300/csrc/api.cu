@@ -11,14 +11,14 @@ namespace moe {
 static std::atomic<unsigned long long> g_launches{0};
 static std::atomic<void* const*> g_trace{nullptr};
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
-void trace_begin(int stage, cudaStream_t s) {
+// A failed trace record must not surface later as a launch error: clear it.
+static void trace_record(int slot, cudaStream_t s) {
   void* const* ev = g_trace.load(std::memory_order_relaxed);
-  if (ev) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[2 * stage]), s);
+  if (ev && ev[slot] && cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[slot]), s) != cudaSuccess)
+    (void)cudaGetLastError();
 }
-void trace_end(int stage, cudaStream_t s) {
-  void* const* ev = g_trace.load(std::memory_order_relaxed);
-  if (ev) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[2 * stage + 1]), s);
-}
+void trace_begin(int stage, cudaStream_t s) { trace_record(2 * stage, s); }
+void trace_end(int stage, cudaStream_t s) { trace_record(2 * stage + 1, s); }
 }  // namespace moe
 
 using namespace moe;
@@ -136,8 +136,16 @@ moe_status_t moe_route(const uint16_t* x, const float* w_gate, const float* bias
   }
   if (!init_once()) return MOE_ERR_CUDA;
   cudaStream_t s = S(stream);
-  if (!logits_in) MOE_TRY(launch_gate_logits(x, w_gate, bias, T, d, E, logits, s));
-  return finish(launch_topk(logits, T, E, R, topk_idx, topk_w, s), nullptr, flags, s);
+  if (!logits_in) {
+    Stage st_(s, MOE_STAGE_GATE);
+    MOE_TRY(launch_gate_logits(x, w_gate, bias, T, d, E, logits, s));
+  }
+  cudaError_t e;
+  {
+    Stage st_(s, MOE_STAGE_TOPK);
+    e = launch_topk(logits, T, E, R, topk_idx, topk_w, s);
+  }
+  return finish(e, nullptr, flags, s);
 }
 
 moe_status_t moe_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int R,
@@ -161,8 +169,12 @@ moe_status_t moe_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int
   cudaStream_t s = S(stream);
   int* err = static_cast<int*>(ws);
   MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
-  cudaError_t e = launch_dispatch(x, topk_idx, T, d, E, R, counts, offsets, row_slot, slot_row,
-                                  x_perm, static_cast<uint8_t*>(ws) + kErrBytes, err, s);
+  cudaError_t e;
+  {
+    Stage st_(s, MOE_STAGE_DISPATCH);
+    e = launch_dispatch(x, topk_idx, T, d, E, R, counts, offsets, row_slot, slot_row, x_perm,
+                        static_cast<uint8_t*>(ws) + kErrBytes, err, s);
+  }
   return finish(e, err, flags, s);
 }
 
@@ -203,7 +215,12 @@ moe_status_t moe_combine(const uint16_t* expert_out, const int32_t* slot_row, co
   if (!expert_out || !slot_row || !y) return MOE_ERR_INVALID_ARG;
   if (!al16(expert_out) || !al16(y)) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = S(stream);
-  return finish(launch_combine(expert_out, slot_row, topk_w, T, d, R, y, s), nullptr, 0, s);
+  cudaError_t e;
+  {
+    Stage st_(s, MOE_STAGE_COMBINE);
+    e = launch_combine(expert_out, slot_row, topk_w, T, d, R, y, s);
+  }
+  return finish(e, nullptr, 0, s);
 }
 
 static moe_status_t check_layer(const moe_layer_t* L) {
