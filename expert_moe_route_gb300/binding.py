@@ -22,8 +22,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 
 # the C ABI's exported symbols (checked against include/moe.h by the tests)
 SYMBOLS = ("moe_status_string", "moe_version", "moe_trace_events", "moe_kernel_launches",
-           "moe_route", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_layer_fwd",
-           "moe_layer_bwd")
+           "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_grouped_ffn",
+           "moe_combine", "moe_layer_fwd", "moe_layer_bwd")
 
 # moe_stage_t
 STAGES = ("gate", "topk", "dispatch", "gateup", "down", "combine", "bwd_route", "bwd_dh", "bwd_dx",
@@ -66,6 +66,9 @@ def _declare(lib):
     lib.moe_dispatch.restype = _i
     lib.moe_dispatch.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _szp, _u,
                                  _vp]
+    lib.moe_dispatch_noalloc.restype = _i
+    lib.moe_dispatch_noalloc.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _u,
+                                         _vp]
     lib.moe_grouped_ffn.restype = _i
     lib.moe_grouped_ffn.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _vp, _szp, _u, _vp]
@@ -156,6 +159,21 @@ def moe_dispatch(x, topk_idx, E, counts, offsets, row_slot, slot_row, x_perm, ws
                             _p(row_slot), _p(slot_row), _p(x_perm), _p(ws), ctypes.byref(n),
                             flags, _stream(stream))
     _check(st, "moe_dispatch")
+
+
+def moe_dispatch_noalloc(x, topk_idx, E, counts, offsets, row_slot, slot_row, x_perm, flags=0,
+                         stream=None):
+    """moe_dispatch with the library's static scratch (no workspace argument)."""
+    T, R = topk_idx.shape
+    d = x.shape[1] if x is not None else (x_perm.shape[1] if x_perm is not None else 8)
+    _dt(x, torch.bfloat16, "x"); _dt(x_perm, torch.bfloat16, "x_perm")
+    for name, t in (("topk_idx", topk_idx), ("counts", counts), ("offsets", offsets),
+                    ("row_slot", row_slot), ("slot_row", slot_row)):
+        _dt(t, torch.int32, name)
+    st = lib().moe_dispatch_noalloc(_p(x), _p(topk_idx), T, d, E, R, _p(counts), _p(offsets),
+                                    _p(row_slot), _p(slot_row), _p(x_perm), flags,
+                                    _stream(stream))
+    _check(st, "moe_dispatch_noalloc")
 
 
 def grouped_ffn_ws_bytes(N, d, f, E) -> int:

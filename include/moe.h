@@ -167,6 +167,30 @@ moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int
 moe_status_t moe_combine(const uint16_t* expert_out, const int32_t* slot_row, const float* topk_w,
                          int T, int d, int R, uint16_t* y, moe_stream_t stream);
 
+/*
+ * moe_dispatch_noalloc -- moe_dispatch without a workspace argument, for
+ * callers that cannot allocate device memory: code running inside a host
+ * application or framework whose allocator owns all device memory, and
+ * latency-critical loops that cannot afford cudaMalloc's implicit device
+ * synchronisation.  (The page has no counterpart; this is a packaging of the
+ * dispatch step above.)
+ * Same arguments, results and error behaviour as moe_dispatch.  Its scratch
+ * (the device error word and 2*E*ceil(T/256) int32 histogram entries) lives in
+ * a 4 MiB array that the library reserves statically on every GPU that loads
+ * it, until the process exits; calls whose scratch would not fit
+ * (256 + 8*E*ceil(T/256) bytes, rounded up to 256, above 4 MiB) return
+ * MOE_ERR_WORKSPACE before anything is enqueued.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.  The first call on each device looks
+ * up the array's device address (set-up; make that first call before any
+ * stream capture).  Every call uses the same array and clears its error word
+ * first; calls that may overlap on the GPU (different streams, or different
+ * host threads) race on it and must be serialised by the caller.
+ */
+moe_status_t moe_dispatch_noalloc(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E,
+                                  int R, int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                                  int32_t* slot_row, uint16_t* x_perm, unsigned flags,
+                                  moe_stream_t stream);
+
 /* Layer parameters (device pointers, caller-owned). */
 typedef struct {
   int T, d, E, R, f;
