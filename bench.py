@@ -48,6 +48,7 @@ def parse():
                    choices=["train", "large", "large_hot", "mid", "tiny", "dispatch",
                             "dispatch_zipf"])
     p.add_argument("--tokens", type=int, default=None, help="override T")
+    p.add_argument("--experts", type=int, default=None, help="override E (smaller profiling cases)")
     p.add_argument("--cpu-tokens", type=int, default=None,
                    help="tokens in the CPU oracle sample (default per workload)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -147,6 +148,32 @@ def stage_work(wl):
     return w
 
 
+def kernel_sources_digest():
+    """sha256 over the CUDA sources; ncu traffic is void once they change."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "expert_moe_route_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload, stage):
+    """DRAM bytes per launch of a stage's kernel from the committed ncu summary, or None
+    when there is none for this workload or the kernels changed since it was taken."""
+    try:
+        with open(PROFILE_TRAFFIC) as fh:
+            table = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if table.get("kernel_sources_sha256") != kernel_sources_digest():
+        return None
+    entry = table.get("workloads", {}).get(workload, {}).get(stage)
+    return entry.get("bytes_per_launch") if entry else None
+
+
 def alu_peak_tflops(sm_mhz):
     """FP32 FMA peak: 152 SMs x 128 lanes x 2 FLOP per cycle."""
     return 152 * 128 * 2 * (sm_mhz or 2070.0) * 1e6 / 1e12
@@ -159,8 +186,7 @@ def run_ours(args, rank, world, device):
     from expert_moe_route_gb300 import binding as B
     from expert_moe_route_gb300 import synth
 
-    over = {} if args.tokens is None else {"T": args.tokens}
-    wl = synth.workload(args.workload, **over)
+    wl = synth.workload(args.workload, **overrides(args))
     identity = wl.f == 0
     stream = torch.cuda.current_stream()
 
@@ -247,7 +273,7 @@ def run_ours(args, rank, world, device):
     ms_total = world_max(ms_total, world, device)
     ms_step = ms_total / args.steps
     tokens_per_step = wl.T
-    value = tokens_per_step * world * args.steps / (ms_total / 1e3)
+    value = job_tokens_per_s(tokens_per_step, world, args.steps, ms_total)
 
     # ---- per-stage device time, averaged over the timed steps
     stage_ms = {}
@@ -281,13 +307,7 @@ def run_ours(args, rank, world, device):
                             "frac": round(ach / alu_peak_tflops(clk.get("sm_mhz")), 4)}
     dom = max(stages, key=lambda n: stages[n]["ms"])
     kind, amount = work[dom]
-    traffic = None
-    try:
-        with open(PROFILE_TRAFFIC) as fh:
-            tr = json.load(fh).get(wl.name, {}).get(dom)
-            traffic = tr.get("bytes_per_launch") if tr else None
-    except (OSError, ValueError):
-        traffic = None
+    traffic = profiled_traffic(wl.name, dom)
     if kind == "tflop":
         roof = {"bound": "tensor", "kernel": dom, "achieved": stages[dom]["tflops"],
                 "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
@@ -349,7 +369,7 @@ def run_ours(args, rank, world, device):
         e1.record(stream)
         torch.cuda.synchronize()
         ems = world_max(e0.elapsed_time(e1), world, device)
-        e2e = {"value": round(tokens_per_step * world * args.steps / (ems / 1e3), 1),
+        e2e = {"value": round(job_tokens_per_s(tokens_per_step, world, args.steps, ems), 1),
                "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "ms_per_step": round(ems / args.steps, 4)}
 
@@ -432,6 +452,15 @@ def cpu_oracle_sample(wl, device, n_tokens, steps=1):
     return n * steps / dt, dt, n
 
 
+def overrides(args):
+    over = {}
+    if args.tokens is not None:
+        over["T"] = args.tokens
+    if args.experts is not None:
+        over["E"] = args.experts
+    return over
+
+
 def world_barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -439,13 +468,20 @@ def world_barrier(world):
 
 
 def world_max(v, world, device):
+    """The maximum of v over all ranks (NCCL on GPUs, gloo on the host)."""
     if world <= 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_step, world, steps, ms_total):
+    """Whole-job throughput: the tokens all ranks processed over the slowest rank's time."""
+    return tokens_per_step * world * steps / (ms_total / 1e3)
 
 
 def default_cpu_tokens(wl):
@@ -465,8 +501,7 @@ def main():
         if rank != 0:
             return
         from expert_moe_route_gb300 import synth
-        over = {} if args.tokens is None else {"T": args.tokens}
-        wl = synth.workload(args.workload, **over)
+        wl = synth.workload(args.workload, **overrides(args))
         n = args.cpu_tokens or (8 if wl.f else 1024)
         device = "cuda:0"
         try:

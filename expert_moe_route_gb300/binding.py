@@ -22,6 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 
 # the C ABI's exported symbols (checked against include/moe.h by the tests)
 SYMBOLS = ("moe_status_string", "moe_version", "moe_trace_events", "moe_kernel_launches",
+           "moe_selftest_wait_timeout",
            "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_grouped_ffn",
            "moe_combine", "moe_layer_fwd", "moe_layer_bwd")
 
@@ -61,8 +62,10 @@ def _declare(lib):
     lib.moe_trace_events.argtypes = [ctypes.POINTER(_vp)]
     lib.moe_kernel_launches.restype = ctypes.c_ulonglong
     lib.moe_kernel_launches.argtypes = []
+    lib.moe_selftest_wait_timeout.restype = _i
+    lib.moe_selftest_wait_timeout.argtypes = [_u, _vp, _vp]
     lib.moe_route.restype = _i
-    lib.moe_route.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _u, _vp]
+    lib.moe_route.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _szp, _u, _vp]
     lib.moe_dispatch.restype = _i
     lib.moe_dispatch.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _szp, _u,
                                  _vp]
@@ -127,15 +130,24 @@ def _dt(t, dtype, name):
 
 
 # ---------------------------------------------------------------- entry points
-def moe_route(x, w_gate, bias, logits, topk_idx, topk_w, flags=0, stream=None):
+def route_ws_bytes(T, d, E, R) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_route(None, None, None, T, d, E, R, None, None, None, None, ctypes.byref(n),
+                           0, None), "moe_route(ws query)")
+    return n.value
+
+
+def moe_route(x, w_gate, bias, logits, topk_idx, topk_w, ws=None, flags=0, stream=None):
+    """Router; ``ws`` may be None with MOE_LOGITS_IN (else see route_ws_bytes)."""
     T, E = logits.shape
     R = topk_idx.shape[1]
     d = x.shape[1] if x is not None else 0
     _dt(x, torch.bfloat16, "x"); _dt(w_gate, torch.float32, "w_gate"); _dt(bias, torch.float32, "bias")
     _dt(logits, torch.float32, "logits"); _dt(topk_idx, torch.int32, "topk_idx")
     _dt(topk_w, torch.float32, "topk_w")
+    n = ctypes.c_size_t(0 if ws is None else ws.numel())
     st = lib().moe_route(_p(x), _p(w_gate), _p(bias), T, d, E, R, _p(logits), _p(topk_idx),
-                         _p(topk_w), flags, _stream(stream))
+                         _p(topk_w), _p(ws), ctypes.byref(n), flags, _stream(stream))
     _check(st, "moe_route")
 
 

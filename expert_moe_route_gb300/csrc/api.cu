@@ -117,9 +117,30 @@ moe_status_t moe_trace_events(void* const* events) {
 
 unsigned long long moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+moe_status_t moe_selftest_wait_timeout(unsigned limit_us, void* ws, moe_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u || !ws) return MOE_ERR_INVALID_ARG;
+  if (!al256(ws)) return MOE_ERR_WORKSPACE;
+  if (!init_once()) return MOE_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  int* err = static_cast<int*>(ws);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  return finish(launch_selftest_wait(limit_us, err, s), err, MOE_CHECK, s);
+}
+
+static size_t gate_ws_bytes(int d, int E) {
+  return gate_tc_supported(d) ? gate_tc_ws_bytes(d, E) : 0;
+}
+
+// Gate projection: tensor-core split path when d % 64 == 0, else fp32 FMA.
+static cudaError_t launch_gate(const uint16_t* x, const float* w_gate, const float* bias, int T,
+                               int d, int E, float* logits, void* gws, int* err, cudaStream_t s) {
+  if (gate_tc_supported(d)) return launch_gate_tc(x, w_gate, bias, T, d, E, logits, gws, err, s);
+  return launch_gate_logits(x, w_gate, bias, T, d, E, logits, s);
+}
+
 moe_status_t moe_route(const uint16_t* x, const float* w_gate, const float* bias, int T, int d,
-                       int E, int R, float* logits, int32_t* topk_idx, float* topk_w,
-                       unsigned flags, moe_stream_t stream) {
+                       int E, int R, float* logits, int32_t* topk_idx, float* topk_w, void* ws,
+                       size_t* ws_bytes, unsigned flags, moe_stream_t stream) {
   const bool logits_in = flags & MOE_LOGITS_IN;
   if (logits_in) {
     if (T < 0 || E <= 0 || R <= 0 || R > E) return MOE_ERR_INVALID_ARG;
@@ -127,6 +148,13 @@ moe_status_t moe_route(const uint16_t* x, const float* w_gate, const float* bias
   } else {
     moe_status_t st = shape_check(T, d, E, R);
     if (st != MOE_OK) return st;
+    if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+    const size_t need = kErrBytes + gate_ws_bytes(d, E);
+    if (!ws) {
+      *ws_bytes = need;
+      return MOE_OK;
+    }
+    if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
   }
   if (T == 0) return MOE_OK;
   if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
@@ -136,16 +164,20 @@ moe_status_t moe_route(const uint16_t* x, const float* w_gate, const float* bias
   }
   if (!init_once()) return MOE_ERR_CUDA;
   cudaStream_t s = S(stream);
+  int* err = nullptr;
   if (!logits_in) {
+    err = static_cast<int*>(ws);
+    MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
     Stage st_(s, MOE_STAGE_GATE);
-    MOE_TRY(launch_gate_logits(x, w_gate, bias, T, d, E, logits, s));
+    MOE_TRY(launch_gate(x, w_gate, bias, T, d, E, logits, static_cast<uint8_t*>(ws) + kErrBytes,
+                        err, s));
   }
   cudaError_t e;
   {
     Stage st_(s, MOE_STAGE_TOPK);
     e = launch_topk(logits, T, E, R, topk_idx, topk_w, s);
   }
-  return finish(e, nullptr, flags, s);
+  return finish(e, err, flags, s);
 }
 
 moe_status_t moe_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int R,
@@ -236,7 +268,8 @@ static moe_status_t check_layer(const moe_layer_t* L) {
 
 static size_t layer_fwd_ws(const moe_layer_t* L) {
   const int N = L->T * L->R;
-  return kErrBytes + align_up(dispatch_ws_bytes(L->T, L->E), 256) + tiles_ws_bytes(N, L->E);
+  return kErrBytes + align_up(dispatch_ws_bytes(L->T, L->E), 256) + tiles_ws_bytes(N, L->E) +
+         align_up(gate_ws_bytes(L->d, L->E), 256);
 }
 
 moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
@@ -267,10 +300,11 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   int* err = static_cast<int*>(c.take(kErrBytes));
   void* dws = c.take(dispatch_ws_bytes(T, E));
   void* tws = c.take(tiles_ws_bytes(N, E));
+  void* gws = c.take(gate_ws_bytes(d, E));
   MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
   {
     Stage st_(s, MOE_STAGE_GATE);
-    MOE_TRY(launch_gate_logits(x, L->w_gate, L->bias, T, d, E, sv->logits, s));
+    MOE_TRY(launch_gate(x, L->w_gate, L->bias, T, d, E, sv->logits, gws, err, s));
   }
   {
     Stage st_(s, MOE_STAGE_TOPK);

@@ -55,7 +55,26 @@ __global__ void __launch_bounds__(CW * 32) combine_kernel(const uint16_t* __rest
     __syncwarp();
   }
 }
+// Failure-detection self-test: the barrier expects one arrival that never comes.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+  __syncthreads();
+}
 }  // namespace
+
+cudaError_t launch_selftest_wait(unsigned limit_us, int* err, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>((unsigned long long)limit_us * 1000ull, err);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const float* w, int T,
                            int d, int R, uint16_t* y, cudaStream_t s) {

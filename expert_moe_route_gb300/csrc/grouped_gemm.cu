@@ -33,16 +33,27 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // every mode moves exactly this per k-block
 constexpr int ATOM_BYTES = 64 * BK * 2;         // MN-major block: 64 elements x 64 k-rows
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+constexpr int EPI_WARP_BYTES = 2 * 32 * 128;     // two 32-row x 128-B fp32 staging boxes
+constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;     // per CTA (weight-gradient modes only)
+constexpr int CTL_BYTES = 256;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 
-enum Mode : int { GATEUP = 0, DOWN = 1, DH = 2, DX = 3, WG2 = 4, WG13 = 5 };
+enum Mode : int { GATEUP = 0, DOWN = 1, DH = 2, DX = 3, WG2 = 4, WG13 = 5, GATE = 6 };
 
 template <int M> struct Traits {
   static constexpr bool a_mn = (M == WG2 || M == WG13);
   static constexpr bool b_mn = (M == DH || M == DX || M == WG2 || M == WG13);
   static constexpr bool wgrad = (M == WG2 || M == WG13);
+  static constexpr int epi_bytes = wgrad ? EPI_BYTES : 0;
+  // GATE: 128-column tiles with four partial accumulators (K-blocks rotate over
+  // them; the epilogue adds them in IEEE fp32), so each accumulator takes a
+  // quarter of the tensor core's accumulation steps.
+  static constexpr bool partials = (M == GATE);
+  static constexpr int bn = partials ? 128 : BN;
+  static constexpr uint32_t stage_tx = partials ? A_BYTES + 128 * BK * 2 : STAGE_BYTES;
+  // stages | epilogue staging | control block, plus slack for 1024-B alignment
+  static constexpr int smem_bytes = STAGES * STAGE_BYTES + epi_bytes + CTL_BYTES + 1024;
 };
 
 struct alignas(8) SharedCtl {
@@ -60,6 +71,17 @@ struct Item {
 };
 
 __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int item, Item& it) {
+  if (mode == GATE) {  // one group of T rows: 128-row tiles x 128-expert column tiles
+    const int mi = item / g.n_tiles_n;
+    it.nt = item % g.n_tiles_n;
+    it.row0 = mi * BM;
+    it.row_end = g.N;
+    it.e = 0;
+    it.mt = 0;
+    it.krow0 = 0;
+    it.kblocks = g.kblocks;
+    return true;
+  }
   if (mode == WG2 || mode == WG13) {
     const int per_e = g.n_tiles_m * g.n_tiles_n;
     it.e = item / per_e;
@@ -86,6 +108,7 @@ __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int ite
 
 __device__ __forceinline__ int total_items(const GemmArgs& g, int mode) {
   if (mode == WG2 || mode == WG13) return g.E * g.n_tiles_m * g.n_tiles_n;
+  if (mode == GATE) return g.n_tiles_m * g.n_tiles_n;
   return (*g.tile_count) * g.n_tiles_n;
 }
 
@@ -97,23 +120,18 @@ __device__ __forceinline__ void store_bf16x16(uint16_t* dst, const float* v, int
   if (ncols_left >= 16) reinterpret_cast<uint4*>(dst)[1] = pack8(v + 8);
 }
 
-__device__ __forceinline__ void store_f32x16(float* dst, const float* v, int ncols_left) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    if (ncols_left >= 4 * (q + 1))
-      reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ GemmArgs g) {
+                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
+                    const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ GemmArgs g) {
   using Tr = Traits<MODE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tile_base = (raw_addr + 1023u) & ~1023u;       // 1024-B aligned stages
   uint8_t* tile_ptr = smem_raw + (tile_base - raw_addr);
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(tile_ptr + STAGES * STAGE_BYTES);
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(tile_ptr + STAGES * STAGE_BYTES + Tr::epi_bytes);
+  static_assert(sizeof(SharedCtl) <= CTL_BYTES, "control block");
   volatile int* abort_flag = &ctl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -134,6 +152,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (MODE == GATEUP || MODE == DX) tma_prefetch_desc(&tmB2);
+    if (Tr::wgrad) tma_prefetch_desc(&tmC);
+    if (MODE == WG13) tma_prefetch_desc(&tmC2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -163,13 +183,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t bar = smem_u32(&ctl->full[s]);
           const uint32_t sa = tile_base + s * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(bar, STAGE_BYTES);
+          mbar_arrive_expect_tx(bar, Tr::stage_tx);
           const int kx = kb * BK;
           if (MODE == GATEUP) {
             tma_load_2d(sa, &tmA, bar, kx, it.row0);
             const int brow = it.e * g.f + it.nt * 128;
             tma_load_2d(sb, &tmB, bar, kx, brow);
             tma_load_2d(sb + B_BYTES / 2, &tmB2, bar, kx, brow);
+          } else if (MODE == GATE) {
+            // A repeats x for the hi, mid and lo thirds of K
+            tma_load_2d(sa, &tmA, bar, kx % g.d, it.row0);
+            tma_load_2d(sb, &tmB, bar, kx, it.nt * Tr::bn);
           } else if (MODE == DOWN) {
             tma_load_2d(sa, &tmA, bar, kx, it.row0);
             tma_load_2d(sb, &tmB, bar, kx, it.e * g.d + it.nt * BN);
@@ -209,7 +233,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(BM, BN, Tr::a_mn, Tr::b_mn);
+    constexpr uint32_t idesc = idesc_bf16(BM, Tr::bn, Tr::a_mn, Tr::b_mn);
     uint32_t it_count = 0;
     int j = 0;
     bool ok = true;
@@ -217,13 +241,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++j) {
       Item it;
       decode_item(g, MODE, item, it);
-      const int acc = j & 1;
-      const uint32_t aph = (j >> 1) & 1u;
+      const int acc = Tr::partials ? 0 : (j & 1);
+      const uint32_t aph = Tr::partials ? (j & 1u) : ((j >> 1) & 1u);
       ok = mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, g.err);
       ok = __all_sync(kFull, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
+      const uint32_t d_base = tmem_base + acc * BN;
       for (int kb = 0; kb < it.kblocks; ++kb, ++it_count) {
         const int s = it_count % STAGES;
         const uint32_t ph = (it_count / STAGES) & 1u;
@@ -232,30 +256,40 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (!ok) break;
         const uint32_t sa = tile_base + s * STAGE_BYTES;
         const uint32_t sb = sa + A_BYTES;
+        int kk_end = BK / 16;
         if (Tr::wgrad) {
+          // The expert's last K-block may hold rows of the next expert: issue
+          // MMAs only for the 16-row groups that contain real rows, and zero the
+          // foreign rows inside the last of those groups.
           const int rem = (g.offsets[it.e + 1] - it.krow0) - kb * BK;
-          if (rem < BK) {  // rows past the expert belong to the next one: zero them
-            const int zrows = BK - rem;
-            const int per_atom = zrows * 8;   // 16-byte chunks
-            for (int q = lane; q < 6 * per_atom; q += 32) {
-              const int atom = q / per_atom, w = q % per_atom;
-              const int row = rem + w / 8, chunk = w % 8;
-              uint8_t* p = tile_ptr + s * STAGE_BYTES + atom * ATOM_BYTES + row * 128 + chunk * 16;
-              *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
+          if (rem < BK) {
+            kk_end = ceil_div(rem, 16);
+            const int z1 = kk_end * 16;
+            if (rem < z1) {
+              const int per_atom = (z1 - rem) * 8;   // 16-byte chunks per 64-element block
+              for (int q = lane; q < 6 * per_atom; q += 32) {
+                const int atom = q / per_atom, w = q % per_atom;
+                const int row = rem + w / 8, chunk = w % 8;
+                uint8_t* p = tile_ptr + s * STAGE_BYTES + atom * ATOM_BYTES + row * 128 + chunk * 16;
+                *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
           }
           __syncwarp();
         }
         if (lane == 0) {
           tc_fence_after();
+          const uint32_t d_tmem = Tr::partials ? tmem_base + (kb & 3) * 128 : d_base;
+          const bool first = Tr::partials ? kb < 4 : kb == 0;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk >= kk_end) break;
             const uint64_t ad = Tr::a_mn ? smem_desc_sw128(sa + kk * 2048, ATOM_BYTES, 1024)
                                          : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, ATOM_BYTES, 1024)
                                          : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
           }
           tc_commit(smem_u32(&ctl->empty[s]));   // frees the stage when these MMAs finish
           issued_any = true;
@@ -281,12 +315,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
     const int r_local = q * 32 + lane;   // accumulator row owned by this thread
+    int epi_buf = 0;                     // staging box in use (weight-gradient modes)
     int j = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
       Item it;
       decode_item(g, MODE, item, it);
-      const int acc = j & 1;
-      const uint32_t aph = (j >> 1) & 1u;
+      const int acc = Tr::partials ? 0 : (j & 1);
+      const uint32_t aph = Tr::partials ? (j & 1u) : ((j >> 1) & 1u);
       bool ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag, g.err);
       ok = __all_sync(kFull, ok);
       if (!ok) break;
@@ -313,6 +348,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
           }
         }
+      } else if (MODE == GATE) {
+        const int row = it.row0 + r_local;
+        const bool valid = row < it.row_end;
+        const int parts = it.kblocks < 4 ? it.kblocks : 4;
+        for (int c = 0; c < 128; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_ld_wait();
+          for (int p = 1; p < parts; ++p) {
+            float w[16];
+            tmem_ld16(t_row + p * 128 + c, w);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) v[u] += w[u];
+          }
+          const int col = it.nt * 128 + c;
+          if (valid && col < g.E) {
+            float* dst = g.out_f32 + (size_t)row * g.E + col;
+            const int n = g.E - col < 16 ? g.E - col : 16;
+            for (int u = 0; u < n; ++u) dst[u] = v[u] + (g.bias ? g.bias[col + u] : 0.f);
+          }
+        }
       } else if (MODE == DOWN || MODE == DX) {
         const int row = it.row0 + r_local;
         const bool valid = row < it.row_end;
@@ -326,25 +383,37 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       } else if (MODE == DH) {
         const int row = it.row0 + r_local;
         const bool valid = row < it.row_end;
+        const uint16_t* pa = g.in_a + (size_t)row * g.f;
+        const uint16_t* pb = g.in_b + (size_t)row * g.f;
+        // saved a, b for a 16-column chunk (zeros past the row's end)
+        auto load_ab = [&](int c, uint4* a4, uint4* b4) {
+          const int col = it.nt * BN + c;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          a4[0] = a4[1] = b4[0] = b4[1] = z;
+          if (valid && col < g.f) {
+            a4[0] = ldg_nc_v4(pa + col);
+            b4[0] = ldg_nc_v4(pb + col);
+            if (g.f - col >= 16) {
+              a4[1] = ldg_nc_v4(pa + col + 8);
+              b4[1] = ldg_nc_v4(pb + col + 8);
+            }
+          }
+        };
+        uint4 na[2], nb[2];
+        load_ab(0, na, nb);   // the next chunk's loads are in flight while this one computes
         for (int c = 0; c < BN; c += 16) {
+          uint4 ca[2] = {na[0], na[1]}, cb[2] = {nb[0], nb[1]};
+          if (c + 16 < BN) load_ab(c + 16, na, nb);
           float dh[16];
           tmem_ld16(t_row + c, dh);
           tmem_ld_wait();
           const int col = it.nt * BN + c;
           if (valid && col < g.f) {
-            const size_t off = (size_t)row * g.f + col;
             float a[16], b[16], da[16], db[16];
-            const uint4* pa = reinterpret_cast<const uint4*>(g.in_a + off);
-            const uint4* pb = reinterpret_cast<const uint4*>(g.in_b + off);
-            unpack8(pa[0], a);
-            unpack8(pb[0], b);
-            if (g.f - col >= 16) {
-              unpack8(pa[1], a + 8);
-              unpack8(pb[1], b + 8);
-            } else {
-#pragma unroll
-              for (int u = 8; u < 16; ++u) a[u] = b[u] = 0.f;
-            }
+            unpack8(ca[0], a);
+            unpack8(ca[1], a + 8);
+            unpack8(cb[0], b);
+            unpack8(cb[1], b + 8);
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
               const float sg = 1.f / (1.f + expf(-a[u]));
@@ -356,32 +425,58 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             store_bf16x16(g.out_bf16 + o2 + g.f, db, g.f - col);
           }
         }
-      } else {  // WG2 / WG13: fp32 weight gradients
-        const int m = it.mt * BM + r_local;
+      } else {  // WG2 / WG13: fp32 weight gradients, staged and written by TMA stores
+        // This warp owns output rows m0 .. m0+31 of expert e.  Each 32-column
+        // chunk goes TMEM -> registers -> a 128-B-swizzled 32x32 fp32 box in
+        // shared memory -> one bulk tensor store; two boxes per warp alternate.
+        const int m0 = it.mt * BM + q * 32;
         const int mrows = (MODE == WG2) ? g.d : 2 * g.f;
         const int ncols = (MODE == WG2) ? g.f : g.d;
-        float* dst_row = nullptr;
-        if (m < mrows) {
-          if (MODE == WG2) dst_row = g.out_f32 + ((size_t)it.e * g.d + m) * g.f;
-          else if (m < g.f) dst_row = g.out_f32 + ((size_t)it.e * g.f + m) * g.d;
-          else dst_row = g.out_f32b + ((size_t)it.e * g.f + (m - g.f)) * g.d;
+        const CUtensorMap* map = &tmC;
+        int mrow = m0;
+        if (MODE == WG13 && m0 >= g.f) {
+          map = &tmC2;
+          mrow = m0 - g.f;
         }
-        for (int c = 0; c < BN; c += 16) {
-          float v[16];
+        const uint32_t box0 = tile_base + STAGES * STAGE_BYTES + (warp - 2) * EPI_WARP_BYTES;
+        uint8_t* box0_ptr = tile_ptr + STAGES * STAGE_BYTES + (warp - 2) * EPI_WARP_BYTES;
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
           if (it.kblocks > 0) {
             tmem_ld16(t_row + c, v);
+            tmem_ld16(t_row + c + 16, v + 16);
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) v[u] = 0.f;
+            for (int u = 0; u < 32; ++u) v[u] = 0.f;
           }
           const int col = it.nt * BN + c;
-          if (dst_row && col < ncols) store_f32x16(dst_row + col, v, ncols - col);
+          if (m0 >= mrows || col >= ncols) continue;          // warp-uniform
+          if (lane == 0) bulk_wait_read_1();                  // this box's last store has read it
+          __syncwarp();
+          uint8_t* bp = box0_ptr + epi_buf * (EPI_WARP_BYTES / 2);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const int phys = lane * 128 + ((ch ^ (lane & 7)) * 16);
+            *reinterpret_cast<float4*>(bp + phys) =
+                make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(map, box0 + epi_buf * (EPI_WARP_BYTES / 2), col, mrow, it.e);
+            bulk_commit();
+          }
+          epi_buf ^= 1;
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+    }
+    if (Tr::wgrad) {
+      if (lane == 0) bulk_wait_all();   // stores done before the CTA's shared memory goes away
+      __syncwarp();
     }
   }
 
@@ -463,6 +558,20 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [E, rows, cols] (dense), box {32 cols, 32 rows, 1}, 128-B swizzle: output
+// of the weight-gradient epilogue's bulk tensor stores.
+bool make_map_f32_3d(CUtensorMap* m, void* base, long long E, long long rows, long long cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)E};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)rows * cols * 4};
+  cuuint32_t box[3] = {32u, 32u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n[64] = {0};
   int dev = 0;
@@ -474,7 +583,9 @@ int sm_count() {
 
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
-                        const GemmArgs& g, long long max_items, cudaStream_t s) {
+                        const CUtensorMap& c, const CUtensorMap& c2, const GemmArgs& g,
+                        long long max_items, cudaStream_t s) {
+  constexpr int SMEM_BYTES = Traits<MODE>::smem_bytes;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -486,11 +597,35 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   }
   if (max_items <= 0) return cudaSuccess;
   const int grid = (int)std::min<long long>(sm_count(), max_items);
-  grouped_gemm_kernel<MODE><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, b2, g);
+  grouped_gemm_kernel<MODE><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, b2, c, c2, g);
   count_launches(1);
   return cudaGetLastError();
 }
 }  // namespace
+
+bool gate_tc_supported(int d) { return d % 64 == 0; }
+
+size_t gate_tc_ws_bytes(int d, int E) { return align_up((size_t)E * 3 * d * 2, 256); }
+
+cudaError_t launch_gate_tc(const uint16_t* x, const float* wg, const float* bias, int T, int d,
+                           int E, float* logits, void* ws, int* err, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  uint16_t* wgs = static_cast<uint16_t*>(ws);
+  cudaError_t e = launch_wg_split(wg, d, E, wgs, s);
+  if (e != cudaSuccess) return e;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, x, T, d, BM) || !make_map(&mb, wgs, E, 3LL * d, 128))
+    return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.E = E; g.N = T; g.d = d; g.f = 0;
+  g.kblocks = 3 * d / BK;
+  g.n_tiles_m = ceil_div(T, BM);
+  g.n_tiles_n = ceil_div(E, 128);
+  g.out_f32 = logits;
+  g.bias = bias;
+  g.err = err;
+  return launch_mode<GATE>(ma, mb, mb, ma, ma, g, (long long)g.n_tiles_m * g.n_tiles_n, s);
+}
 
 size_t tiles_ws_bytes(int N, int E) {
   return align_up(sizeof(int2) * ((size_t)ceil_div(N, BM) + E) + 16, 256);
@@ -528,7 +663,7 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.kblocks = ceil_div(d, BK);
   g.n_tiles_n = ceil_div(f, 128);
   g.out_bf16 = h; g.save_a = a_save; g.save_b = b_save;
-  e = launch_mode<GATEUP>(ma, mb, mb2, g, max_m_tiles * g.n_tiles_n, s);
+  e = launch_mode<GATEUP>(ma, mb, mb2, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
   trace_end(MOE_STAGE_GATEUP, s);
   if (e != cudaSuccess) return e;
   // down: A = h, B = W2 rows (256 per tile)
@@ -538,7 +673,7 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.n_tiles_n = ceil_div(d, BN);
   g.out_bf16 = out; g.save_a = g.save_b = nullptr;
   trace_begin(MOE_STAGE_DOWN, s);
-  e = launch_mode<DOWN>(ma, mb, mb, g, max_m_tiles * g.n_tiles_n, s);
+  e = launch_mode<DOWN>(ma, mb, mb, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
   trace_end(MOE_STAGE_DOWN, s);
   return e;
 }
@@ -568,7 +703,7 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
     g.kblocks = d / BK;
     g.n_tiles_n = ceil_div(f, BN);
     g.out_bf16 = dab; g.in_a = a_s; g.in_b = b_s;
-    e = launch_mode<DH>(ma, mb, mb, g, max_m_tiles * g.n_tiles_n, s);
+    e = launch_mode<DH>(ma, mb, mb, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
     trace_end(MOE_STAGE_BWD_DH, s);
     if (e != cudaSuccess) return e;
     // dx_perm = [da | db] [W1[e]; W3[e]] (B MN-major: W1, W3 viewed [E*f, d])
@@ -579,7 +714,7 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
     g.n_tiles_n = ceil_div(d, BN);
     g.out_bf16 = dx_perm;
     trace_begin(MOE_STAGE_BWD_DX, s);
-    e = launch_mode<DX>(ma, mb, mb2, g, max_m_tiles * g.n_tiles_n, s);
+    e = launch_mode<DX>(ma, mb, mb2, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
     trace_end(MOE_STAGE_BWD_DX, s);
     if (e != cudaSuccess) return e;
   }
@@ -589,8 +724,10 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.n_tiles_m = ceil_div(d, BM);
   g.n_tiles_n = ceil_div(f, BN);
   g.out_f32 = dW2;
+  CUtensorMap mc, mc2;
+  if (!make_map_f32_3d(&mc, dW2, E, d, f)) return cudaErrorInvalidValue;
   trace_begin(MOE_STAGE_BWD_WG2, s);
-  e = launch_mode<WG2>(ma, mb, mb, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
+  e = launch_mode<WG2>(ma, mb, mb, mc, mc, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
   trace_end(MOE_STAGE_BWD_WG2, s);
   if (e != cudaSuccess) return e;
   // [dW1[e]; dW3[e]] = [da | db]^T x_perm: A = dab [N, 2f], B = x_perm [N, d]
@@ -599,8 +736,10 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.n_tiles_m = ceil_div(2 * f, BM);
   g.n_tiles_n = ceil_div(d, BN);
   g.out_f32 = dW1; g.out_f32b = dW3;
+  if (!make_map_f32_3d(&mc, dW1, E, f, d) || !make_map_f32_3d(&mc2, dW3, E, f, d))
+    return cudaErrorInvalidValue;
   trace_begin(MOE_STAGE_BWD_WG13, s);
-  e = launch_mode<WG13>(ma, mb, mb, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
+  e = launch_mode<WG13>(ma, mb, mb, mc, mc2, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
   trace_end(MOE_STAGE_BWD_WG13, s);
   return e;
 }

@@ -29,11 +29,21 @@ struct GemmArgs {
   const uint16_t* in_b;
   float* out_f32;
   float* out_f32b;
+  const float* bias;
   int* err;
 };
 
 cudaError_t launch_gate_logits(const uint16_t* x, const float* wg, const float* bias, int T, int d,
                                int E, float* logits, cudaStream_t s);
+cudaError_t launch_wg_split(const float* wg, int d, int E, uint16_t* wgs, cudaStream_t s);
+// Gate projection on the tensor cores (needs d % 64 == 0): logits = x W_g + bias
+// through the 3-term bf16 split of W_g; ws holds the split weights.
+bool gate_tc_supported(int d);
+size_t gate_tc_ws_bytes(int d, int E);
+cudaError_t launch_gate_tc(const uint16_t* x, const float* wg, const float* bias, int T, int d,
+                           int E, float* logits, void* ws, int* err, cudaStream_t s);
+// One block waits (bounded) on an mbarrier that nothing arrives on.
+cudaError_t launch_selftest_wait(unsigned limit_us, int* err, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int T, int E, int R, int32_t* idx, float* w,
                         cudaStream_t s);
 

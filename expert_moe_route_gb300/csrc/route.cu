@@ -137,7 +137,43 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     }
   }
 }
+// W_g [d, E] fp32 -> W_gs [E, 3d] bf16 with W_gs[e, k] = hi, [e, d+k] = mid,
+// [e, 2d+k] = lo: hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid).
+// Both differences are exact in fp32 (Sterbenz), so hi + mid + lo carries
+// w's 24-bit significand to within 2^-24 |w|, and x (bf16) times each term is
+// exact in fp32: logits = x hi + x mid + x lo is a bf16 GEMM with K = 3d.
+__global__ void wg_split_kernel(const float* __restrict__ wg, int d, int E,
+                                uint16_t* __restrict__ wgs) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int k = k0 + i, e = e0 + threadIdx.x;
+    tile[i][threadIdx.x] = (k < d && e < E) ? wg[(size_t)k * E + e] : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int e = e0 + i, k = k0 + threadIdx.x;
+    if (k >= d || e >= E) continue;
+    const float w = tile[threadIdx.x][i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    uint16_t* row = wgs + (size_t)e * 3 * d;
+    row[k] = *reinterpret_cast<const uint16_t*>(&hi);
+    row[d + k] = *reinterpret_cast<const uint16_t*>(&mid);
+    row[2 * d + k] = *reinterpret_cast<const uint16_t*>(&lo);
+  }
+}
 }  // namespace
+
+cudaError_t launch_wg_split(const float* wg, int d, int E, uint16_t* wgs, cudaStream_t s) {
+  dim3 grid(ceil_div(d, 32), ceil_div(E, 32));
+  wg_split_kernel<<<grid, dim3(32, 8), 0, s>>>(wg, d, E, wgs);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gate_logits(const uint16_t* x, const float* wg, const float* bias, int T, int d,
                                int E, float* logits, cudaStream_t s) {

@@ -96,6 +96,18 @@ moe_status_t moe_trace_events(void* const* events);
 /* Number of CUDA kernels this library has launched in this process (utility). */
 unsigned long long moe_kernel_launches(void);
 
+/*
+ * moe_selftest_wait_timeout -- failure-detection self-test (utility; the page
+ * has no counterpart).  Launches one small block whose pipeline wait is on an
+ * mbarrier that nothing ever arrives on, through the same bounded-wait routine
+ * the GEMM pipelines use, with a limit of limit_us microseconds (1..10^6).  The
+ * wait gives up, the kernel records the timeout in ws (at least 256 bytes,
+ * 256-byte aligned, device memory) and returns; the call waits for it and
+ * returns MOE_ERR_TIMEOUT when the timeout was detected and reported, MOE_OK if
+ * the wait was (wrongly) satisfied.  The GPU context stays usable.
+ */
+moe_status_t moe_selftest_wait_timeout(unsigned limit_us, void* ws, moe_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(moe_status_t status);
 
@@ -113,11 +125,17 @@ int moe_version(void);
  * x: bf16 [T,d]; w_gate: fp32 [d,E]; bias: fp32 [E] or NULL.
  * logits: fp32 [T,E], written (or read, with MOE_LOGITS_IN: then x, w_gate
  * and bias are ignored and may be NULL).  topk_idx: int32 [T,R]; topk_w: fp32
- * [T,R].  Logits must be finite.  No workspace.
+ * [T,R].  Logits must be finite.
+ * Workspace (two-call convention; ignored with MOE_LOGITS_IN): when d is a
+ * multiple of 64 the projection runs on the tensor cores with W_g split into
+ * three bf16 terms (hi + mid + lo carry its fp32 significand; products with
+ * the bf16 x are exact), which needs 6*E*d bytes of workspace; otherwise an
+ * fp32 FMA kernel runs and the workspace holds only the error word.
  */
 moe_status_t moe_route(const uint16_t* x, const float* w_gate, const float* bias,
                        int T, int d, int E, int R, float* logits,
-                       int32_t* topk_idx, float* topk_w, unsigned flags, moe_stream_t stream);
+                       int32_t* topk_idx, float* topk_w, void* ws, size_t* ws_bytes,
+                       unsigned flags, moe_stream_t stream);
 
 /*
  * moe_dispatch -- group the routed tokens by expert (section "Dispatch and

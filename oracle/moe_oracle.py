@@ -242,6 +242,30 @@ def layer_fwd(x, w_gate, bias, W1, W3, W2, R, rounding=True,
                 row_slot=row_slot, slot_row=slot_row, x_perm=x_perm, a=a, b=b, h=h, o=o, y=y)
 
 
+def expert_bwd(x_rows, a, b, h, do, W1e, W3e, W2e, rounding=True):
+    """Backward of one expert's SwiGLU FFN over its rows (float64).
+
+    a, b: the forward pre-activations (kept as bf16 for the backward); h: the
+    forward hidden rows; do: the rows' output gradients (bf16 values).
+        dh      = do W2e
+        da      = bf16(dh * b_s * silu'(a_s)),  db = bf16(dh * silu(a_s)),
+                  a_s = bf16(a), b_s = bf16(b), silu'(a) = s(a)(1 + a(1 - s(a)))
+        dx_perm = bf16(da W1e + db W3e)
+        dW2e = do^T h,  dW1e = da^T x,  dW3e = db^T x
+    """
+    x_rows = values(x_rows)
+    w1, w3, w2 = values(W1e), values(W3e), values(W2e)
+    a_s = bf16_round(a, rounding)
+    b_s = bf16_round(b, rounding)
+    dh = do @ w2
+    sg = 1.0 / (1.0 + np.exp(-a_s))
+    dsilu = sg * (1.0 + a_s * (1.0 - sg))
+    da = bf16_round(dh * b_s * dsilu, rounding)
+    db = bf16_round(dh * a_s * sg, rounding)
+    return dict(da=da, db=db, dx_perm=bf16_round(da @ w1 + db @ w3, rounding),
+                dW2=do.T @ h, dW1=da.T @ x_rows, dW3=db.T @ x_rows)
+
+
 def layer_bwd(fwd, x, w_gate, W1, W3, W2, dy, R, rounding=True):
     """Backward pass for L = sum(y * g) with dy = g (bf16 bits or float64 values).
 
@@ -279,9 +303,6 @@ def layer_bwd(fwd, x, w_gate, W1, W3, W2, dy, R, rounding=True):
         dw[:, r] = np.sum(dy * o[rows], axis=1)
         do[rows] = bf16_round(w[:, r:r + 1] * dy, rounding)
 
-    a_s = bf16_round(fwd["a"], rounding)
-    b_s = bf16_round(fwd["b"], rounding)
-    h = fwd["h"]
     x_perm = values(fwd["x_perm"])
     dx_perm = np.zeros((N, d))
     da = np.zeros((N, f))
@@ -293,19 +314,10 @@ def layer_bwd(fwd, x, w_gate, W1, W3, W2, dy, R, rounding=True):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r0 == r1:
             continue
-        w1 = values(W1[e])
-        w3 = values(W3[e])
-        w2 = values(W2[e])
-        dh = do[r0:r1] @ w2
-        sg = 1.0 / (1.0 + np.exp(-a_s[r0:r1]))
-        dsilu = sg * (1.0 + a_s[r0:r1] * (1.0 - sg))
-        da_e = bf16_round(dh * b_s[r0:r1] * dsilu, rounding)
-        db_e = bf16_round(dh * a_s[r0:r1] * sg, rounding)
-        dx_perm[r0:r1] = bf16_round(da_e @ w1 + db_e @ w3, rounding)
-        dW2[e] = do[r0:r1].T @ h[r0:r1]
-        dW1[e] = da_e.T @ x_perm[r0:r1]
-        dW3[e] = db_e.T @ x_perm[r0:r1]
-        da[r0:r1], db[r0:r1] = da_e, db_e
+        eb = expert_bwd(x_perm[r0:r1], fwd["a"][r0:r1], fwd["b"][r0:r1], fwd["h"][r0:r1],
+                        do[r0:r1], W1[e], W3[e], W2[e], rounding)
+        dx_perm[r0:r1], da[r0:r1], db[r0:r1] = eb["dx_perm"], eb["da"], eb["db"]
+        dW1[e], dW3[e], dW2[e] = eb["dW1"], eb["dW3"], eb["dW2"]
 
     wdw = np.sum(w * dw, axis=1, keepdims=True)
     dsel = w * (dw - wdw)

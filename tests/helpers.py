@@ -55,3 +55,13 @@ def random_routing(T, E, R, seed, skew=0.0):
     u = g.random((T, R)) + 0.5
     w = (u / u.sum(1, keepdims=True)).astype(np.float32)
     return idx, w
+
+
+class LazyExperts:
+    """[E, ...] device weight tensor read one expert at a time as bf16 bits."""
+
+    def __init__(self, t):
+        self.t, self.shape = t, tuple(t.shape)
+
+    def __getitem__(self, e):
+        return bits(self.t[e])

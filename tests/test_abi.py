@@ -66,8 +66,15 @@ def test_host_argument_checks():
     assert lib.moe_dispatch(None, None, 100, 64, 8, 2, None, None, None, None, None,
                             ctypes.c_void_p(4096 + 16), ctypes.byref(big), 0, None) == 3
     # route: R > 32 unsupported, R > E invalid
-    assert lib.moe_route(None, None, None, 4, 64, 64, 33, None, None, None, 0, None) == 2
-    assert lib.moe_route(None, None, None, 4, 64, 4, 5, None, None, None, 0, None) == 1
+    assert lib.moe_route(None, None, None, 4, 64, 64, 33, None, None, None, None,
+                         ctypes.byref(n), 0, None) == 2
+    assert lib.moe_route(None, None, None, 4, 64, 4, 5, None, None, None, None,
+                         ctypes.byref(n), 0, None) == 1
+    # route workspace: split gate weights when d % 64 == 0, error word only otherwise
+    assert lib.moe_route(None, None, None, 4, 128, 8, 2, None, None, None, None,
+                         ctypes.byref(n), 0, None) == 0 and n.value >= 6 * 8 * 128
+    assert lib.moe_route(None, None, None, 4, 72, 8, 2, None, None, None, None,
+                         ctypes.byref(n), 0, None) == 0 and n.value == 256
     # combine: misaligned output
     assert lib.moe_combine(ctypes.c_void_p(4096), ctypes.c_void_p(8192), None, 4, 64, 2,
                            ctypes.c_void_p(4098), None) == 2
@@ -99,3 +106,11 @@ def test_no_cpu_fallback_without_gpu():
     st = lib.moe_combine(ctypes.c_void_p(4096), ctypes.c_void_p(8192), None, 4, 64, 2,
                          ctypes.c_void_p(1 << 20), None)
     assert st == 6
+
+
+def test_selftest_argument_checks():
+    lib = B.lib()
+    assert lib.moe_selftest_wait_timeout(0, ctypes.c_void_p(4096), None) == 1
+    assert lib.moe_selftest_wait_timeout(2000000, ctypes.c_void_p(4096), None) == 1
+    assert lib.moe_selftest_wait_timeout(100, None, None) == 1
+    assert lib.moe_selftest_wait_timeout(100, ctypes.c_void_p(4096 + 8), None) == 3

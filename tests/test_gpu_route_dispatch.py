@@ -15,7 +15,11 @@ def _route(B, x, wg, bias, T, E, R, logits_in=None):
               else torch.empty((T, E), dtype=torch.float32, device="cuda"))
     idx = torch.empty((T, R), dtype=torch.int32, device="cuda")
     w = torch.empty((T, R), dtype=torch.float32, device="cuda")
-    B.moe_route(x, wg, bias, logits, idx, w, flags=B.MOE_LOGITS_IN if logits_in is not None else 0)
+    if logits_in is not None:
+        B.moe_route(None, None, None, logits, idx, w, flags=B.MOE_LOGITS_IN)
+    else:
+        ws = B.workspace(B.route_ws_bytes(T, x.shape[1], E, R))
+        B.moe_route(x, wg, bias, logits, idx, w, ws=ws, flags=B.MOE_CHECK)
     torch.cuda.synchronize()
     return logits, idx, w
 
@@ -147,3 +151,18 @@ def test_combine_matches_oracle(lib, T, d, R, weighted):
     y2 = torch.empty_like(y)
     lib.moe_combine(o.cuda(), torch.from_numpy(slot_row).cuda(), wt, y2, R)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))     # bitwise reproducible
+
+
+@pytest.mark.parametrize("T,d,E,R", [(500, 200, 64, 6), (129, 8, 3, 2), (300, 1024, 1000, 8)])
+def test_route_gate_paths(lib, T, d, E, R):
+    # d % 64 != 0 runs the fp32 FMA projection; d % 64 == 0 the split-bf16 tensor-core one
+    g = torch.Generator().manual_seed(T + d)
+    x = torch.randn((T, d), generator=g).to(torch.bfloat16)
+    wg = torch.randn((d, E), generator=g) * 0.05
+    bias = torch.randn((E,), generator=g)
+    ref_l = O.gate_logits(bits(x), wg.numpy(), bias.numpy())
+    logits, idx, w = _route(lib, x.cuda(), wg.cuda(), bias.cuda(), T, E, R)
+    assert_close(f64(logits), ref_l, "logits", max_rel=3e-5, mean_rel=1e-5)
+    ridx, _ = O.route_topk(ref_l, R)
+    same = (idx.cpu().numpy() == ridx).all(axis=1)
+    assert (same | near_tie_tokens(ref_l, R)).all()
