@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--experts", type=int, default=None, help="override E (smaller profiling cases)")
     p.add_argument("--cpu-tokens", type=int, default=None,
                    help="tokens in the CPU oracle sample (default per workload)")
+    p.add_argument("--fp8", action="store_true",
+                   help="dispatch workloads: block-scaled fp8 dispatch (E4M3 + per-128 scales), "
+                        "dequantising identity experts, bf16 combine")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -119,7 +122,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- work model
-def stage_work(wl):
+def stage_work(wl, fp8=False):
     """Algorithmic work of one launch of each traced stage: (kind, amount).
 
     kind "tflop": FLOPs of real rows only (no padding); "gb": bytes that must
@@ -130,7 +133,8 @@ def stage_work(wl):
     w = {
         "gate": ("alu", 2.0 * T * d * E),
         "topk": ("gb", 4.0 * T * E + 8.0 * N),
-        "dispatch": ("gb", 2.0 * T * d + 2.0 * N * d + 4.0 * N * 3),
+        "dispatch": ("gb", 2.0 * T * d + (N * d + 4.0 * N * d / 128 if fp8 else 2.0 * N * d)
+                     + 4.0 * N * 3),
         "combine": ("gb", 2.0 * N * d + 8.0 * N + 2.0 * T * d),
     }
     if f:
@@ -202,10 +206,18 @@ def run_ours(args, rank, world, device):
         x_perm = torch.empty((N, wl.d), dtype=torch.bfloat16, device=device)
         y = torch.empty_like(x)
         ws = B.workspace(B.dispatch_ws_bytes(wl.T, wl.d, wl.E, wl.R), device)
+        if args.fp8:
+            xq = torch.empty((N, wl.d), dtype=torch.uint8, device=device)
+            xs = torch.empty((N, wl.d // 128), dtype=torch.float32, device=device)
 
         def step(xin=None, yout=None):
-            B.moe_dispatch(x if xin is None else xin, idx, wl.E, counts, offsets, row_slot,
-                           slot_row, x_perm, ws)
+            if args.fp8:   # fp8 dispatch, identity experts dequantise to bf16, bf16 combine
+                B.moe_dispatch_fp8(x if xin is None else xin, idx, wl.E, counts, offsets,
+                                   row_slot, slot_row, xq, xs, ws)
+                B.moe_dequant_fp8(xq, xs, x_perm)
+            else:
+                B.moe_dispatch(x if xin is None else xin, idx, wl.E, counts, offsets, row_slot,
+                               slot_row, x_perm, ws)
             B.moe_combine(x_perm, slot_row, w, y if yout is None else yout, wl.R)
         train = False
         host_in = [("x", x)]
@@ -281,7 +293,7 @@ def run_ours(args, rank, world, device):
         for name, ms in tr.elapsed_ms().items():
             stage_ms[name] = stage_ms.get(name, 0.0) + ms / args.steps
     pk, pk_src = load_peaks()
-    work = stage_work(wl)
+    work = stage_work(wl, fp8=args.fp8)
     if identity:
         ran = ("dispatch", "combine")
     elif train:
@@ -386,7 +398,8 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": "bf16 (fp32 accumulation)",
         "data": "synthetic (seeded, shapes and distributions of the workload)",
-        "config": {"workload": synth.describe(wl) + (" fwd+bwd" if train else " fwd"),
+        "config": {"workload": synth.describe(wl) + (" fwd+bwd" if train else " fwd")
+                   + (" fp8-dispatch" if args.fp8 else ""),
                    "parallelism": f"replicas x{world} (no cross-GPU exchange)",
                    "global_batch_tokens": wl.T * world,
                    "l2": "inputs larger than L2 every step (no flush)"},

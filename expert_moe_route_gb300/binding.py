@@ -23,7 +23,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 # the C ABI's exported symbols (checked against include/moe.h by the tests)
 SYMBOLS = ("moe_status_string", "moe_version", "moe_trace_events", "moe_kernel_launches",
            "moe_selftest_wait_timeout",
-           "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_grouped_ffn",
+           "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_dispatch_fp8",
+           "moe_dequant_fp8", "moe_grouped_ffn",
            "moe_combine", "moe_layer_fwd", "moe_layer_bwd")
 
 # moe_stage_t
@@ -72,6 +73,11 @@ def _declare(lib):
     lib.moe_dispatch_noalloc.restype = _i
     lib.moe_dispatch_noalloc.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _u,
                                          _vp]
+    lib.moe_dispatch_fp8.restype = _i
+    lib.moe_dispatch_fp8.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     _szp, _u, _vp]
+    lib.moe_dequant_fp8.restype = _i
+    lib.moe_dequant_fp8.argtypes = [_vp, _vp, _i, _i, _vp, _vp]
     lib.moe_grouped_ffn.restype = _i
     lib.moe_grouped_ffn.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _vp, _szp, _u, _vp]
@@ -186,6 +192,30 @@ def moe_dispatch_noalloc(x, topk_idx, E, counts, offsets, row_slot, slot_row, x_
                                     _p(row_slot), _p(slot_row), _p(x_perm), flags,
                                     _stream(stream))
     _check(st, "moe_dispatch_noalloc")
+
+
+def moe_dispatch_fp8(x, topk_idx, E, counts, offsets, row_slot, slot_row, xq_perm, xscale_perm,
+                     ws, flags=0, stream=None):
+    """Block-scaled fp8 dispatch: E4M3 codes (uint8 [N,d]) and fp32 scales [N, d/128]."""
+    T, R = topk_idx.shape
+    d = x.shape[1]
+    _dt(x, torch.bfloat16, "x"); _dt(xq_perm, torch.uint8, "xq_perm")
+    _dt(xscale_perm, torch.float32, "xscale_perm")
+    for name, t in (("topk_idx", topk_idx), ("counts", counts), ("offsets", offsets),
+                    ("row_slot", row_slot), ("slot_row", slot_row)):
+        _dt(t, torch.int32, name)
+    n = ctypes.c_size_t(ws.numel())
+    st = lib().moe_dispatch_fp8(_p(x), _p(topk_idx), T, d, E, R, _p(counts), _p(offsets),
+                                _p(row_slot), _p(slot_row), _p(xq_perm), _p(xscale_perm), _p(ws),
+                                ctypes.byref(n), flags, _stream(stream))
+    _check(st, "moe_dispatch_fp8")
+
+
+def moe_dequant_fp8(xq, xscale, out, stream=None):
+    N, d = xq.shape
+    _dt(xq, torch.uint8, "xq"); _dt(xscale, torch.float32, "xscale"); _dt(out, torch.bfloat16, "out")
+    _check(lib().moe_dequant_fp8(_p(xq), _p(xscale), N, d, _p(out), _stream(stream)),
+           "moe_dequant_fp8")
 
 
 def grouped_ffn_ws_bytes(N, d, f, E) -> int:

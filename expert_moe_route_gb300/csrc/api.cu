@@ -210,6 +210,49 @@ moe_status_t moe_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int
   return finish(e, err, flags, s);
 }
 
+moe_status_t moe_dispatch_fp8(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E,
+                              int R, int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                              int32_t* slot_row, uint8_t* xq_perm, float* xscale_perm, void* ws,
+                              size_t* ws_bytes, unsigned flags, moe_stream_t stream) {
+  moe_status_t st = shape_check(T, d, E, R);
+  if (st != MOE_OK) return st;
+  if (d % 128) return MOE_ERR_UNSUPPORTED;
+  if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t need = kErrBytes + dispatch_ws_bytes(T, E);
+  if (!ws) {
+    *ws_bytes = need;
+    return MOE_OK;
+  }
+  if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
+  if (!counts || !offsets || (T > 0 && (!x || !topk_idx || !row_slot || !slot_row || !xq_perm ||
+                                        !xscale_perm)))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!al16(x) || ((uintptr_t)xq_perm & 7) || ((uintptr_t)xscale_perm & 3)))
+    return MOE_ERR_UNSUPPORTED;
+  if (!init_once()) return MOE_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  int* err = static_cast<int*>(ws);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  cudaError_t e;
+  {
+    Stage st_(s, MOE_STAGE_DISPATCH);
+    e = launch_dispatch_fp8(x, topk_idx, T, d, E, R, counts, offsets, row_slot, slot_row, xq_perm,
+                            xscale_perm, static_cast<uint8_t*>(ws) + kErrBytes, err, s);
+  }
+  return finish(e, err, flags, s);
+}
+
+moe_status_t moe_dequant_fp8(const uint8_t* xq, const float* xscale, int N, int d, uint16_t* out,
+                             moe_stream_t stream) {
+  if (N < 0 || d <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 128) return MOE_ERR_UNSUPPORTED;
+  if (N == 0) return MOE_OK;
+  if (!xq || !xscale || !out) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)xq & 7) || ((uintptr_t)xscale & 3) || !al16(out)) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = S(stream);
+  return finish(launch_dequant_fp8(xq, xscale, N, d, out, s), nullptr, 0, s);
+}
+
 moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
                              int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                              uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
@@ -335,6 +378,7 @@ static size_t layer_bwd_ws(const moe_layer_t* L) {
   n += align_up(N * 4, 256);            // dlogits per slot (token order)
   n += align_up(N * 4, 256);            // dlogits per row
   n += align_up(E * d * 4, 256);        // W_g^T
+  n += dwg_ws_bytes((int)d, (int)E);    // router weight-gradient partials
   return n;
 }
 
@@ -371,6 +415,7 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
   float* dsel_tok = static_cast<float*>(c.take((size_t)N * 4));
   float* dsel_row = static_cast<float*>(c.take((size_t)N * 4));
   float* wgT = static_cast<float*>(c.take((size_t)E * d * 4));
+  void* dwg_ws = c.take(dwg_ws_bytes(d, E));
   MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
   if (N == 0) {
     MOE_TRY(cudaMemsetAsync(dW_gate, 0, sizeof(float) * d * E, s));
@@ -387,7 +432,7 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
                          sv->h, dO, dab, dxp, dW1, dW3, dW2, tws, err, s));
   {
     Stage st_(s, MOE_STAGE_BWD_DWG);
-    MOE_TRY(launch_dwg(sv->x_perm, sv->offsets, dsel_row, d, E, dW_gate, s));
+    MOE_TRY(launch_dwg(sv->x_perm, sv->offsets, dsel_row, d, E, dW_gate, dwg_ws, s));
   }
   cudaError_t e;
   {

@@ -38,21 +38,32 @@ __global__ void __launch_bounds__(BW * 32) bwd_route_kernel(
       float g[8];
       unpack8(ldg_nc_v4(dy + (size_t)t * d + (size_t)v * 8), g);
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        if (r >= R) break;
-        const int row = rows_s[wid][r];
-        if (row < 0) continue;
-        float ov[8], dv[8];
-        unpack8(ldg_nc_v4(o + (size_t)row * d + (size_t)v * 8), ov);
-        const float wr = w_s[wid][r];
-        float s = 0.f;
+      for (int r0 = 0; r0 < 32; r0 += 4) {
+        if (r0 >= R) break;
+        uint4 q[4];   // four rows' loads in flight before any is used
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          s = fmaf(g[j], ov[j], s);
-          dv[j] = wr * g[j];
+        for (int u = 0; u < 4; ++u) {
+          const int row = (r0 + u < R) ? rows_s[wid][r0 + u] : -1;
+          q[u] = row >= 0 ? ldg_nc_v4(o + (size_t)row * d + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
         }
-        acc[r] += s;
-        reinterpret_cast<uint4*>(dO + (size_t)row * d)[v] = pack8(dv);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = r0 + u;
+          if (r >= R) break;
+          const int row = rows_s[wid][r];
+          if (row < 0) continue;
+          float ov[8], dv[8];
+          unpack8(q[u], ov);
+          const float wr = w_s[wid][r];
+          float s = 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            s = fmaf(g[j], ov[j], s);
+            dv[j] = wr * g[j];
+          }
+          acc[r] += s;
+          reinterpret_cast<uint4*>(dO + (size_t)row * d)[v] = pack8(dv);
+        }
       }
     }
 #pragma unroll
@@ -98,22 +109,66 @@ __global__ void wg_transpose_kernel(const float* __restrict__ wg, int d, int E,
 }
 
 // dW_g[k, e] = sum over expert e's rows (ascending) of dsel_row[row] * x_perm[row, k].
-// Block = (expert, 256-column chunk); thread = one column k.
-__global__ void __launch_bounds__(256) dwg_kernel(const uint16_t* __restrict__ x_perm,
-                                                  const int32_t* __restrict__ offsets,
-                                                  const float* __restrict__ dsel_row, int d, int E,
-                                                  float* __restrict__ dW_gate) {
-  const int e = blockIdx.y;
-  const int k = blockIdx.x * 256 + threadIdx.x;
-  const int r0 = offsets[e], r1 = offsets[e + 1];
-  float acc = 0.f;
-  if (k < d) {
-    const unsigned short* xp = reinterpret_cast<const unsigned short*>(x_perm);
-    for (int row = r0; row < r1; ++row) {
-      const float xv = __uint_as_float((uint32_t)xp[(size_t)row * d + k] << 16);
-      acc = fmaf(dsel_row[row], xv, acc);
+// Pass 1: block = (1024-column chunk, expert, row chunk s of DWG_SPLIT); thread =
+// 8 consecutive columns (16-byte loads), four rows' loads in flight per step,
+// fp32 accumulation in row order -> part[s][e][k].  Pass 2 adds the DWG_SPLIT
+// partials in s order and writes dW_g transposed through shared memory.
+constexpr int DWG_THREADS = 128;
+constexpr int DWG_SPLIT = 4;
+__global__ void __launch_bounds__(DWG_THREADS) dwg_partial_kernel(
+    const uint16_t* __restrict__ x_perm, const int32_t* __restrict__ offsets,
+    const float* __restrict__ dsel_row, int d, int E, float* __restrict__ part) {
+  const int e = blockIdx.y, sp = blockIdx.z;
+  const int k0 = (blockIdx.x * DWG_THREADS + threadIdx.x) * 8;
+  if (k0 >= d) return;
+  const int e0 = offsets[e], n = offsets[e + 1] - e0;
+  const int r0 = e0 + (int)((long long)n * sp / DWG_SPLIT);
+  const int r1 = e0 + (int)((long long)n * (sp + 1) / DWG_SPLIT);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int row = r0;
+  for (; row + 4 <= r1; row += 4) {
+    uint4 q[4];
+    float s[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      q[u] = ldg_nc_v4(x_perm + (size_t)(row + u) * d + k0);
+      s[u] = dsel_row[row + u];
     }
-    dW_gate[(size_t)k * E + e] = acc;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float xv[8];
+      unpack8(q[u], xv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(s[u], xv[j], acc[j]);
+    }
+  }
+  for (; row < r1; ++row) {
+    float xv[8];
+    unpack8(ldg_nc_v4(x_perm + (size_t)row * d + k0), xv);
+    const float s = dsel_row[row];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = fmaf(s, xv[j], acc[j]);
+  }
+  float4* dst = reinterpret_cast<float4*>(part + ((size_t)sp * E + e) * d + k0);
+  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+__global__ void dwg_reduce_kernel(const float* __restrict__ part, int d, int E,
+                                  float* __restrict__ dW_gate) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {      // i: expert in tile, x: column
+    const int e = e0 + i, k = k0 + threadIdx.x;
+    float v = 0.f;
+    if (e < E && k < d)
+      for (int sp = 0; sp < DWG_SPLIT; ++sp) v += part[((size_t)sp * E + e) * d + k];
+    tile[i][threadIdx.x] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {      // i: column in tile, x: expert
+    const int k = k0 + i, e = e0 + threadIdx.x;
+    if (k < d && e < E) dW_gate[(size_t)k * E + e] = tile[threadIdx.x][i];
   }
 }
 
@@ -138,24 +193,47 @@ __global__ void __launch_bounds__(BW * 32) dx_combine_kernel(
     __syncwarp();
     for (int v = lane; v < nv; v += 32) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int r = 0; r < R; ++r) {
-        const int row = rows_s[wid][r];
-        if (row < 0) continue;
-        float f[8];
-        unpack8(ldg_nc_v4(dx_perm + (size_t)row * d + (size_t)v * 8), f);
+      for (int r0 = 0; r0 < R; r0 += 4) {       // sum of the token's dx_perm rows, r order
+        uint4 q[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] += f[j];
+        for (int u = 0; u < 4; ++u) {
+          const int row = (r0 + u < R) ? rows_s[wid][r0 + u] : -1;
+          q[u] = row >= 0 ? ldg_nc_v4(dx_perm + (size_t)row * d + (size_t)v * 8)
+                          : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (r0 + u >= R) break;
+          if (rows_s[wid][r0 + u] < 0) continue;
+          float f[8];
+          unpack8(q[u], f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] += f[j];
+        }
       }
-      for (int r = 0; r < R; ++r) {
-        const int e = exp_s[wid][r];
-        if (e < 0) continue;
-        const float ds = ds_s[wid][r];
-        const float4* p = reinterpret_cast<const float4*>(wgT + (size_t)e * d + (size_t)v * 8);
-        const float4 a = p[0], b = p[1];
-        acc[0] = fmaf(ds, a.x, acc[0]); acc[1] = fmaf(ds, a.y, acc[1]);
-        acc[2] = fmaf(ds, a.z, acc[2]); acc[3] = fmaf(ds, a.w, acc[3]);
-        acc[4] = fmaf(ds, b.x, acc[4]); acc[5] = fmaf(ds, b.y, acc[5]);
-        acc[6] = fmaf(ds, b.z, acc[6]); acc[7] = fmaf(ds, b.w, acc[7]);
+      for (int r0 = 0; r0 < R; r0 += 4) {       // + dlogits_t W_g^T, r order
+        float4 a[4], b[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = (r0 + u < R) ? exp_s[wid][r0 + u] : -1;
+          if (e >= 0) {
+            const float4* p = reinterpret_cast<const float4*>(wgT + (size_t)e * d + (size_t)v * 8);
+            a[u] = p[0];
+            b[u] = p[1];
+          } else {
+            a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (r0 + u >= R) break;
+          if (exp_s[wid][r0 + u] < 0) continue;
+          const float ds = ds_s[wid][r0 + u];
+          acc[0] = fmaf(ds, a[u].x, acc[0]); acc[1] = fmaf(ds, a[u].y, acc[1]);
+          acc[2] = fmaf(ds, a[u].z, acc[2]); acc[3] = fmaf(ds, a[u].w, acc[3]);
+          acc[4] = fmaf(ds, b[u].x, acc[4]); acc[5] = fmaf(ds, b[u].y, acc[5]);
+          acc[6] = fmaf(ds, b[u].z, acc[6]); acc[7] = fmaf(ds, b[u].w, acc[7]);
+        }
       }
       reinterpret_cast<uint4*>(dx + (size_t)t * d)[v] = pack8(acc);
     }
@@ -186,11 +264,16 @@ cudaError_t launch_wg_transpose(const float* wg, int d, int E, float* wgT, cudaS
   return cudaGetLastError();
 }
 
+size_t dwg_ws_bytes(int d, int E) { return align_up((size_t)DWG_SPLIT * E * d * 4, 256); }
+
 cudaError_t launch_dwg(const uint16_t* x_perm, const int32_t* offsets, const float* dsel_row,
-                       int d, int E, float* dW_gate, cudaStream_t s) {
-  dim3 grid(ceil_div(d, 256), E);
-  dwg_kernel<<<grid, 256, 0, s>>>(x_perm, offsets, dsel_row, d, E, dW_gate);
-  count_launches(1);
+                       int d, int E, float* dW_gate, void* ws, cudaStream_t s) {
+  float* part = static_cast<float*>(ws);
+  dim3 grid(ceil_div(d, DWG_THREADS * 8), E, DWG_SPLIT);
+  dwg_partial_kernel<<<grid, DWG_THREADS, 0, s>>>(x_perm, offsets, dsel_row, d, E, part);
+  dwg_reduce_kernel<<<dim3(ceil_div(d, 32), ceil_div(E, 32)), dim3(32, 8), 0, s>>>(part, d, E,
+                                                                                  dW_gate);
+  count_launches(2);
   return cudaGetLastError();
 }
 

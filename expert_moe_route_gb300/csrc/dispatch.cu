@@ -15,6 +15,8 @@
 //      row = blk_base + earlier warps + earlier groups + rank (stable order).
 //   4. permute_rows: one warp per token reads x[t] once (16-byte vectors) and
 //      writes it to its R rows of x_perm.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -202,6 +204,79 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __res
     }
   }
 }
+// Block-scaled fp8 variant of permute_rows: one warp per token quantises each
+// 128-channel block once (16 lanes x 8 channels: amax by half-warp shuffles,
+// scale = amax / 448, codes = E4M3(x / scale) rounded to nearest even with
+// saturation) and writes the 8-byte code groups and the block scales to the
+// token's R rows.  An all-zero block gets scale 0 and zero codes.
+__global__ void __launch_bounds__(256) permute_rows_fp8_kernel(
+    const uint16_t* __restrict__ x, int T, int d, int R, int N,
+    const int32_t* __restrict__ slot_row, uint8_t* __restrict__ xq, float* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x / 32;
+  const int nb = d / 128;
+  for (int t = blockIdx.x * warps + threadIdx.x / 32; t < T; t += gridDim.x * warps) {
+    int my_row = lane < R ? slot_row[(size_t)t * R + lane] : -1;
+    if ((unsigned)my_row >= (unsigned)N) my_row = -1;
+    for (int base = 0; base < d; base += 256) {       // two blocks per pass, warp-uniform
+      const int c = base + lane * 8;
+      const bool valid = c < d;
+      float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (valid) unpack8(ldg_nc_v4(x + (size_t)t * d + c), v);
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+      const float scale = amax / 448.f;
+      uint32_t lo = 0, hi = 0;
+      if (scale > 0.f) {
+        __nv_fp8x2_storage_t p0 = __nv_cvt_float2_to_fp8x2(make_float2(v[0] / scale, v[1] / scale), __NV_SATFINITE, __NV_E4M3);
+        __nv_fp8x2_storage_t p1 = __nv_cvt_float2_to_fp8x2(make_float2(v[2] / scale, v[3] / scale), __NV_SATFINITE, __NV_E4M3);
+        __nv_fp8x2_storage_t p2 = __nv_cvt_float2_to_fp8x2(make_float2(v[4] / scale, v[5] / scale), __NV_SATFINITE, __NV_E4M3);
+        __nv_fp8x2_storage_t p3 = __nv_cvt_float2_to_fp8x2(make_float2(v[6] / scale, v[7] / scale), __NV_SATFINITE, __NV_E4M3);
+        lo = (uint32_t)p0 | ((uint32_t)p1 << 16);
+        hi = (uint32_t)p2 | ((uint32_t)p3 << 16);
+      }
+      const int blk = c / 128;
+      for (int r = 0; r < R; ++r) {
+        const int row = __shfl_sync(kFull, my_row, r);
+        if (row < 0 || !valid) continue;
+        *reinterpret_cast<uint2*>(xq + (size_t)row * d + c) = make_uint2(lo, hi);
+        if ((lane & 15) == 0) xs[(size_t)row * nb + blk] = scale;
+      }
+    }
+  }
+}
+
+// Identity expert for fp8-dispatched rows: out = bf16(code * scale).
+__global__ void __launch_bounds__(256) dequant_fp8_kernel(const uint8_t* __restrict__ xq,
+                                                          const float* __restrict__ xs, long long N,
+                                                          int d, uint16_t* __restrict__ out) {
+  const int nb = d / 128;
+  const long long groups = N * (d / 8);
+  for (long long gi = blockIdx.x * (long long)blockDim.x + threadIdx.x; gi < groups;
+       gi += (long long)gridDim.x * blockDim.x) {
+    const long long row = gi / (d / 8);
+    const int c = (int)(gi % (d / 8)) * 8;
+    const float scale = xs[row * nb + c / 128];
+    const uint2 q = *reinterpret_cast<const uint2*>(xq + row * d + c);
+    float f[8];
+    const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[h] >> (16 * j)) & 0xffff);
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+        const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        f[h * 4 + j * 2] = ff.x * scale;
+        f[h * 4 + j * 2 + 1] = ff.y * scale;
+      }
+    }
+    *reinterpret_cast<uint4*>(out + row * d + c) = pack8(f);
+  }
+}
 }  // namespace
 
 size_t dispatch_ws_bytes(int T, int E) {
@@ -231,6 +306,30 @@ cudaError_t launch_dispatch(const uint16_t* x, const int32_t* idx, int T, int d,
     permute_rows_kernel<<<blocks, 256, 0, s>>>(x, T, d, R, T * R, slot_row, x_perm);
     count_launches(1);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_fp8(const uint16_t* x, const int32_t* idx, int T, int d, int E, int R,
+                                int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                                int32_t* slot_row, uint8_t* xq, float* xs, void* ws, int* err,
+                                cudaStream_t s) {
+  cudaError_t e = launch_dispatch(nullptr, idx, T, d, E, R, counts, offsets, row_slot, slot_row,
+                                  nullptr, ws, err, s);
+  if (e != cudaSuccess || T == 0) return e;
+  const int blocks = ceil_div(T, 8) < 152 * 8 ? ceil_div(T, 8) : 152 * 8;
+  permute_rows_fp8_kernel<<<blocks, 256, 0, s>>>(x, T, d, R, T * R, slot_row, xq, xs);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_fp8(const uint8_t* xq, const float* xs, long long N, int d,
+                               uint16_t* out, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  const long long groups = N * (d / 8);
+  const long long want = (groups + 255) / 256;
+  const int blocks = want < 152 * 16 ? (int)want : 152 * 16;
+  dequant_fp8_kernel<<<blocks, 256, 0, s>>>(xq, xs, N, d, out);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -11,9 +11,10 @@
 //   DX      dx_perm = bf16([da|db] [W1[e]; W3[e]])
 //   WG2     dW2[e] = do^T h                     (K = the expert's rows, ragged)
 //   WG13    [dW1[e]; dW3[e]] = [da|db]^T x_perm (K ragged)
-// Roles (192 threads): warp 0 issues TMA loads into a 4-stage shared-memory
+// Roles (320 threads): warp 0 issues TMA loads into a 4-stage shared-memory
 // ring, warp 1 owns TMEM and issues tcgen05.mma (128 x 256 x 16, bf16 in, fp32
-// accumulate), warps 2-5 drain the accumulator (tcgen05.ld) and run the
+// accumulate), warps 2-9 drain the accumulator (tcgen05.ld; two warps per TMEM
+// lane quadrant, each taking half of the columns) and run the
 // epilogue.  Two 256-column TMEM accumulators let the epilogue of one tile
 // overlap the main loop of the next.  Every wait is bounded (kWaitLimitNs);
 // a timeout sets the error word and all roles return after their in-flight
@@ -33,10 +34,11 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // every mode moves exactly this per k-block
 constexpr int ATOM_BYTES = 64 * BK * 2;         // MN-major block: 64 elements x 64 k-rows
-constexpr int EPI_WARP_BYTES = 2 * 32 * 128;     // two 32-row x 128-B fp32 staging boxes
-constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;     // per CTA (weight-gradient modes only)
+constexpr int EPI_WARPS = 8;                      // two per TMEM lane quadrant
+constexpr int EPI_WARP_BYTES = 32 * 128;          // one 32-row x 128-B fp32 staging box
+constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;  // per CTA (weight-gradient modes only)
 constexpr int CTL_BYTES = 256;
-constexpr int THREADS = 192;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;     // TMA warp, MMA warp, epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 
 enum Mode : int { GATEUP = 0, DOWN = 1, DH = 2, DX = 3, WG2 = 4, WG13 = 5, GATE = 6 };
@@ -67,7 +69,7 @@ struct alignas(8) SharedCtl {
 };
 
 struct Item {
-  int e, row0, row_end, mt, nt, kblocks, krow0;
+  int e, row0, row_end, mt, nt, kblocks, krow0, krows;   // krows: K rows (weight-gradient modes)
 };
 
 __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int item, Item& it) {
@@ -78,7 +80,7 @@ __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int ite
     it.row_end = g.N;
     it.e = 0;
     it.mt = 0;
-    it.krow0 = 0;
+    it.krow0 = it.krows = 0;
     it.kblocks = g.kblocks;
     return true;
   }
@@ -89,8 +91,8 @@ __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int ite
     it.mt = rem / g.n_tiles_n;
     it.nt = rem % g.n_tiles_n;
     it.krow0 = g.offsets[it.e];
-    const int rows = g.offsets[it.e + 1] - it.krow0;
-    it.kblocks = ceil_div(rows, BK);
+    it.krows = g.offsets[it.e + 1] - it.krow0;
+    it.kblocks = ceil_div(it.krows, BK);
     it.row0 = it.row_end = 0;
     return true;
   }
@@ -101,7 +103,7 @@ __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int ite
   it.e = tl.y;
   it.row_end = g.offsets[it.e + 1];
   it.mt = 0;
-  it.krow0 = 0;
+  it.krow0 = it.krows = 0;
   it.kblocks = g.kblocks;
   return true;
 }
@@ -144,7 +146,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
-      mbar_init(smem_u32(&ctl->tempty[a]), 4);
+      mbar_init(smem_u32(&ctl->tempty[a]), EPI_WARPS);
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     ctl->abort = 0;
@@ -261,18 +263,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           // The expert's last K-block may hold rows of the next expert: issue
           // MMAs only for the 16-row groups that contain real rows, and zero the
           // foreign rows inside the last of those groups.
-          const int rem = (g.offsets[it.e + 1] - it.krow0) - kb * BK;
+          const int rem = it.krows - kb * BK;
           if (rem < BK) {
             kk_end = ceil_div(rem, 16);
             const int z1 = kk_end * 16;
             if (rem < z1) {
-              const int per_atom = (z1 - rem) * 8;   // 16-byte chunks per 64-element block
-              for (int q = lane; q < 6 * per_atom; q += 32) {
-                const int atom = q / per_atom, w = q % per_atom;
-                const int row = rem + w / 8, chunk = w % 8;
-                uint8_t* p = tile_ptr + s * STAGE_BYTES + atom * ATOM_BYTES + row * 128 + chunk * 16;
-                *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
-              }
+              // rows rem .. z1-1 of each of the stage's six 64-element blocks:
+              // (z1 - rem) rows x 8 chunks of 16 B, lane-strided within a block
+              const int per_atom = (z1 - rem) * 8;
+              uint8_t* base = tile_ptr + s * STAGE_BYTES + rem * 128;
+#pragma unroll
+              for (int atom = 0; atom < 6; ++atom)
+                for (int w = lane; w < per_atom; w += 32)
+                  *reinterpret_cast<uint4*>(base + atom * ATOM_BYTES + (w >> 3) * 128 + (w & 7) * 16) =
+                      make_uint4(0, 0, 0, 0);
               fence_proxy_async_smem();
             }
           }
@@ -315,7 +319,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
     const int r_local = q * 32 + lane;   // accumulator row owned by this thread
-    int epi_buf = 0;                     // staging box in use (weight-gradient modes)
+    const int half = (warp - 2) >> 2;    // which half of the tile's columns this warp drains
     int j = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
       Item it;
@@ -330,7 +334,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       if (MODE == GATEUP) {
         const int row = it.row0 + r_local;
         const bool valid = row < it.row_end;
-        for (int c = 0; c < 128; c += 16) {
+        for (int c = half * 64; c < half * 64 + 64; c += 16) {
           float a[16], b[16];
           tmem_ld16(t_row + c, a);
           tmem_ld16(t_row + 128 + c, b);
@@ -352,7 +356,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int row = it.row0 + r_local;
         const bool valid = row < it.row_end;
         const int parts = it.kblocks < 4 ? it.kblocks : 4;
-        for (int c = 0; c < 128; c += 16) {
+        for (int c = half * 64; c < half * 64 + 64; c += 16) {
           float v[16];
           tmem_ld16(t_row + c, v);
           tmem_ld_wait();
@@ -373,7 +377,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       } else if (MODE == DOWN || MODE == DX) {
         const int row = it.row0 + r_local;
         const bool valid = row < it.row_end;
-        for (int c = 0; c < BN; c += 16) {
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 16) {
           float v[16];
           tmem_ld16(t_row + c, v);
           tmem_ld_wait();
@@ -400,10 +404,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
         };
         uint4 na[2], nb[2];
-        load_ab(0, na, nb);   // the next chunk's loads are in flight while this one computes
-        for (int c = 0; c < BN; c += 16) {
+        const int c0 = half * (BN / 2), c1 = c0 + BN / 2;
+        load_ab(c0, na, nb);  // the next chunk's loads are in flight while this one computes
+        for (int c = c0; c < c1; c += 16) {
           uint4 ca[2] = {na[0], na[1]}, cb[2] = {nb[0], nb[1]};
-          if (c + 16 < BN) load_ab(c + 16, na, nb);
+          if (c + 16 < c1) load_ab(c + 16, na, nb);
           float dh[16];
           tmem_ld16(t_row + c, dh);
           tmem_ld_wait();
@@ -426,9 +431,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
         }
       } else {  // WG2 / WG13: fp32 weight gradients, staged and written by TMA stores
-        // This warp owns output rows m0 .. m0+31 of expert e.  Each 32-column
-        // chunk goes TMEM -> registers -> a 128-B-swizzled 32x32 fp32 box in
-        // shared memory -> one bulk tensor store; two boxes per warp alternate.
+        // This warp owns output rows m0 .. m0+31 of expert e and half of the
+        // columns.  Each 32-column chunk goes TMEM -> registers -> a
+        // 128-B-swizzled 32x32 fp32 box in shared memory -> one bulk tensor store.
         const int m0 = it.mt * BM + q * 32;
         const int mrows = (MODE == WG2) ? g.d : 2 * g.f;
         const int ncols = (MODE == WG2) ? g.f : g.d;
@@ -438,9 +443,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           map = &tmC2;
           mrow = m0 - g.f;
         }
-        const uint32_t box0 = tile_base + STAGES * STAGE_BYTES + (warp - 2) * EPI_WARP_BYTES;
-        uint8_t* box0_ptr = tile_ptr + STAGES * STAGE_BYTES + (warp - 2) * EPI_WARP_BYTES;
-        for (int c = 0; c < BN; c += 32) {
+        const uint32_t box = tile_base + STAGES * STAGE_BYTES + (warp - 2) * EPI_WARP_BYTES;
+        uint8_t* box_ptr = tile_ptr + STAGES * STAGE_BYTES + (warp - 2) * EPI_WARP_BYTES;
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           float v[32];
           if (it.kblocks > 0) {
             tmem_ld16(t_row + c, v);
@@ -452,9 +457,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
           const int col = it.nt * BN + c;
           if (m0 >= mrows || col >= ncols) continue;          // warp-uniform
-          if (lane == 0) bulk_wait_read_1();                  // this box's last store has read it
+          if (lane == 0) bulk_wait_read_0();                  // the box's last store has read it
           __syncwarp();
-          uint8_t* bp = box0_ptr + epi_buf * (EPI_WARP_BYTES / 2);
+          uint8_t* bp = box_ptr;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             const int phys = lane * 128 + ((ch ^ (lane & 7)) * 16);
@@ -464,10 +469,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(map, box0 + epi_buf * (EPI_WARP_BYTES / 2), col, mrow, it.e);
+            tma_store_3d(map, box, col, mrow, it.e);
             bulk_commit();
           }
-          epi_buf ^= 1;
         }
       }
       tc_fence_before();

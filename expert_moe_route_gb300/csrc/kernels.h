@@ -53,6 +53,12 @@ cudaError_t launch_dispatch(const uint16_t* x, const int32_t* idx, int T, int d,
                             int32_t* slot_row, uint16_t* x_perm, void* ws, int* err,
                             cudaStream_t s);
 cudaError_t dispatch_set_smem_limits();
+cudaError_t launch_dispatch_fp8(const uint16_t* x, const int32_t* idx, int T, int d, int E, int R,
+                                int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                                int32_t* slot_row, uint8_t* xq, float* xs, void* ws, int* err,
+                                cudaStream_t s);
+cudaError_t launch_dequant_fp8(const uint8_t* xq, const float* xs, long long N, int d,
+                               uint16_t* out, cudaStream_t s);
 
 cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const float* w, int T,
                            int d, int R, uint16_t* y, cudaStream_t s);
@@ -73,8 +79,9 @@ cudaError_t launch_bwd_route(const uint16_t* dy, const uint16_t* o, const int32_
                              const float* w, int T, int d, int R, uint16_t* dO, float* dsel_tok,
                              float* dsel_row, cudaStream_t s);
 cudaError_t launch_wg_transpose(const float* wg, int d, int E, float* wgT, cudaStream_t s);
+size_t dwg_ws_bytes(int d, int E);
 cudaError_t launch_dwg(const uint16_t* x_perm, const int32_t* offsets, const float* dsel_row,
-                       int d, int E, float* dW_gate, cudaStream_t s);
+                       int d, int E, float* dW_gate, void* ws, cudaStream_t s);
 cudaError_t launch_dx_combine(const uint16_t* dx_perm, const int32_t* slot_row,
                               const int32_t* idx, const float* dsel_tok, const float* wgT, int T,
                               int d, int E, int R, uint16_t* dx, cudaStream_t s);

@@ -158,6 +158,33 @@ moe_status_t moe_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int
                           moe_stream_t stream);
 
 /*
+ * moe_dispatch_fp8 -- dispatch in block-scaled fp8 (section "Evaluation": the
+ * page dispatches tokens in block-scaled fp8 and combines in bf16).  Same plan
+ * as moe_dispatch (counts, offsets, row_slot, slot_row); instead of bf16 rows
+ * it writes, per row and per 128-channel block b of the row's token x_t:
+ *   xscale_perm[row, b] = amax_b / 448          (fp32; amax_b = max |x_t| over the block)
+ *   xq_perm[row, c]     = E4M3(x_t[c] / xscale) (OCP E4M3 codes, round to nearest
+ *                                                even, saturating at +-448)
+ * An all-zero block has scale 0 and zero codes; code * scale approximates x
+ * within half an E4M3 step (2^-4 relative).  d must be a multiple of 128.
+ * xq_perm: uint8 [T*R, d]; xscale_perm: fp32 [T*R, d/128].  Workspace as for
+ * moe_dispatch.
+ */
+moe_status_t moe_dispatch_fp8(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E,
+                              int R, int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                              int32_t* slot_row, uint8_t* xq_perm, float* xscale_perm, void* ws,
+                              size_t* ws_bytes, unsigned flags, moe_stream_t stream);
+
+/*
+ * moe_dequant_fp8 -- out[i, c] = bf16(E4M3 value of xq[i, c] * xscale[i, c/128])
+ * for N rows of width d (d a multiple of 128): the identity expert on
+ * fp8-dispatched rows.  xq: uint8 [N, d]; xscale: fp32 [N, d/128]; out: bf16
+ * [N, d].  No workspace.
+ */
+moe_status_t moe_dequant_fp8(const uint8_t* xq, const float* xscale, int N, int d, uint16_t* out,
+                             moe_stream_t stream);
+
+/*
  * moe_grouped_ffn -- the grouped GEMMs that apply each expert's weights to its
  * rows (section "MoE all-to-all over EFA"), as a SwiGLU FFN.  For every expert
  * e and row i in [offsets[e], offsets[e+1]):

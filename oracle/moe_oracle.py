@@ -216,6 +216,82 @@ def combine(o, slot_row, w, T, R, rounding=True):
 
 
 # ----------------------------------------------------------------------------
+# Block-scaled fp8 dispatch ("Enabling trillion-parameter models on AWS EFA",
+# section "Evaluation": tokens are dispatched in block-scaled fp8 and combined
+# in bf16).  Reading: E4M3 codes (the OCP 8-bit E4M3 format without
+# infinities), one fp32 scale per token and 128 consecutive hidden channels,
+# scale = amax / 448 so the block's largest magnitude maps to the largest
+# finite code; codes are rounded to nearest even from the fp32 quotient
+# x / scale and saturate at +-448.
+# ----------------------------------------------------------------------------
+E4M3_MAX = 448.0
+FP8_BLOCK = 128
+
+
+def e4m3_decode(codes):
+    """E4M3 bit patterns (uint8) -> float64: 1 sign, 4 exponent bits (bias 7),
+    3 fraction bits; exponent 0 is subnormal (fraction * 2^-9); exponent 15 with
+    fraction 7 is NaN; there are no infinities."""
+    b = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b >> 7, -1.0, 1.0)
+    ex = (b >> 3) & 0xF
+    fr = b & 0x7
+    mag = np.where(ex == 0, fr * 2.0 ** -9, (1.0 + fr / 8.0) * np.ldexp(1.0, ex - 7))
+    mag = np.where((ex == 15) & (fr == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_round(v):
+    """Nearest E4M3 value, ties to even, magnitudes above 448 saturate to 448.
+
+    A value |v| in [2^k, 2^(k+1)) with k >= -6 keeps 4 significant bits
+    (spacing 2^(k-3)); below 2^-6 the spacing is the subnormal step 2^-9.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, e = np.frexp(a)                                  # a = m 2^e, 0.5 <= m < 1
+    q = np.ldexp(1.0, np.maximum(e - 1 - 3, -9))
+    r = np.rint(a / q) * q
+    r = np.where(a == 0, 0.0, np.minimum(r, E4M3_MAX))
+    return np.copysign(r, v)
+
+
+def e4m3_encode(vals):
+    """E4M3-representable float64 values -> their uint8 codes."""
+    table = e4m3_decode(np.arange(256, dtype=np.uint8))
+    lookup = {float(table[c]): c for c in range(256) if np.isfinite(table[c]) and c != 0x80}
+    flat = [lookup[float(x)] if x != 0 or not np.signbit(x) else 0x80
+            for x in np.asarray(vals, np.float64).ravel()]
+    return np.array(flat, dtype=np.uint8).reshape(np.shape(vals))
+
+
+def quantize_fp8_blocks(x):
+    """Per token and 128-channel block: scale = fp32(amax / 448), codes =
+    e4m3(fp32(x / scale)).  x: bf16 bits or values [T, d] with d % 128 == 0.
+    Returns codes uint8 [T, d] and scales float32 [T, d/128]; an all-zero block
+    has scale 0 and zero codes."""
+    xv = values(x).astype(np.float32)
+    T, d = xv.shape
+    assert d % FP8_BLOCK == 0
+    blocks = xv.reshape(T, d // FP8_BLOCK, FP8_BLOCK)
+    amax = np.abs(blocks).max(axis=2)
+    scales = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scales > 0, scales, np.float32(1.0))
+    quot = (blocks / safe[:, :, None]).astype(np.float32)       # fp32 quotient
+    vals = e4m3_round(quot.astype(np.float64))
+    vals = np.where(scales[:, :, None] > 0, vals, 0.0)
+    return e4m3_encode(vals).reshape(T, d), scales
+
+
+def dequantize_fp8_blocks(codes, scales):
+    """codes [N, d] uint8, scales [N, d/128] -> float64 values code * scale."""
+    c = e4m3_decode(codes)
+    N, d = c.shape
+    return (c.reshape(N, d // FP8_BLOCK, FP8_BLOCK) * np.asarray(scales, np.float64)[:, :, None]
+            ).reshape(N, d)
+
+
+# ----------------------------------------------------------------------------
 # Whole layer.
 # ----------------------------------------------------------------------------
 def layer_fwd(x, w_gate, bias, W1, W3, W2, R, rounding=True,

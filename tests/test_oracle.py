@@ -365,3 +365,51 @@ def test_backward_rounding_points_applied():
         assert np.array_equal(fw[key], O.bf16_round(fw[key]))
     for key in ("dx", "do", "da", "db", "dx_perm"):
         assert np.array_equal(bw[key], O.bf16_round(bw[key]))
+
+
+# ---------------------------------------------------------------- fp8 (E4M3) dispatch
+def test_e4m3_decode_definition_cases():
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for code, val in cases.items():
+        assert O.e4m3_decode(np.array([code], np.uint8))[0] == val, hex(code)
+    assert np.isnan(O.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+    finite = O.e4m3_decode(np.arange(256, dtype=np.uint8))
+    finite = finite[np.isfinite(finite)]
+    assert len(finite) == 254 and np.abs(finite).max() == 448.0
+
+
+def test_e4m3_round_matches_torch_and_saturates():
+    r = _rng(20)
+    v = np.concatenate([r.standard_normal(100000) * 50, r.standard_normal(20000) * 1e-3,
+                        r.uniform(-464, 464, 20000)]).astype(np.float32)
+    grid = O.e4m3_decode(np.arange(256, dtype=np.uint8))
+    grid = grid[np.isfinite(grid)]
+    mids = ((grid[:-1] + grid[1:]) / 2)[np.abs(grid[:-1]) < 448]   # exact ties
+    v = np.concatenate([v, np.sort(grid).astype(np.float32), np.sort(mids).astype(np.float32)])
+    want = torch.tensor(v).to(torch.float8_e4m3fn).to(torch.float64).numpy()   # RNE
+    got = O.e4m3_round(v.astype(np.float64))
+    assert np.array_equal(got, want)
+    # hand cases: ties to even and saturation (torch overflows to NaN instead)
+    assert list(O.e4m3_round(np.array([1.0625, 1.1875, 464.0, 500.0, -1e9, 2.0 ** -10, 3 * 2.0 ** -10]))) \
+        == [1.0, 1.25, 448.0, 448.0, -448.0, 0.0, 2.0 ** -8]
+
+
+def test_fp8_block_quantization_properties():
+    r = _rng(21)
+    x = _bf16_bits_of(r.standard_normal((7, 512)) * np.exp(r.uniform(-6, 6, (7, 1))))
+    codes, scales = O.quantize_fp8_blocks(x)
+    xv = O.bf16_to_f64(x)
+    blocks = xv.reshape(7, 4, 128)
+    # the block's largest magnitude maps to the largest finite code
+    assert np.array_equal(scales, (np.abs(blocks).max(2).astype(np.float32) / np.float32(448)))
+    dec = O.e4m3_decode(codes).reshape(7, 4, 128)
+    assert (np.abs(dec).max(axis=2) == 448.0).all()
+    # round trip within half an E4M3 step: relative 2^-4 for normal codes
+    back = O.dequantize_fp8_blocks(codes, scales).reshape(7, 4, 128)
+    tol = np.maximum(np.abs(blocks) * 2.0 ** -4, scales[:, :, None].astype(np.float64) * 2.0 ** -10)
+    assert (np.abs(back - blocks) <= tol * (1 + 1e-6)).all()
+    # an all-zero block: scale 0, zero codes
+    z = np.zeros((1, 256), np.uint16)
+    c0, s0 = O.quantize_fp8_blocks(z)
+    assert not c0.any() and not s0.any()
