@@ -17,6 +17,7 @@ from . import build as _build
 MOE_OK = 0
 MOE_LOGITS_IN = 0x1
 MOE_CHECK = 0x2
+MOE_WEIGHTS_PREPACKED = 0x4
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CUDA"}
 
@@ -24,7 +25,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 SYMBOLS = ("moe_status_string", "moe_version", "moe_trace_events", "moe_kernel_launches",
            "moe_selftest_wait_timeout",
            "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_dispatch_fp8",
-           "moe_dequant_fp8", "moe_grouped_ffn",
+           "moe_dequant_fp8", "moe_prepack_weights", "moe_grouped_ffn",
            "moe_combine", "moe_layer_fwd", "moe_layer_bwd")
 
 # moe_stage_t
@@ -78,6 +79,8 @@ def _declare(lib):
                                      _szp, _u, _vp]
     lib.moe_dequant_fp8.restype = _i
     lib.moe_dequant_fp8.argtypes = [_vp, _vp, _i, _i, _vp, _vp]
+    lib.moe_prepack_weights.restype = _i
+    lib.moe_prepack_weights.argtypes = [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]
     lib.moe_grouped_ffn.restype = _i
     lib.moe_grouped_ffn.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _vp, _szp, _u, _vp]
@@ -238,6 +241,15 @@ def moe_grouped_ffn(x_perm, offsets, W1, W3, W2, h, out, ws, a_save=None, b_save
                                _p(a_save), _p(b_save), _p(h), _p(out), _p(ws), ctypes.byref(n),
                                flags, _stream(stream))
     _check(st, "moe_grouped_ffn")
+
+
+def moe_prepack_weights(W1, W3, W2, W1p, W3p, W2p, stream=None):
+    """Forward weight tiles (see include/moe.h); returns nothing, fills W1p, W3p, W2p."""
+    E, f, d = W1.shape
+    for name, t in (("W1", W1), ("W3", W3), ("W2", W2), ("W1p", W1p), ("W3p", W3p), ("W2p", W2p)):
+        _dt(t, torch.bfloat16, name)
+    _check(lib().moe_prepack_weights(_p(W1), _p(W3), _p(W2), E, d, f, _p(W1p), _p(W3p), _p(W2p),
+                                     _stream(stream)), "moe_prepack_weights")
 
 
 def moe_combine(expert_out, slot_row, topk_w, y, R, stream=None):

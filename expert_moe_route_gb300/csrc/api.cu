@@ -259,6 +259,7 @@ moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int
                              void* ws, size_t* ws_bytes, unsigned flags, moe_stream_t stream) {
   if (N < 0 || d <= 0 || f <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
   if (d % 8 || f % 8 || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if ((flags & MOE_WEIGHTS_PREPACKED) && !prepack_supported(d, f)) return MOE_ERR_UNSUPPORTED;
   if (!ws_bytes) return MOE_ERR_INVALID_ARG;
   const size_t need = kErrBytes + tiles_ws_bytes(N, E);
   if (!ws) {
@@ -277,8 +278,23 @@ moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int
   int* err = static_cast<int*>(ws);
   MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
   cudaError_t e = launch_ffn_fwd(x_perm, offsets, N, d, f, E, W1, W3, W2, a_save, b_save, h, out,
-                                 static_cast<uint8_t*>(ws) + kErrBytes, err, s);
+                                 static_cast<uint8_t*>(ws) + kErrBytes, err,
+                                 (flags & MOE_WEIGHTS_PREPACKED) != 0, s);
   return finish(e, err, flags, s);
+}
+
+moe_status_t moe_prepack_weights(const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, int E,
+                                 int d, int f, uint16_t* W1p, uint16_t* W3p, uint16_t* W2p,
+                                 moe_stream_t stream) {
+  if (E <= 0 || d <= 0 || f <= 0) return MOE_ERR_INVALID_ARG;
+  if (!prepack_supported(d, f) || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (!W1 || !W3 || !W2 || !W1p || !W3p || !W2p) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {W1, W3, W2, W1p, W3p, W2p};
+  for (const void* p : ps)
+    if (!al16(p)) return MOE_ERR_UNSUPPORTED;
+  if (!init_once()) return MOE_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  return finish(launch_prepack(W1, W3, W2, E, d, f, W1p, W3p, W2p, s), nullptr, 0, s);
 }
 
 moe_status_t moe_combine(const uint16_t* expert_out, const int32_t* slot_row, const float* topk_w,
@@ -320,6 +336,7 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
                            moe_stream_t stream) {
   moe_status_t st = check_layer(L);
   if (st != MOE_OK) return st;
+  if ((flags & MOE_WEIGHTS_PREPACKED) && !prepack_supported(L->d, L->f)) return MOE_ERR_UNSUPPORTED;
   if (!ws_bytes) return MOE_ERR_INVALID_ARG;
   const size_t need = layer_fwd_ws(L);
   if (!ws) {
@@ -327,6 +344,7 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
     return MOE_OK;
   }
   if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
+  if (L->T == 0) return MOE_OK;   // nothing to route: no buffer is touched
   if (!sv || !x || !y) return MOE_ERR_INVALID_ARG;
   if (!sv->logits || !sv->topk_idx || !sv->topk_w || !sv->counts || !sv->offsets ||
       !sv->row_slot || !sv->slot_row || !sv->x_perm || !sv->h || !sv->o)
@@ -335,7 +353,6 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   const void* ps[] = {x, y, sv->x_perm, sv->a, sv->b, sv->h, sv->o};
   for (const void* p : ps)
     if (p && !al16(p)) return MOE_ERR_UNSUPPORTED;
-  if (L->T == 0) return MOE_OK;
   if (!init_once()) return MOE_ERR_CUDA;
   const int T = L->T, d = L->d, E = L->E, R = L->R, f = L->f, N = T * R;
   cudaStream_t s = S(stream);
@@ -359,7 +376,7 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
                             sv->slot_row, sv->x_perm, dws, err, s));
   }
   MOE_TRY(launch_ffn_fwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
-                         sv->h, sv->o, tws, err, s));
+                         sv->h, sv->o, tws, err, (flags & MOE_WEIGHTS_PREPACKED) != 0, s));
   cudaError_t e;
   {
     Stage st_(s, MOE_STAGE_COMBINE);
@@ -388,7 +405,7 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
                            moe_stream_t stream) {
   moe_status_t st = check_layer(L);
   if (st != MOE_OK) return st;
-  if (L->d % 64 || L->f % 64) return MOE_ERR_UNSUPPORTED;
+  if (L->d % 64 || L->f % 64 || (flags & MOE_WEIGHTS_PREPACKED)) return MOE_ERR_UNSUPPORTED;
   if (!ws_bytes) return MOE_ERR_INVALID_ARG;
   const size_t need = layer_bwd_ws(L);
   if (!ws) {
@@ -396,7 +413,18 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
     return MOE_OK;
   }
   if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
-  if (!sv || !x || !dy || !dx || !dW_gate || !dW1 || !dW3 || !dW2) return MOE_ERR_INVALID_ARG;
+  if (!dW_gate || !dW1 || !dW3 || !dW2) return MOE_ERR_INVALID_ARG;
+  if (L->T == 0) {   // no tokens: every gradient is zero
+    if (!al16(dW_gate) || !al16(dW1) || !al16(dW3) || !al16(dW2)) return MOE_ERR_UNSUPPORTED;
+    if (!init_once()) return MOE_ERR_CUDA;
+    cudaStream_t s0 = S(stream);
+    const size_t d = L->d, E = L->E, f = L->f;
+    MOE_TRY(cudaMemsetAsync(dW_gate, 0, sizeof(float) * d * E, s0));
+    MOE_TRY(cudaMemsetAsync(dW1, 0, sizeof(float) * E * f * d, s0));
+    MOE_TRY(cudaMemsetAsync(dW3, 0, sizeof(float) * E * f * d, s0));
+    return finish(cudaMemsetAsync(dW2, 0, sizeof(float) * E * f * d, s0), nullptr, flags, s0);
+  }
+  if (!sv || !x || !dy || !dx) return MOE_ERR_INVALID_ARG;
   if (!sv->a || !sv->b || !sv->h || !sv->o || !sv->x_perm || !sv->topk_idx || !sv->topk_w ||
       !sv->offsets || !sv->slot_row)
     return MOE_ERR_INVALID_ARG;

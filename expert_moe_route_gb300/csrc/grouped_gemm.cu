@@ -38,6 +38,7 @@ constexpr int EPI_WARPS = 8;                      // two per TMEM lane quadrant
 constexpr int EPI_WARP_BYTES = 32 * 128;          // one 32-row x 128-B fp32 staging box
 constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;  // per CTA (weight-gradient modes only)
 constexpr int CTL_BYTES = 256;
+
 constexpr int THREADS = 64 + 32 * EPI_WARPS;     // TMA warp, MMA warp, epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -189,16 +190,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const int kx = kb * BK;
           if (MODE == GATEUP) {
             tma_load_2d(sa, &tmA, bar, kx, it.row0);
-            const int brow = it.e * g.f + it.nt * 128;
-            tma_load_2d(sb, &tmB, bar, kx, brow);
-            tma_load_2d(sb + B_BYTES / 2, &tmB2, bar, kx, brow);
+            if (g.prepacked) {   // one contiguous 16 KB tile per box
+              const int rt = it.e * (g.f / 128) + it.nt;
+              tma_load_4d(sb, &tmB, bar, 0, 0, kb, rt);
+              tma_load_4d(sb + B_BYTES / 2, &tmB2, bar, 0, 0, kb, rt);
+            } else {
+              const int brow = it.e * g.f + it.nt * 128;
+              tma_load_2d(sb, &tmB, bar, kx, brow);
+              tma_load_2d(sb + B_BYTES / 2, &tmB2, bar, kx, brow);
+            }
           } else if (MODE == GATE) {
             // A repeats x for the hi, mid and lo thirds of K
             tma_load_2d(sa, &tmA, bar, kx % g.d, it.row0);
             tma_load_2d(sb, &tmB, bar, kx, it.nt * Tr::bn);
           } else if (MODE == DOWN) {
             tma_load_2d(sa, &tmA, bar, kx, it.row0);
-            tma_load_2d(sb, &tmB, bar, kx, it.e * g.d + it.nt * BN);
+            if (g.prepacked) {   // one contiguous 32 KB tile
+              const int rt = it.e * (g.d / BN) + it.nt;
+              tma_load_4d(sb, &tmB, bar, 0, 0, kb, rt);
+            }
+            else
+              tma_load_2d(sb, &tmB, bar, kx, it.e * g.d + it.nt * BN);
           } else if (MODE == DH) {
             tma_load_2d(sa, &tmA, bar, kx, it.row0);
 #pragma unroll
@@ -492,6 +504,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   }
 }
 
+// Weight prepacking: W [E * rows_per_e, K] row-major -> tiles
+// [E * rows_per_e / TR][K / 64][TR][64]; each (row tile, k-block) box of the
+// forward GEMMs becomes one contiguous TR * 128-byte region.  One thread moves
+// 16 bytes (8 bf16).
+__global__ void prepack_kernel(const uint16_t* __restrict__ W, long long rows, int K, int TR,
+                               uint16_t* __restrict__ Wp) {
+  const long long chunks = rows * (K / 8);
+  const int kb_n = K / 64;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < chunks;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / (K / 8);
+    const int c8 = (int)(i % (K / 8));          // 16-byte chunk within the row
+    const int kb = c8 / 8, cin = c8 % 8;
+    const long long rt = r / TR;
+    const int rin = (int)(r % TR);
+    const size_t dst = (((size_t)rt * kb_n + kb) * TR + rin) * 64 + (size_t)cin * 8;
+    reinterpret_cast<uint4*>(Wp)[dst / 8] = reinterpret_cast<const uint4*>(W)[i];
+  }
+}
+
 // Ragged M tiles: expert e's rows [offsets[e], offsets[e+1]) split into 128-row
 // tiles; tiles[i] = {first row, expert}, ordered by expert then row.
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
@@ -576,6 +608,20 @@ bool make_map_f32_3d(CUtensorMap* m, void* base, long long E, long long rows, lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Prepacked weight tiles [tiles][kb][rows][64] viewed 4-D: {64, rows, kblocks, tiles}.
+bool make_map_tiles(CUtensorMap* m, const void* base, long long tiles, long long kblocks,
+                    int rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)kblocks, (cuuint64_t)tiles};
+  cuuint64_t strides[3] = {128, (cuuint64_t)rows * 128, (cuuint64_t)kblocks * rows * 128};
+  cuuint32_t box[4] = {64u, (cuuint32_t)rows, 1u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n[64] = {0};
   int dev = 0;
@@ -631,6 +677,19 @@ cudaError_t launch_gate_tc(const uint16_t* x, const float* wg, const float* bias
   return launch_mode<GATE>(ma, mb, mb, ma, ma, g, (long long)g.n_tiles_m * g.n_tiles_n, s);
 }
 
+bool prepack_supported(int d, int f) { return d % BN == 0 && f % 128 == 0; }
+
+cudaError_t launch_prepack(const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, int E,
+                           int d, int f, uint16_t* W1p, uint16_t* W3p, uint16_t* W2p,
+                           cudaStream_t s) {
+  const int blocks = 152 * 8;
+  prepack_kernel<<<blocks, 256, 0, s>>>(W1, (long long)E * f, d, 128, W1p);
+  prepack_kernel<<<blocks, 256, 0, s>>>(W3, (long long)E * f, d, 128, W3p);
+  prepack_kernel<<<blocks, 256, 0, s>>>(W2, (long long)E * d, f, BN, W2p);
+  count_launches(3);
+  return cudaGetLastError();
+}
+
 size_t tiles_ws_bytes(int N, int E) {
   return align_up(sizeof(int2) * ((size_t)ceil_div(N, BM) + E) + 16, 256);
 }
@@ -647,7 +706,7 @@ cudaError_t launch_build_tiles(const int32_t* offsets, int E, void* ws, cudaStre
 cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
-                           void* tiles_ws, int* err, cudaStream_t s) {
+                           void* tiles_ws, int* err, bool prepacked, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   trace_begin(MOE_STAGE_GATEUP, s);
   cudaError_t e = launch_build_tiles(offsets, E, tiles_ws, s);
@@ -661,8 +720,13 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   const long long max_m_tiles = ceil_div(N, BM) + E;
   CUtensorMap ma, mb, mb2;
   // gate-up: A = x_perm, B = W1 / W3 rows (128 per tile each)
-  if (!make_map(&ma, x_perm, N, d, BM) || !make_map(&mb, W1, (long long)E * f, d, 128) ||
-      !make_map(&mb2, W3, (long long)E * f, d, 128))
+  g.prepacked = prepacked ? 1 : 0;
+
+  if (!make_map(&ma, x_perm, N, d, BM)) return cudaErrorInvalidValue;
+  if (prepacked ? !(make_map_tiles(&mb, W1, (long long)E * f / 128, d / 64, 128) &&
+                    make_map_tiles(&mb2, W3, (long long)E * f / 128, d / 64, 128))
+                : !(make_map(&mb, W1, (long long)E * f, d, 128) &&
+                    make_map(&mb2, W3, (long long)E * f, d, 128)))
     return cudaErrorInvalidValue;
   g.kblocks = ceil_div(d, BK);
   g.n_tiles_n = ceil_div(f, 128);
@@ -671,11 +735,14 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   trace_end(MOE_STAGE_GATEUP, s);
   if (e != cudaSuccess) return e;
   // down: A = h, B = W2 rows (256 per tile)
-  if (!make_map(&ma, h, N, f, BM) || !make_map(&mb, W2, (long long)E * d, f, BN))
+  if (!make_map(&ma, h, N, f, BM)) return cudaErrorInvalidValue;
+  if (prepacked ? !make_map_tiles(&mb, W2, (long long)E * d / BN, f / 64, BN)
+                : !make_map(&mb, W2, (long long)E * d, f, BN))
     return cudaErrorInvalidValue;
   g.kblocks = ceil_div(f, BK);
   g.n_tiles_n = ceil_div(d, BN);
   g.out_bf16 = out; g.save_a = g.save_b = nullptr;
+
   trace_begin(MOE_STAGE_DOWN, s);
   e = launch_mode<DOWN>(ma, mb, mb, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
   trace_end(MOE_STAGE_DOWN, s);

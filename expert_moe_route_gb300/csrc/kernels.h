@@ -20,6 +20,7 @@ struct GemmArgs {
   const int2* tiles;          // ragged 128-row tiles {first row, expert}
   const int32_t* tile_count;  // number of valid entries in tiles
   int kblocks;                // 64-deep k-blocks per tile (row-ragged modes)
+  int prepacked;              // forward weights in the tiled layout of moe_prepack_weights
   int n_tiles_n;              // output column tiles
   int n_tiles_m;              // output row tiles per expert (weight-gradient modes)
   uint16_t* out_bf16;
@@ -67,7 +68,13 @@ size_t tiles_ws_bytes(int N, int E);
 cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
-                           void* tiles_ws, int* err, cudaStream_t s);
+                           void* tiles_ws, int* err, bool prepacked, cudaStream_t s);
+// Weight tiles for the forward GEMMs: W1p, W3p [E][f/128][d/64][128][64] and
+// W2p [E][d/256][f/64][256][64] (bf16), each tile one TMA box, contiguous.
+bool prepack_supported(int d, int f);
+cudaError_t launch_prepack(const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, int E,
+                           int d, int f, uint16_t* W1p, uint16_t* W3p, uint16_t* W2p,
+                           cudaStream_t s);
 cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            const uint16_t* a_s, const uint16_t* b_s, const uint16_t* h,

@@ -64,6 +64,8 @@ typedef void* moe_stream_t;  /* cudaStream_t */
 /* flags */
 #define MOE_LOGITS_IN 0x1u   /* moe_route: `logits` is an input; skip the gate projection */
 #define MOE_CHECK 0x2u       /* wait for the call's work and report device-side errors */
+#define MOE_WEIGHTS_PREPACKED 0x4u  /* moe_grouped_ffn / moe_layer_fwd: W1, W3, W2 are the
+                                       tiles written by moe_prepack_weights */
 
 /* Stages of moe_layer_fwd / moe_layer_bwd, for moe_trace_events. */
 typedef enum {
@@ -200,6 +202,22 @@ moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int
                              int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                              uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
                              void* ws, size_t* ws_bytes, unsigned flags, moe_stream_t stream);
+
+/*
+ * moe_prepack_weights -- copy the expert weights into the tile layout the
+ * forward grouped GEMMs stream (a performance layout for forward-only use, e.g.
+ * inference; the page's grouped GEMMs take the weights as they are):
+ *   W1p, W3p[e][j][k][r][c] = W1, W3[e][128 j + r][64 k + c]   ([E][f/128][d/64][128][64])
+ *   W2p[e][j][k][r][c]      = W2[e][256 j + r][64 k + c]       ([E][d/256][f/64][256][64])
+ * so that every 128x64 (W1, W3) or 256x64 (W2) box the GEMM loads is one
+ * contiguous 16 or 32 KB region.  Requires d % 256 == 0 and f % 128 == 0.
+ * Pass MOE_WEIGHTS_PREPACKED to moe_grouped_ffn / moe_layer_fwd to use them
+ * (same results, bit for bit); moe_layer_bwd takes the plain layout only.
+ * W1p, W3p, W2p: bf16, the sizes of W1, W3, W2; must not alias them.
+ */
+moe_status_t moe_prepack_weights(const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, int E,
+                                 int d, int f, uint16_t* W1p, uint16_t* W3p, uint16_t* W2p,
+                                 moe_stream_t stream);
 
 /*
  * moe_combine -- bring each token's R expert outputs back and take their
