@@ -32,7 +32,6 @@ namespace {
 constexpr int BM = 128, BK = 64, BN = 256, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // every mode moves exactly this per k-block
 constexpr int ATOM_BYTES = 64 * BK * 2;         // MN-major block: 64 elements x 64 k-rows
 constexpr int EPI_WARPS = 8;                      // two per TMEM lane quadrant
 constexpr int EPI_WARP_BYTES = 32 * 128;          // one 32-row x 128-B fp32 staging box
@@ -42,7 +41,8 @@ constexpr int CTL_BYTES = 256;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;     // TMA warp, MMA warp, epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 
-enum Mode : int { GATEUP = 0, DOWN = 1, DH = 2, DX = 3, WG2 = 4, WG13 = 5, GATE = 6 };
+enum Mode : int { GATEUP = 0, DOWN = 1, DH = 2, DX = 3, WG2 = 4, WG13 = 5, GATE = 6,
+                  GATEUP2 = 7, DOWN2 = 8 };
 
 template <int M> struct Traits {
   static constexpr bool a_mn = (M == WG2 || M == WG13);
@@ -54,9 +54,22 @@ template <int M> struct Traits {
   // quarter of the tensor core's accumulation steps.
   static constexpr bool partials = (M == GATE);
   static constexpr int bn = partials ? 128 : BN;
-  static constexpr uint32_t stage_tx = partials ? A_BYTES + 128 * BK * 2 : STAGE_BYTES;
+  // GATEUP2 / DOWN2: each item is a 256-row block of one expert, computed as
+  // two 128-row accumulators (TMEM columns 0-255 and 256-511) that share every
+  // B (weight) stage: each weight tile is read once per 256 rows and each SM
+  // keeps twice the distinct weight bytes in flight -- the weight-streaming
+  // regime (few rows per expert).  No second accumulator set, so the epilogue
+  // does not overlap the next item's main loop.
+  static constexpr bool pair = (M == GATEUP2 || M == DOWN2);
+  static constexpr bool is_gateup = (M == GATEUP || M == GATEUP2);
+  static constexpr bool is_down = (M == DOWN || M == DOWN2);
+  static constexpr bool single_acc = partials || pair;
+  static constexpr int stages = pair ? 3 : STAGES;
+  static constexpr int a_bytes = pair ? 2 * A_BYTES : A_BYTES;
+  static constexpr int stage_bytes = a_bytes + B_BYTES;
+  static constexpr uint32_t stage_tx = partials ? A_BYTES + 128 * BK * 2 : (uint32_t)stage_bytes;
   // stages | epilogue staging | control block, plus slack for 1024-B alignment
-  static constexpr int smem_bytes = STAGES * STAGE_BYTES + epi_bytes + CTL_BYTES + 1024;
+  static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + CTL_BYTES + 1024;
 };
 
 struct alignas(8) SharedCtl {
@@ -133,7 +146,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tile_base = (raw_addr + 1023u) & ~1023u;       // 1024-B aligned stages
   uint8_t* tile_ptr = smem_raw + (tile_base - raw_addr);
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(tile_ptr + STAGES * STAGE_BYTES + Tr::epi_bytes);
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(tile_ptr + Tr::stages * Tr::stage_bytes + Tr::epi_bytes);
   static_assert(sizeof(SharedCtl) <= CTL_BYTES, "control block");
   volatile int* abort_flag = &ctl->abort;
 
@@ -141,7 +154,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < Tr::stages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
@@ -154,7 +167,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (MODE == GATEUP || MODE == DX) tma_prefetch_desc(&tmB2);
+    if (Tr::is_gateup || MODE == DX) tma_prefetch_desc(&tmB2);
     if (Tr::wgrad) tma_prefetch_desc(&tmC);
     if (MODE == WG13) tma_prefetch_desc(&tmC2);
   }
@@ -177,18 +190,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         Item it;
         decode_item(g, MODE, item, it);
         for (int kb = 0; kb < it.kblocks; ++kb, ++it_count) {
-          const int s = it_count % STAGES;
-          const uint32_t ph = (it_count / STAGES) & 1u;
+          const int s = it_count % Tr::stages;
+          const uint32_t ph = (it_count / Tr::stages) & 1u;
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, g.err)) {
             ok = false;
             break;
           }
           const uint32_t bar = smem_u32(&ctl->full[s]);
-          const uint32_t sa = tile_base + s * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sa = tile_base + s * Tr::stage_bytes;
+          const uint32_t sb = sa + Tr::a_bytes;
           mbar_arrive_expect_tx(bar, Tr::stage_tx);
           const int kx = kb * BK;
-          if (MODE == GATEUP) {
+          if (Tr::pair) tma_load_2d(sa + A_BYTES, &tmA, bar, kx, it.row0 + BM);   // rows 128-255
+          if (Tr::is_gateup) {
             tma_load_2d(sa, &tmA, bar, kx, it.row0);
             if (g.prepacked) {   // one contiguous 16 KB tile per box
               const int rt = it.e * (g.f / 128) + it.nt;
@@ -203,7 +217,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // A repeats x for the hi, mid and lo thirds of K
             tma_load_2d(sa, &tmA, bar, kx % g.d, it.row0);
             tma_load_2d(sb, &tmB, bar, kx, it.nt * Tr::bn);
-          } else if (MODE == DOWN) {
+          } else if (Tr::is_down) {
             tma_load_2d(sa, &tmA, bar, kx, it.row0);
             if (g.prepacked) {   // one contiguous 32 KB tile
               const int rt = it.e * (g.d / BN) + it.nt;
@@ -236,12 +250,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }
       if (!ok) {
         // drain: the last (up to STAGES) issued loads must land before the CTA exits
-        const uint32_t n = it_count < (uint32_t)STAGES ? it_count : (uint32_t)STAGES;
+        const uint32_t n = it_count < (uint32_t)Tr::stages ? it_count : (uint32_t)Tr::stages;
         int dummy = 0;
         for (uint32_t q = 0; q < n; ++q) {
           const uint32_t c = it_count - 1 - q;
           volatile int never = 0;
-          mbar_wait_bounded(smem_u32(&ctl->full[c % STAGES]), (c / STAGES) & 1u, &never, &dummy);
+          mbar_wait_bounded(smem_u32(&ctl->full[c % Tr::stages]), (c / Tr::stages) & 1u, &never,
+                            &dummy);
         }
       }
     }
@@ -255,21 +270,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++j) {
       Item it;
       decode_item(g, MODE, item, it);
-      const int acc = Tr::partials ? 0 : (j & 1);
-      const uint32_t aph = Tr::partials ? (j & 1u) : ((j >> 1) & 1u);
+      const int acc = Tr::single_acc ? 0 : (j & 1);
+      const uint32_t aph = Tr::single_acc ? (j & 1u) : ((j >> 1) & 1u);
       ok = mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, g.err);
       ok = __all_sync(kFull, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t d_base = tmem_base + acc * BN;
       for (int kb = 0; kb < it.kblocks; ++kb, ++it_count) {
-        const int s = it_count % STAGES;
-        const uint32_t ph = (it_count / STAGES) & 1u;
+        const int s = it_count % Tr::stages;
+        const uint32_t ph = (it_count / Tr::stages) & 1u;
         ok = mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, g.err);
         ok = __all_sync(kFull, ok);
         if (!ok) break;
-        const uint32_t sa = tile_base + s * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
+        const uint32_t sa = tile_base + s * Tr::stage_bytes;
+        const uint32_t sb = sa + Tr::a_bytes;
         int kk_end = BK / 16;
         if (Tr::wgrad) {
           // The expert's last K-block may hold rows of the next expert: issue
@@ -283,7 +298,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               // rows rem .. z1-1 of each of the stage's six 64-element blocks:
               // (z1 - rem) rows x 8 chunks of 16 B, lane-strided within a block
               const int per_atom = (z1 - rem) * 8;
-              uint8_t* base = tile_ptr + s * STAGE_BYTES + rem * 128;
+              uint8_t* base = tile_ptr + s * Tr::stage_bytes + rem * 128;
 #pragma unroll
               for (int atom = 0; atom < 6; ++atom)
                 for (int w = lane; w < per_atom; w += 32)
@@ -306,6 +321,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint64_t bd = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, ATOM_BYTES, 1024)
                                          : smem_desc_sw128(sb + kk * 32, 16, 1024);
             tc_mma_bf16(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
+            if (Tr::pair && it.row_end - it.row0 > BM)   // rows 128-255 share the B stage
+              tc_mma_bf16(tmem_base + BN, smem_desc_sw128(sa + A_BYTES + kk * 32, 16, 1024), bd,
+                          idesc, (!first || kk > 0) ? 1u : 0u);
           }
           tc_commit(smem_u32(&ctl->empty[s]));   // frees the stage when these MMAs finish
           issued_any = true;
@@ -336,15 +354,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
       Item it;
       decode_item(g, MODE, item, it);
-      const int acc = Tr::partials ? 0 : (j & 1);
-      const uint32_t aph = Tr::partials ? (j & 1u) : ((j >> 1) & 1u);
+      const int acc = Tr::single_acc ? 0 : (j & 1);
+      const uint32_t aph = Tr::single_acc ? (j & 1u) : ((j >> 1) & 1u);
       bool ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag, g.err);
       ok = __all_sync(kFull, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      if (MODE == GATEUP) {
-        const int row = it.row0 + r_local;
+      for (int hh = 0; hh < (Tr::pair ? 2 : 1); ++hh) {   // row halves of a 256-row item
+      if (hh == 1 && it.row_end - it.row0 <= BM) break;
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + hh * BN;
+      if (Tr::is_gateup) {
+        const int row = it.row0 + hh * BM + r_local;
         const bool valid = row < it.row_end;
         for (int c = half * 64; c < half * 64 + 64; c += 16) {
           float a[16], b[16];
@@ -386,8 +406,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int u = 0; u < n; ++u) dst[u] = v[u] + (g.bias ? g.bias[col + u] : 0.f);
           }
         }
-      } else if (MODE == DOWN || MODE == DX) {
-        const int row = it.row0 + r_local;
+      } else if (Tr::is_down || MODE == DX) {
+        const int row = it.row0 + hh * BM + r_local;
         const bool valid = row < it.row_end;
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 16) {
           float v[16];
@@ -455,8 +475,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           map = &tmC2;
           mrow = m0 - g.f;
         }
-        const uint32_t box = tile_base + STAGES * STAGE_BYTES + (warp - 2) * EPI_WARP_BYTES;
-        uint8_t* box_ptr = tile_ptr + STAGES * STAGE_BYTES + (warp - 2) * EPI_WARP_BYTES;
+        const uint32_t box = tile_base + Tr::stages * Tr::stage_bytes + (warp - 2) * EPI_WARP_BYTES;
+        uint8_t* box_ptr = tile_ptr + Tr::stages * Tr::stage_bytes + (warp - 2) * EPI_WARP_BYTES;
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           float v[32];
           if (it.kblocks > 0) {
@@ -486,6 +506,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
         }
       }
+      }  // row halves
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
@@ -524,10 +545,12 @@ __global__ void prepack_kernel(const uint16_t* __restrict__ W, long long rows, i
   }
 }
 
-// Ragged M tiles: expert e's rows [offsets[e], offsets[e+1]) split into 128-row
-// tiles; tiles[i] = {first row, expert}, ordered by expert then row.
+// Ragged M tiles: expert e's rows [offsets[e], offsets[e+1]) split into
+// tile_rows-row tiles (128, or 256 for the paired modes); tiles[i] = {first row,
+// expert}, ordered by expert then row.
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
-                                                           int E, int2* __restrict__ tiles,
+                                                           int E, int tile_rows,
+                                                           int2* __restrict__ tiles,
                                                            int32_t* __restrict__ tile_count) {
   __shared__ int warp_sums[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -537,7 +560,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
     int r0 = 0, n = 0;
     if (e < E) {
       r0 = offsets[e];
-      n = ceil_div(offsets[e + 1] - r0, BM);
+      n = ceil_div(offsets[e + 1] - r0, tile_rows);
     }
     int incl = n;
 #pragma unroll
@@ -558,7 +581,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
     }
     __syncthreads();
     const int start = carry + (wid > 0 ? warp_sums[wid - 1] : 0) + incl - n;
-    for (int i = 0; i < n; ++i) tiles[start + i] = make_int2(r0 + i * BM, e);
+    for (int i = 0; i < n; ++i) tiles[start + i] = make_int2(r0 + i * tile_rows, e);
     carry += warp_sums[31];
     __syncthreads();
   }
@@ -694,10 +717,11 @@ size_t tiles_ws_bytes(int N, int E) {
   return align_up(sizeof(int2) * ((size_t)ceil_div(N, BM) + E) + 16, 256);
 }
 
-cudaError_t launch_build_tiles(const int32_t* offsets, int E, void* ws, cudaStream_t s) {
+cudaError_t launch_build_tiles(const int32_t* offsets, int E, void* ws, cudaStream_t s,
+                               int tile_rows = BM) {
   int32_t* count = static_cast<int32_t*>(ws);
   int2* tiles = reinterpret_cast<int2*>(static_cast<uint8_t*>(ws) + 16);
-  build_tiles_kernel<<<1, 1024, 0, s>>>(offsets, E, tiles, count);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(offsets, E, tile_rows, tiles, count);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -708,8 +732,13 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
                            void* tiles_ws, int* err, bool prepacked, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
+  // Few rows per expert (on average at most two 128-row tiles): the layer
+  // streams weights, so pair an expert's 128-row tiles in one CTA to share each
+  // weight tile (GATEUP2 / DOWN2); otherwise overlap epilogue and main loop.
+  const bool pair = (long long)N <= 2LL * BM * E;
+  const int tile_rows = pair ? 2 * BM : BM;
   trace_begin(MOE_STAGE_GATEUP, s);
-  cudaError_t e = launch_build_tiles(offsets, E, tiles_ws, s);
+  cudaError_t e = launch_build_tiles(offsets, E, tiles_ws, s, tile_rows);
   if (e != cudaSuccess) return e;
   GemmArgs g{};
   g.E = E; g.N = N; g.d = d; g.f = f;
@@ -717,7 +746,7 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.tile_count = static_cast<const int32_t*>(tiles_ws);
   g.tiles = reinterpret_cast<const int2*>(static_cast<const uint8_t*>(tiles_ws) + 16);
   g.err = err;
-  const long long max_m_tiles = ceil_div(N, BM) + E;
+  const long long max_m_tiles = ceil_div(N, tile_rows) + E;
   CUtensorMap ma, mb, mb2;
   // gate-up: A = x_perm, B = W1 / W3 rows (128 per tile each)
   g.prepacked = prepacked ? 1 : 0;
@@ -731,7 +760,8 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.kblocks = ceil_div(d, BK);
   g.n_tiles_n = ceil_div(f, 128);
   g.out_bf16 = h; g.save_a = a_save; g.save_b = b_save;
-  e = launch_mode<GATEUP>(ma, mb, mb2, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
+  e = pair ? launch_mode<GATEUP2>(ma, mb, mb2, ma, ma, g, max_m_tiles * g.n_tiles_n, s)
+           : launch_mode<GATEUP>(ma, mb, mb2, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
   trace_end(MOE_STAGE_GATEUP, s);
   if (e != cudaSuccess) return e;
   // down: A = h, B = W2 rows (256 per tile)
@@ -744,7 +774,8 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.out_bf16 = out; g.save_a = g.save_b = nullptr;
 
   trace_begin(MOE_STAGE_DOWN, s);
-  e = launch_mode<DOWN>(ma, mb, mb, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
+  e = pair ? launch_mode<DOWN2>(ma, mb, mb, ma, ma, g, max_m_tiles * g.n_tiles_n, s)
+           : launch_mode<DOWN>(ma, mb, mb, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
   trace_end(MOE_STAGE_DOWN, s);
   return e;
 }
