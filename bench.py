@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--no-prepack", action="store_true",
                    help="forward-only workloads: stream the plain weight layout instead of the "
                         "tiles moe_prepack_weights writes once before timing")
+    p.add_argument("--single-cta", action="store_true",
+                   help="expert GEMMs on single-CTA 128-row tiles instead of 256-row tiles on "
+                        "CTA pairs")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -229,7 +232,8 @@ def run_ours(args, rank, world, device):
         big = wl.E * wl.f * wl.d > (1 << 28)
         inp = synth.layer_inputs(wl, device=device, weight_device=device if big else "cpu")
         train = wl.train
-        fwd_flags = 0
+        gemm_flags = B.MOE_SINGLE_CTA_TILES if args.single_cta else 0
+        fwd_flags = gemm_flags
         weights_note = "plain [E, out, in]"
         if (not train and not args.no_prepack and wl.d % 256 == 0 and wl.f % 128 == 0):
             # inference: the weights are laid out once (like loading a model), outside the timing
@@ -238,7 +242,7 @@ def run_ours(args, rank, world, device):
             torch.cuda.synchronize()
             for k, t in zip(("W1", "W3", "W2"), packed):
                 inp[k] = t
-            fwd_flags = B.MOE_WEIGHTS_PREPACKED
+            fwd_flags |= B.MOE_WEIGHTS_PREPACKED
             weights_note = "prepacked tiles (moe_prepack_weights once, before timing)"
         layer = B.Layer(inp["w_gate"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], wl.R, wl.T)
         saved = B.Saved(layer, device, train=train)
@@ -259,7 +263,8 @@ def run_ours(args, rank, world, device):
             B.moe_layer_fwd(layer, xx, y if yout is None else yout, saved, fws, flags=fwd_flags)
             if train:
                 B.moe_layer_bwd(layer, xx, saved, g if gin is None else gin,
-                                dx if dxout is None else dxout, dWg, dW1, dW3, dW2, bws)
+                                dx if dxout is None else dxout, dWg, dW1, dW3, dW2, bws,
+                                flags=gemm_flags)
         host_in = [("x", x)] + ([("g", inp["g"])] if train else [])
         host_out = [("y", y)] + ([("dx", dx)] if train else [])
     if identity:
@@ -271,7 +276,8 @@ def run_ours(args, rank, world, device):
     else:
         B.moe_layer_fwd(layer, x, y, saved, fws, flags=B.MOE_CHECK | fwd_flags)
         if train:
-            B.moe_layer_bwd(layer, x, saved, g, dx, dWg, dW1, dW3, dW2, bws, flags=B.MOE_CHECK)
+            B.moe_layer_bwd(layer, x, saved, g, dx, dWg, dW1, dW3, dW2, bws,
+                            flags=B.MOE_CHECK | gemm_flags)
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         step()
@@ -419,7 +425,9 @@ def run_ours(args, rank, world, device):
                    "parallelism": f"replicas x{world} (no cross-GPU exchange)",
                    "global_batch_tokens": wl.T * world,
                    "l2": "inputs larger than L2 every step (no flush)",
-                   "weights": weights_note},
+                   "weights": weights_note,
+                   "gemm_tiles": None if identity else
+                   ("128-row, one CTA" if args.single_cta else "256-row, CTA pairs")},
         "roofline": roof,
         "summary": summary,
         "stages": stages,

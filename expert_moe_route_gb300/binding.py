@@ -18,6 +18,7 @@ MOE_OK = 0
 MOE_LOGITS_IN = 0x1
 MOE_CHECK = 0x2
 MOE_WEIGHTS_PREPACKED = 0x4
+MOE_SINGLE_CTA_TILES = 0x8
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CUDA"}
 

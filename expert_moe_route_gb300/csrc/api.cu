@@ -279,7 +279,8 @@ moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int
   MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
   cudaError_t e = launch_ffn_fwd(x_perm, offsets, N, d, f, E, W1, W3, W2, a_save, b_save, h, out,
                                  static_cast<uint8_t*>(ws) + kErrBytes, err,
-                                 (flags & MOE_WEIGHTS_PREPACKED) != 0, s);
+                                 (flags & MOE_WEIGHTS_PREPACKED) != 0,
+                                 !(flags & MOE_SINGLE_CTA_TILES), s);
   return finish(e, err, flags, s);
 }
 
@@ -376,7 +377,8 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
                             sv->slot_row, sv->x_perm, dws, err, s));
   }
   MOE_TRY(launch_ffn_fwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
-                         sv->h, sv->o, tws, err, (flags & MOE_WEIGHTS_PREPACKED) != 0, s));
+                         sv->h, sv->o, tws, err, (flags & MOE_WEIGHTS_PREPACKED) != 0,
+                         !(flags & MOE_SINGLE_CTA_TILES), s));
   cudaError_t e;
   {
     Stage st_(s, MOE_STAGE_COMBINE);
@@ -457,7 +459,8 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
                              s));
   }
   MOE_TRY(launch_ffn_bwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
-                         sv->h, dO, dab, dxp, dW1, dW3, dW2, tws, err, s));
+                         sv->h, dO, dab, dxp, dW1, dW3, dW2, tws, err,
+                         !(flags & MOE_SINGLE_CTA_TILES), s));
   {
     Stage st_(s, MOE_STAGE_BWD_DWG);
     MOE_TRY(launch_dwg(sv->x_perm, sv->offsets, dsel_row, d, E, dW_gate, dwg_ws, s));

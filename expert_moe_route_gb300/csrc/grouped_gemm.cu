@@ -44,11 +44,12 @@ constexpr uint32_t TMEM_COLS = 512;
 enum Mode : int { GATEUP = 0, DOWN = 1, DH = 2, DX = 3, WG2 = 4, WG13 = 5, GATE = 6,
                   GATEUP2 = 7, DOWN2 = 8 };
 
-template <int M> struct Traits {
+template <int M, bool C2 = false> struct Traits {
   static constexpr bool a_mn = (M == WG2 || M == WG13);
   static constexpr bool b_mn = (M == DH || M == DX || M == WG2 || M == WG13);
   static constexpr bool wgrad = (M == WG2 || M == WG13);
-  static constexpr int epi_bytes = wgrad ? EPI_BYTES : 0;
+  // one 32-row x 128-B staging box per epilogue warp (all modes but the gate)
+  static constexpr int epi_bytes = (M == GATE) ? 0 : EPI_BYTES;
   // GATE: 128-column tiles with four partial accumulators (K-blocks rotate over
   // them; the epilogue adds them in IEEE fp32), so each accumulator takes a
   // quarter of the tensor core's accumulation steps.
@@ -64,17 +65,25 @@ template <int M> struct Traits {
   static constexpr bool is_gateup = (M == GATEUP || M == GATEUP2);
   static constexpr bool is_down = (M == DOWN || M == DOWN2);
   static constexpr bool single_acc = partials || pair;
-  static constexpr int stages = pair ? 3 : STAGES;
+  // C2: the CTA pair computes 256-row tiles; each CTA stages 128 rows of A
+  // and half of B (128 of the 256 columns), so a stage is 32 KB and six fit.
+  static constexpr int tile_m = C2 ? 2 * BM : BM;
+  static constexpr int stages = pair ? 3 : (C2 ? 6 : STAGES);
   static constexpr int a_bytes = pair ? 2 * A_BYTES : A_BYTES;
-  static constexpr int stage_bytes = a_bytes + B_BYTES;
-  static constexpr uint32_t stage_tx = partials ? A_BYTES + 128 * BK * 2 : (uint32_t)stage_bytes;
+  static constexpr int b_bytes = C2 ? B_BYTES / 2 : B_BYTES;
+  static constexpr int stage_bytes = a_bytes + b_bytes;
+  // bytes the full barrier expects per stage (rank 0's barrier counts both CTAs' loads)
+  static constexpr uint32_t stage_tx =
+      partials ? A_BYTES + 128 * BK * 2 : (uint32_t)(C2 ? 2 * stage_bytes : stage_bytes);
   // stages | epilogue staging | control block, plus slack for 1024-B alignment
   static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + CTL_BYTES + 1024;
 };
 
+constexpr int MAX_STAGES = 6;
+
 struct alignas(8) SharedCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -136,12 +145,15 @@ __device__ __forceinline__ void store_bf16x16(uint16_t* dst, const float* v, int
   if (ncols_left >= 16) reinterpret_cast<uint4*>(dst)[1] = pack8(v + 8);
 }
 
-template <int MODE>
+template <int MODE, bool C2>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
-                    const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ GemmArgs g) {
-  using Tr = Traits<MODE>;
+                    const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ CUtensorMap tmC3,
+                    const __grid_constant__ GemmArgs g) {
+  using Tr = Traits<MODE, C2>;
+  static_assert(Tr::stages <= MAX_STAGES, "stages");
+  static_assert(!C2 || (!Tr::pair && !Tr::partials), "CTA pairs: 256-row modes only");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tile_base = (raw_addr + 1023u) & ~1023u;       // 1024-B aligned stages
@@ -152,6 +164,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // C2: rank 0 of the pair issues the MMAs; both CTAs walk the same items.
+  const uint32_t rank = C2 ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
+  const int first_item = C2 ? (int)cluster_index() : (int)blockIdx.x;
+  const int item_step = C2 ? (int)cluster_count() : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Tr::stages; ++s) {
@@ -160,7 +177,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
-      mbar_init(smem_u32(&ctl->tempty[a]), EPI_WARPS);
+      mbar_init(smem_u32(&ctl->tempty[a]), C2 ? 2 * EPI_WARPS : EPI_WARPS);
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     ctl->abort = 0;
@@ -168,15 +185,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (Tr::is_gateup || MODE == DX) tma_prefetch_desc(&tmB2);
-    if (Tr::wgrad) tma_prefetch_desc(&tmC);
-    if (MODE == WG13) tma_prefetch_desc(&tmC2);
+    if (MODE != GATE) tma_prefetch_desc(&tmC);
+    if (MODE == WG13 || Tr::is_gateup) tma_prefetch_desc(&tmC2);
+    if (Tr::is_gateup) tma_prefetch_desc(&tmC3);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    if (C2) {
+      tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (C2) cluster_sync_all();   // both CTAs' barriers and tensor memory are ready
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   const int total = total_items(g, MODE);
@@ -186,7 +210,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (lane == 0) {
       uint32_t it_count = 0;   // k-blocks issued so far (all items)
       bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      // C2: this CTA's loads land in its own shared memory and signal rank 0's barrier
+      auto ld2 = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y) {
+        if (C2) tma_load_2d_pair(dst, m, bar, x, y);
+        else tma_load_2d(dst, m, bar, x, y);
+      };
+      auto ld4 = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y, int z, int w) {
+        if (C2) tma_load_4d_pair(dst, m, bar, x, y, z, w);
+        else tma_load_4d(dst, m, bar, x, y, z, w);
+      };
+      const int rrow = (int)rank * BM;        // this CTA's rows of a 256-row tile
+      const int rcol = (int)rank * (BN / 2);  // this CTA's half of the B columns
+      for (int item = first_item; item < total && ok; item += item_step) {
         Item it;
         decode_item(g, MODE, item, it);
         for (int kb = 0; kb < it.kblocks; ++kb, ++it_count) {
@@ -196,83 +231,100 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             ok = false;
             break;
           }
-          const uint32_t bar = smem_u32(&ctl->full[s]);
+          const uint32_t bar_local = smem_u32(&ctl->full[s]);
+          const uint32_t bar = C2 ? mapa_shared(bar_local, 0) : bar_local;
           const uint32_t sa = tile_base + s * Tr::stage_bytes;
           const uint32_t sb = sa + Tr::a_bytes;
-          mbar_arrive_expect_tx(bar, Tr::stage_tx);
+          if (leader) mbar_arrive_expect_tx(bar_local, Tr::stage_tx);
           const int kx = kb * BK;
           if (Tr::pair) tma_load_2d(sa + A_BYTES, &tmA, bar, kx, it.row0 + BM);   // rows 128-255
           if (Tr::is_gateup) {
-            tma_load_2d(sa, &tmA, bar, kx, it.row0);
+            ld2(sa, &tmA, bar, kx, it.row0 + rrow);
+            // B = [W1 rows; W3 rows] of the column tile (C2: rank 0 W1, rank 1 W3)
             if (g.prepacked) {   // one contiguous 16 KB tile per box
               const int rt = it.e * (g.f / 128) + it.nt;
-              tma_load_4d(sb, &tmB, bar, 0, 0, kb, rt);
-              tma_load_4d(sb + B_BYTES / 2, &tmB2, bar, 0, 0, kb, rt);
+              if (C2) {
+                ld4(sb, rank ? &tmB2 : &tmB, bar, 0, 0, kb, rt);
+              } else {
+                tma_load_4d(sb, &tmB, bar, 0, 0, kb, rt);
+                tma_load_4d(sb + B_BYTES / 2, &tmB2, bar, 0, 0, kb, rt);
+              }
             } else {
               const int brow = it.e * g.f + it.nt * 128;
-              tma_load_2d(sb, &tmB, bar, kx, brow);
-              tma_load_2d(sb + B_BYTES / 2, &tmB2, bar, kx, brow);
+              if (C2) {
+                ld2(sb, rank ? &tmB2 : &tmB, bar, kx, brow);
+              } else {
+                tma_load_2d(sb, &tmB, bar, kx, brow);
+                tma_load_2d(sb + B_BYTES / 2, &tmB2, bar, kx, brow);
+              }
             }
           } else if (MODE == GATE) {
             // A repeats x for the hi, mid and lo thirds of K
             tma_load_2d(sa, &tmA, bar, kx % g.d, it.row0);
             tma_load_2d(sb, &tmB, bar, kx, it.nt * Tr::bn);
           } else if (Tr::is_down) {
-            tma_load_2d(sa, &tmA, bar, kx, it.row0);
-            if (g.prepacked) {   // one contiguous 32 KB tile
+            ld2(sa, &tmA, bar, kx, it.row0 + rrow);
+            if (g.prepacked) {   // one contiguous 32 KB tile (C2: each CTA its 128 rows)
               const int rt = it.e * (g.d / BN) + it.nt;
-              tma_load_4d(sb, &tmB, bar, 0, 0, kb, rt);
+              ld4(sb, &tmB, bar, 0, rcol, kb, rt);
+            } else {
+              ld2(sb, &tmB, bar, kx, it.e * g.d + it.nt * BN + rcol);
             }
-            else
-              tma_load_2d(sb, &tmB, bar, kx, it.e * g.d + it.nt * BN);
           } else if (MODE == DH) {
-            tma_load_2d(sa, &tmA, bar, kx, it.row0);
+            ld2(sa, &tmA, bar, kx, it.row0 + rrow);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(sb + j * ATOM_BYTES, &tmB, bar, it.nt * BN + j * 64, it.e * g.d + kx);
+            for (int j = 0; j < Tr::b_bytes / ATOM_BYTES; ++j)
+              ld2(sb + j * ATOM_BYTES, &tmB, bar, it.nt * BN + rcol + j * 64, it.e * g.d + kx);
           } else if (MODE == DX) {
-            tma_load_2d(sa, &tmA, bar, kx, it.row0);
+            ld2(sa, &tmA, bar, kx, it.row0 + rrow);
             const bool first = kx < g.f;
             const int krow = it.e * g.f + (first ? kx : kx - g.f);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(sb + j * ATOM_BYTES, first ? &tmB : &tmB2, bar, it.nt * BN + j * 64, krow);
+            for (int j = 0; j < Tr::b_bytes / ATOM_BYTES; ++j)
+              ld2(sb + j * ATOM_BYTES, first ? &tmB : &tmB2, bar, it.nt * BN + rcol + j * 64, krow);
           } else {  // WG2 / WG13: both operands MN-major, K = rows of expert e
             const int krow = it.krow0 + kx;
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-              tma_load_2d(sa + j * ATOM_BYTES, &tmA, bar, it.mt * BM + j * 64, krow);
+              ld2(sa + j * ATOM_BYTES, &tmA, bar, it.mt * Tr::tile_m + rrow + j * 64, krow);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(sb + j * ATOM_BYTES, &tmB, bar, it.nt * BN + j * 64, krow);
+            for (int j = 0; j < Tr::b_bytes / ATOM_BYTES; ++j)
+              ld2(sb + j * ATOM_BYTES, &tmB, bar, it.nt * BN + rcol + j * 64, krow);
           }
         }
       }
-      if (!ok) {
+      if (!ok && C2) {
+        // The pair's loads signal rank 0's barriers, which this CTA cannot
+        // observe: give any load still in flight time to land (tens of us).
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 200000ull) {
+        }
+      } else if (!ok) {
         // drain: the last (up to STAGES) issued loads must land before the CTA exits
         const uint32_t n = it_count < (uint32_t)Tr::stages ? it_count : (uint32_t)Tr::stages;
-        int dummy = 0;
         for (uint32_t q = 0; q < n; ++q) {
           const uint32_t c = it_count - 1 - q;
           volatile int never = 0;
           mbar_wait_bounded(smem_u32(&ctl->full[c % Tr::stages]), (c / Tr::stages) & 1u, &never,
-                            &dummy);
+                            nullptr);
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(BM, Tr::bn, Tr::a_mn, Tr::b_mn);
+    constexpr uint32_t idesc = idesc_bf16(Tr::tile_m, Tr::bn, Tr::a_mn, Tr::b_mn);
     uint32_t it_count = 0;
     int j = 0;
     bool ok = true;
     bool issued_any = false;
-    for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++j) {
+    for (int item = first_item; item < total && ok; item += item_step, ++j) {
       Item it;
       decode_item(g, MODE, item, it);
       const int acc = Tr::single_acc ? 0 : (j & 1);
       const uint32_t aph = Tr::single_acc ? (j & 1u) : ((j >> 1) & 1u);
-      ok = mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, g.err);
+      // C2: both CTAs' epilogues arrive on this barrier
+      ok = C2 ? mbar_wait_bounded_cluster(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, g.err)
+              : mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, g.err);
       ok = __all_sync(kFull, ok);
       if (!ok) break;
       tc_fence_after();
@@ -295,16 +347,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             kk_end = ceil_div(rem, 16);
             const int z1 = kk_end * 16;
             if (rem < z1) {
-              // rows rem .. z1-1 of each of the stage's six 64-element blocks:
-              // (z1 - rem) rows x 8 chunks of 16 B, lane-strided within a block
+              // rows rem .. z1-1 of each of the stage's 64-element blocks (six;
+              // C2: four in each CTA of the pair): (z1 - rem) rows x 8 chunks of
+              // 16 B, lane-strided within a block
+              constexpr int atoms = Tr::stage_bytes / ATOM_BYTES;
               const int per_atom = (z1 - rem) * 8;
-              uint8_t* base = tile_ptr + s * Tr::stage_bytes + rem * 128;
+              const uint32_t base = tile_base + s * Tr::stage_bytes + rem * 128;
+              uint8_t* base_ptr = tile_ptr + s * Tr::stage_bytes + rem * 128;
 #pragma unroll
-              for (int atom = 0; atom < 6; ++atom)
-                for (int w = lane; w < per_atom; w += 32)
-                  *reinterpret_cast<uint4*>(base + atom * ATOM_BYTES + (w >> 3) * 128 + (w & 7) * 16) =
-                      make_uint4(0, 0, 0, 0);
+              for (int atom = 0; atom < atoms; ++atom)
+                for (int w = lane; w < per_atom; w += 32) {
+                  const uint32_t off = atom * ATOM_BYTES + (w >> 3) * 128 + (w & 7) * 16;
+                  *reinterpret_cast<uint4*>(base_ptr + off) = make_uint4(0, 0, 0, 0);
+                  if (C2) st_shared_cluster_v4(mapa_shared(base + off, 1), make_uint4(0, 0, 0, 0));
+                }
               fence_proxy_async_smem();
+              if (C2) fence_proxy_async_cluster();
             }
           }
           __syncwarp();
@@ -320,38 +378,69 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                          : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, ATOM_BYTES, 1024)
                                          : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
+            if (C2) tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
+            else tc_mma_bf16(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
             if (Tr::pair && it.row_end - it.row0 > BM)   // rows 128-255 share the B stage
               tc_mma_bf16(tmem_base + BN, smem_desc_sw128(sa + A_BYTES + kk * 32, 16, 1024), bd,
                           idesc, (!first || kk > 0) ? 1u : 0u);
           }
-          tc_commit(smem_u32(&ctl->empty[s]));   // frees the stage when these MMAs finish
+          // frees the stage (C2: in both CTAs) when these MMAs finish
+          if (C2) tc_commit_pair(smem_u32(&ctl->empty[s]), 3);
+          else tc_commit(smem_u32(&ctl->empty[s]));
           issued_any = true;
         }
         __syncwarp();
       }
       if (!ok) break;
       if (lane == 0) {
-        if (it.kblocks > 0) tc_commit(smem_u32(&ctl->tfull[acc]));
-        else mbar_arrive(smem_u32(&ctl->tfull[acc]));
+        const uint32_t tf = smem_u32(&ctl->tfull[acc]);
+        if (it.kblocks > 0) {
+          if (C2) tc_commit_pair(tf, 3);
+          else tc_commit(tf);
+        } else {
+          mbar_arrive(tf);
+          if (C2) mbar_arrive_cluster(mapa_shared(tf, 1));
+        }
       }
       __syncwarp();
     }
     // drain outstanding MMAs before TMEM is released
     if (lane == 0 && issued_any) {
-      tc_commit(smem_u32(&ctl->mma_done));
+      if (C2) tc_commit_pair(smem_u32(&ctl->mma_done), 1);
+      else tc_commit(smem_u32(&ctl->mma_done));
       volatile int never = 0;
-      int dummy = 0;
-      mbar_wait_bounded(smem_u32(&ctl->mma_done), 0, &never, &dummy);
+      mbar_wait_bounded(smem_u32(&ctl->mma_done), 0, &never, nullptr);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
     const int r_local = q * 32 + lane;   // accumulator row owned by this thread
     const int half = (warp - 2) >> 2;    // which half of the tile's columns this warp drains
+    const int rrow = (int)rank * BM;     // C2: this CTA's rows of the 256-row tile
+    // This warp's staging box: 32 rows (its TMEM lanes) x 128 B, 128-B swizzled
+    // (16-B chunk j of row r at r * 128 + (j ^ (r & 7)) * 16), written by the
+    // warp and sent to global memory by one bulk tensor store.
+    const uint32_t sbox = tile_base + Tr::stages * Tr::stage_bytes + (warp - 2) * EPI_WARP_BYTES;
+    uint8_t* sbox_row = tile_ptr + Tr::stages * Tr::stage_bytes + (warp - 2) * EPI_WARP_BYTES +
+                        lane * 128;
+    auto stage_begin = [&]() {   // the box is free once its previous store has read it
+      if (lane == 0) bulk_wait_read_0();
+      __syncwarp();
+    };
+    auto stage_put = [&](int j, uint4 v) {   // 16-B chunk j (8 bf16) of this lane's row
+      *reinterpret_cast<uint4*>(sbox_row + ((j ^ (lane & 7)) * 16)) = v;
+    };
+    auto stage_end = [&](const CUtensorMap* m, int x, int y) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(m, sbox, x, y);
+        bulk_commit();
+      }
+    };
     int j = 0;
-    for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
+    for (int item = first_item; item < total; item += item_step, ++j) {
       Item it;
       decode_item(g, MODE, item, it);
       const int acc = Tr::single_acc ? 0 : (j & 1);
@@ -363,10 +452,42 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       for (int hh = 0; hh < (Tr::pair ? 2 : 1); ++hh) {   // row halves of a 256-row item
       if (hh == 1 && it.row_end - it.row0 <= BM) break;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + hh * BN;
-      if (Tr::is_gateup) {
-        const int row = it.row0 + hh * BM + r_local;
+      const int grow0 = it.row0 + rrow + hh * BM + q * 32;   // this warp's first row
+      // Whole 32-row groups of the expert go out as staged boxes; the group
+      // holding the expert's last row (the next expert's rows follow it) is
+      // written row by row.
+      const bool boxed = grow0 + 32 <= it.row_end;
+      if (Tr::is_gateup && boxed) {
+        // h, then the saved a and b: 64 columns of this warp's 32 rows each
+        const int c0 = half * 64;
+        const int col0 = it.nt * 128 + c0;
+        const int nout = g.save_a ? 3 : 1;
+        for (int o = 0; o < nout && col0 < g.f; ++o) {
+          stage_begin();
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) {
+            float a[16], b[16];
+            if (o != 2) tmem_ld16(t_row + c0 + 16 * k, a);
+            if (o != 1) tmem_ld16(t_row + 128 + c0 + 16 * k, b);
+            tmem_ld_wait();
+            if (o == 0) {
+#pragma unroll
+              for (int u = 0; u < 16; ++u) a[u] = silu_f(a[u]) * b[u];
+            }
+            if (o == 2) {
+              stage_put(2 * k, pack8(b));
+              stage_put(2 * k + 1, pack8(b + 8));
+            } else {
+              stage_put(2 * k, pack8(a));
+              stage_put(2 * k + 1, pack8(a + 8));
+            }
+          }
+          stage_end(o == 0 ? &tmC : (o == 1 ? &tmC2 : &tmC3), col0, grow0);
+        }
+      } else if (Tr::is_gateup) {
+        const int row = it.row0 + rrow + hh * BM + r_local;
         const bool valid = row < it.row_end;
-        for (int c = half * 64; c < half * 64 + 64; c += 16) {
+        for (int c = half * 64; c < half * 64 + 64 && grow0 < it.row_end; c += 16) {
           float a[16], b[16];
           tmem_ld16(t_row + c, a);
           tmem_ld16(t_row + 128 + c, b);
@@ -406,10 +527,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int u = 0; u < n; ++u) dst[u] = v[u] + (g.bias ? g.bias[col + u] : 0.f);
           }
         }
+      } else if ((Tr::is_down || MODE == DX) && boxed) {
+        for (int bx = 0; bx < 2; ++bx) {   // two boxes of 64 columns
+          const int c0 = half * (BN / 2) + bx * 64;
+          const int col0 = it.nt * BN + c0;
+          if (col0 >= g.d) break;
+          float v[64];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tmem_ld16(t_row + c0 + 16 * k, v + 16 * k);
+          tmem_ld_wait();
+          stage_begin();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) stage_put(k, pack8(v + 8 * k));
+          stage_end(&tmC, col0, grow0);
+        }
       } else if (Tr::is_down || MODE == DX) {
-        const int row = it.row0 + hh * BM + r_local;
+        const int row = it.row0 + rrow + hh * BM + r_local;
         const bool valid = row < it.row_end;
-        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 16) {
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2) && grow0 < it.row_end; c += 16) {
           float v[16];
           tmem_ld16(t_row + c, v);
           tmem_ld_wait();
@@ -417,7 +552,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           if (valid && col < g.d) store_bf16x16(g.out_bf16 + (size_t)row * g.d + col, v, g.d - col);
         }
       } else if (MODE == DH) {
-        const int row = it.row0 + r_local;
+        const int row = it.row0 + rrow + r_local;
         const bool valid = row < it.row_end;
         const uint16_t* pa = g.in_a + (size_t)row * g.f;
         const uint16_t* pb = g.in_b + (size_t)row * g.f;
@@ -436,8 +571,50 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
         };
         uint4 na[2], nb[2];
-        const int c0 = half * (BN / 2), c1 = c0 + BN / 2;
-        load_ab(c0, na, nb);  // the next chunk's loads are in flight while this one computes
+        auto dadb = [&](const float* dh, const uint4* ca, const uint4* cb, float* da, float* db) {
+          float a[16], b[16];
+          unpack8(ca[0], a);
+          unpack8(ca[1], a + 8);
+          unpack8(cb[0], b);
+          unpack8(cb[1], b + 8);
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const float sg = 1.f / (1.f + expf(-a[u]));
+            da[u] = dh[u] * b[u] * (sg * (1.f + a[u] * (1.f - sg)));
+            db[u] = dh[u] * a[u] * sg;
+          }
+        };
+        if (boxed) {
+          // f % 64 == 0: a 64-column box lies wholly inside da (or db)
+          for (int bx = 0; bx < 2; ++bx) {
+            const int c0 = half * (BN / 2) + bx * 64;
+            const int col0 = it.nt * BN + c0;
+            if (col0 >= g.f) break;
+            uint4 dbp[8];   // this box's db, packed, while da's box is stored
+            load_ab(c0, na, nb);
+            stage_begin();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint4 ca[2] = {na[0], na[1]}, cb[2] = {nb[0], nb[1]};
+              if (k < 3) load_ab(c0 + 16 * (k + 1), na, nb);
+              float dh[16], da[16], db[16];
+              tmem_ld16(t_row + c0 + 16 * k, dh);
+              tmem_ld_wait();
+              dadb(dh, ca, cb, da, db);
+              stage_put(2 * k, pack8(da));
+              stage_put(2 * k + 1, pack8(da + 8));
+              dbp[2 * k] = pack8(db);
+              dbp[2 * k + 1] = pack8(db + 8);
+            }
+            stage_end(&tmC, col0, grow0);
+            stage_begin();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) stage_put(k, dbp[k]);
+            stage_end(&tmC, g.f + col0, grow0);
+          }
+        }
+        const int c0 = half * (BN / 2), c1 = boxed ? c0 : c0 + BN / 2;
+        if (c0 < c1) load_ab(c0, na, nb);  // the next chunk's loads are in flight while this one computes
         for (int c = c0; c < c1; c += 16) {
           uint4 ca[2] = {na[0], na[1]}, cb[2] = {nb[0], nb[1]};
           if (c + 16 < c1) load_ab(c + 16, na, nb);
@@ -446,17 +623,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           tmem_ld_wait();
           const int col = it.nt * BN + c;
           if (valid && col < g.f) {
-            float a[16], b[16], da[16], db[16];
-            unpack8(ca[0], a);
-            unpack8(ca[1], a + 8);
-            unpack8(cb[0], b);
-            unpack8(cb[1], b + 8);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const float sg = 1.f / (1.f + expf(-a[u]));
-              da[u] = dh[u] * b[u] * (sg * (1.f + a[u] * (1.f - sg)));
-              db[u] = dh[u] * a[u] * sg;
-            }
+            float da[16], db[16];
+            dadb(dh, ca, cb, da, db);
             const size_t o2 = (size_t)row * (2 * g.f) + col;
             store_bf16x16(g.out_bf16 + o2, da, g.f - col);
             store_bf16x16(g.out_bf16 + o2 + g.f, db, g.f - col);
@@ -466,7 +634,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // This warp owns output rows m0 .. m0+31 of expert e and half of the
         // columns.  Each 32-column chunk goes TMEM -> registers -> a
         // 128-B-swizzled 32x32 fp32 box in shared memory -> one bulk tensor store.
-        const int m0 = it.mt * BM + q * 32;
+        const int m0 = it.mt * Tr::tile_m + rrow + q * 32;
         const int mrows = (MODE == WG2) ? g.d : 2 * g.f;
         const int ncols = (MODE == WG2) ? g.f : g.d;
         const CUtensorMap* map = &tmC;
@@ -509,9 +677,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }  // row halves
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+      if (lane == 0) {
+        const uint32_t te = smem_u32(&ctl->tempty[acc]);
+        if (C2 && !leader) mbar_arrive_cluster(mapa_shared(te, 0));
+        else mbar_arrive(te);
+      }
     }
-    if (Tr::wgrad) {
+    if (MODE != GATE) {
       if (lane == 0) bulk_wait_all();   // stores done before the CTA's shared memory goes away
       __syncwarp();
     }
@@ -519,9 +691,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
   tc_fence_before();
   __syncthreads();
+  if (C2) cluster_sync_all();   // the pair's MMAs, loads and remote arrivals are over
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (C2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -631,14 +805,15 @@ bool make_map_f32_3d(CUtensorMap* m, void* base, long long E, long long rows, lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Prepacked weight tiles [tiles][kb][rows][64] viewed 4-D: {64, rows, kblocks, tiles}.
+// Prepacked weight tiles [tiles][kb][rows][64] viewed 4-D: {64, rows, kblocks, tiles};
+// a box is box_rows rows of one tile's k-block (all of them by default).
 bool make_map_tiles(CUtensorMap* m, const void* base, long long tiles, long long kblocks,
-                    int rows) {
+                    int rows, int box_rows = 0) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)kblocks, (cuuint64_t)tiles};
   cuuint64_t strides[3] = {128, (cuuint64_t)rows * 128, (cuuint64_t)kblocks * rows * 128};
-  cuuint32_t box[4] = {64u, (cuuint32_t)rows, 1u, 1u};
+  cuuint32_t box[4] = {64u, (cuuint32_t)(box_rows > 0 ? box_rows : rows), 1u, 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -654,25 +829,51 @@ int sm_count() {
   return n[dev] > 0 ? n[dev] : 148;
 }
 
-template <int MODE>
+template <int MODE, bool C2 = false>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
-                        const CUtensorMap& c, const CUtensorMap& c2, const GemmArgs& g,
-                        long long max_items, cudaStream_t s) {
-  constexpr int SMEM_BYTES = Traits<MODE>::smem_bytes;
+                        const CUtensorMap& c, const CUtensorMap& c2, const CUtensorMap& c3,
+                        const GemmArgs& g, long long max_items, cudaStream_t s) {
+  constexpr int SMEM_BYTES = Traits<MODE, C2>::smem_bytes;
+  auto kernel = grouped_gemm_kernel<MODE, C2>;
   static bool attr_done[64] = {false};
+  static int pair_slots[64] = {0};   // C2: clusters of two that fit on the GPU at once
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  if (C2) {
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (!attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    if (C2) {
+      cfg.gridDim = dim3(2 * (sm_count() / 2));
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      pair_slots[dev] = n;
+    }
     attr_done[dev] = true;
   }
   if (max_items <= 0) return cudaSuccess;
-  const int grid = (int)std::min<long long>(sm_count(), max_items);
-  grouped_gemm_kernel<MODE><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, b2, c, c2, g);
+  const long long ctas = C2 ? 2 * std::min<long long>(pair_slots[dev], max_items)
+                            : std::min<long long>(sm_count(), max_items);
+  cfg.gridDim = dim3((unsigned)ctas);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, b, b2, c, c2, c3, g);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 }  // namespace
 
@@ -697,7 +898,7 @@ cudaError_t launch_gate_tc(const uint16_t* x, const float* wg, const float* bias
   g.out_f32 = logits;
   g.bias = bias;
   g.err = err;
-  return launch_mode<GATE>(ma, mb, mb, ma, ma, g, (long long)g.n_tiles_m * g.n_tiles_n, s);
+  return launch_mode<GATE>(ma, mb, mb, ma, ma, ma, g, (long long)g.n_tiles_m * g.n_tiles_n, s);
 }
 
 bool prepack_supported(int d, int f) { return d % BN == 0 && f % 128 == 0; }
@@ -730,13 +931,15 @@ cudaError_t launch_build_tiles(const int32_t* offsets, int E, void* ws, cudaStre
 cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
-                           void* tiles_ws, int* err, bool prepacked, cudaStream_t s) {
+                           void* tiles_ws, int* err, bool prepacked, bool cta_pairs,
+                           cudaStream_t s) {
   if (N == 0) return cudaSuccess;
-  // Few rows per expert (on average at most two 128-row tiles): the layer
-  // streams weights, so pair an expert's 128-row tiles in one CTA to share each
-  // weight tile (GATEUP2 / DOWN2); otherwise overlap epilogue and main loop.
-  const bool pair = (long long)N <= 2LL * BM * E;
-  const int tile_rows = pair ? 2 * BM : BM;
+  // cta_pairs: 256-row tiles on CTA pairs (tcgen05 .cta_group::2).  Otherwise
+  // single-CTA tiles; with few rows per expert (on average at most two 128-row
+  // tiles) the layer streams weights, so one CTA takes both 128-row halves of
+  // a 256-row block to share each weight tile (GATEUP2 / DOWN2).
+  const bool pair = !cta_pairs && (long long)N <= 2LL * BM * E;
+  const int tile_rows = (pair || cta_pairs) ? 2 * BM : BM;
   trace_begin(MOE_STAGE_GATEUP, s);
   cudaError_t e = launch_build_tiles(offsets, E, tiles_ws, s, tile_rows);
   if (e != cudaSuccess) return e;
@@ -760,22 +963,35 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.kblocks = ceil_div(d, BK);
   g.n_tiles_n = ceil_div(f, 128);
   g.out_bf16 = h; g.save_a = a_save; g.save_b = b_save;
-  e = pair ? launch_mode<GATEUP2>(ma, mb, mb2, ma, ma, g, max_m_tiles * g.n_tiles_n, s)
-           : launch_mode<GATEUP>(ma, mb, mb2, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
+  // epilogue outputs, stored in 32-row x 64-column boxes
+  CUtensorMap mh, msa, msb;
+  if (!make_map(&mh, h, N, f, 32)) return cudaErrorInvalidValue;
+  msa = msb = mh;
+  if (a_save && !(make_map(&msa, a_save, N, f, 32) && make_map(&msb, b_save, N, f, 32)))
+    return cudaErrorInvalidValue;
+  const long long items = max_m_tiles * g.n_tiles_n;
+  e = cta_pairs ? launch_mode<GATEUP, true>(ma, mb, mb2, mh, msa, msb, g, items, s)
+      : pair    ? launch_mode<GATEUP2>(ma, mb, mb2, mh, msa, msb, g, items, s)
+                : launch_mode<GATEUP>(ma, mb, mb2, mh, msa, msb, g, items, s);
   trace_end(MOE_STAGE_GATEUP, s);
   if (e != cudaSuccess) return e;
-  // down: A = h, B = W2 rows (256 per tile)
+  // down: A = h, B = W2 rows (256 per tile; each CTA of a pair loads 128)
+  const int w2_box = cta_pairs ? BN / 2 : BN;
   if (!make_map(&ma, h, N, f, BM)) return cudaErrorInvalidValue;
-  if (prepacked ? !make_map_tiles(&mb, W2, (long long)E * d / BN, f / 64, BN)
-                : !make_map(&mb, W2, (long long)E * d, f, BN))
+  if (prepacked ? !make_map_tiles(&mb, W2, (long long)E * d / BN, f / 64, BN, w2_box)
+                : !make_map(&mb, W2, (long long)E * d, f, w2_box))
     return cudaErrorInvalidValue;
   g.kblocks = ceil_div(f, BK);
   g.n_tiles_n = ceil_div(d, BN);
   g.out_bf16 = out; g.save_a = g.save_b = nullptr;
+  CUtensorMap mo;
+  if (!make_map(&mo, out, N, d, 32)) return cudaErrorInvalidValue;
 
   trace_begin(MOE_STAGE_DOWN, s);
-  e = pair ? launch_mode<DOWN2>(ma, mb, mb, ma, ma, g, max_m_tiles * g.n_tiles_n, s)
-           : launch_mode<DOWN>(ma, mb, mb, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
+  const long long items_down = max_m_tiles * g.n_tiles_n;
+  e = cta_pairs ? launch_mode<DOWN, true>(ma, mb, mb, mo, mo, mo, g, items_down, s)
+      : pair    ? launch_mode<DOWN2>(ma, mb, mb, mo, mo, mo, g, items_down, s)
+                : launch_mode<DOWN>(ma, mb, mb, mo, mo, mo, g, items_down, s);
   trace_end(MOE_STAGE_DOWN, s);
   return e;
 }
@@ -785,8 +1001,10 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            const uint16_t* a_s, const uint16_t* b_s, const uint16_t* h,
                            const uint16_t* dO, uint16_t* dab, uint16_t* dx_perm, float* dW1,
-                           float* dW3, float* dW2, void* tiles_ws, int* err, cudaStream_t s) {
+                           float* dW3, float* dW2, void* tiles_ws, int* err, bool cta_pairs,
+                           cudaStream_t s) {
   cudaError_t e;
+  const int tile_m = cta_pairs ? 2 * BM : BM;   // rows per M tile (pairs: 256)
   GemmArgs g{};
   g.E = E; g.N = N; g.d = d; g.f = f;
   g.offsets = offsets;
@@ -796,16 +1014,19 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
   CUtensorMap ma, mb, mb2;
   if (N > 0) {
     trace_begin(MOE_STAGE_BWD_DH, s);
-    e = launch_build_tiles(offsets, E, tiles_ws, s);
+    e = launch_build_tiles(offsets, E, tiles_ws, s, tile_m);
     if (e != cudaSuccess) return e;
-    const long long max_m_tiles = ceil_div(N, BM) + E;
+    const long long max_m_tiles = ceil_div(N, tile_m) + E;
     // dh = do W2[e] (B MN-major: W2 viewed [E*d, f]); epilogue -> dab = [da | db]
     if (!make_map(&ma, dO, N, d, BM) || !make_map(&mb, W2, (long long)E * d, f, 64))
       return cudaErrorInvalidValue;
     g.kblocks = d / BK;
     g.n_tiles_n = ceil_div(f, BN);
     g.out_bf16 = dab; g.in_a = a_s; g.in_b = b_s;
-    e = launch_mode<DH>(ma, mb, mb, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
+    CUtensorMap mo;
+    if (!make_map(&mo, dab, N, 2LL * f, 32)) return cudaErrorInvalidValue;
+    e = cta_pairs ? launch_mode<DH, true>(ma, mb, mb, mo, mo, mo, g, max_m_tiles * g.n_tiles_n, s)
+                  : launch_mode<DH>(ma, mb, mb, mo, mo, mo, g, max_m_tiles * g.n_tiles_n, s);
     trace_end(MOE_STAGE_BWD_DH, s);
     if (e != cudaSuccess) return e;
     // dx_perm = [da | db] [W1[e]; W3[e]] (B MN-major: W1, W3 viewed [E*f, d])
@@ -815,33 +1036,39 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
     g.kblocks = 2 * f / BK;
     g.n_tiles_n = ceil_div(d, BN);
     g.out_bf16 = dx_perm;
+    if (!make_map(&mo, dx_perm, N, d, 32)) return cudaErrorInvalidValue;
     trace_begin(MOE_STAGE_BWD_DX, s);
-    e = launch_mode<DX>(ma, mb, mb2, ma, ma, g, max_m_tiles * g.n_tiles_n, s);
+    e = cta_pairs ? launch_mode<DX, true>(ma, mb, mb2, mo, mo, mo, g, max_m_tiles * g.n_tiles_n, s)
+                  : launch_mode<DX>(ma, mb, mb2, mo, mo, mo, g, max_m_tiles * g.n_tiles_n, s);
     trace_end(MOE_STAGE_BWD_DX, s);
     if (e != cudaSuccess) return e;
   }
   // dW2[e] = do^T h: A = do [N, d] MN-major, B = h [N, f] MN-major
   const long long rows = N > 0 ? N : 1;
   if (!make_map(&ma, dO, rows, d, 64) || !make_map(&mb, h, rows, f, 64)) return cudaErrorInvalidValue;
-  g.n_tiles_m = ceil_div(d, BM);
+  g.n_tiles_m = ceil_div(d, tile_m);
   g.n_tiles_n = ceil_div(f, BN);
   g.out_f32 = dW2;
   CUtensorMap mc, mc2;
   if (!make_map_f32_3d(&mc, dW2, E, d, f)) return cudaErrorInvalidValue;
   trace_begin(MOE_STAGE_BWD_WG2, s);
-  e = launch_mode<WG2>(ma, mb, mb, mc, mc, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
+  const long long wg2_items = (long long)E * g.n_tiles_m * g.n_tiles_n;
+  e = cta_pairs ? launch_mode<WG2, true>(ma, mb, mb, mc, mc, mc, g, wg2_items, s)
+                : launch_mode<WG2>(ma, mb, mb, mc, mc, mc, g, wg2_items, s);
   trace_end(MOE_STAGE_BWD_WG2, s);
   if (e != cudaSuccess) return e;
   // [dW1[e]; dW3[e]] = [da | db]^T x_perm: A = dab [N, 2f], B = x_perm [N, d]
   if (!make_map(&ma, dab, rows, 2LL * f, 64) || !make_map(&mb, x_perm, rows, d, 64))
     return cudaErrorInvalidValue;
-  g.n_tiles_m = ceil_div(2 * f, BM);
+  g.n_tiles_m = ceil_div(2 * f, tile_m);
   g.n_tiles_n = ceil_div(d, BN);
   g.out_f32 = dW1; g.out_f32b = dW3;
   if (!make_map_f32_3d(&mc, dW1, E, f, d) || !make_map_f32_3d(&mc2, dW3, E, f, d))
     return cudaErrorInvalidValue;
   trace_begin(MOE_STAGE_BWD_WG13, s);
-  e = launch_mode<WG13>(ma, mb, mb, mc, mc2, g, (long long)E * g.n_tiles_m * g.n_tiles_n, s);
+  const long long wg13_items = (long long)E * g.n_tiles_m * g.n_tiles_n;
+  e = cta_pairs ? launch_mode<WG13, true>(ma, mb, mb, mc, mc2, mc2, g, wg13_items, s)
+                : launch_mode<WG13>(ma, mb, mb, mc, mc2, mc2, g, wg13_items, s);
   trace_end(MOE_STAGE_BWD_WG13, s);
   return e;
 }

@@ -68,7 +68,8 @@ size_t tiles_ws_bytes(int N, int E);
 cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
-                           void* tiles_ws, int* err, bool prepacked, cudaStream_t s);
+                           void* tiles_ws, int* err, bool prepacked, bool cta_pairs,
+                           cudaStream_t s);
 // Weight tiles for the forward GEMMs: W1p, W3p [E][f/128][d/64][128][64] and
 // W2p [E][d/256][f/64][256][64] (bf16), each tile one TMA box, contiguous.
 bool prepack_supported(int d, int f);
@@ -79,7 +80,8 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            const uint16_t* a_s, const uint16_t* b_s, const uint16_t* h,
                            const uint16_t* dO, uint16_t* dab, uint16_t* dx_perm, float* dW1,
-                           float* dW3, float* dW2, void* tiles_ws, int* err, cudaStream_t s);
+                           float* dW3, float* dW2, void* tiles_ws, int* err, bool cta_pairs,
+                           cudaStream_t s);
 
 // backward of routing / dispatch / combine
 cudaError_t launch_bwd_route(const uint16_t* dy, const uint16_t* o, const int32_t* slot_row,

@@ -66,6 +66,10 @@ typedef void* moe_stream_t;  /* cudaStream_t */
 #define MOE_CHECK 0x2u       /* wait for the call's work and report device-side errors */
 #define MOE_WEIGHTS_PREPACKED 0x4u  /* moe_grouped_ffn / moe_layer_fwd: W1, W3, W2 are the
                                        tiles written by moe_prepack_weights */
+#define MOE_SINGLE_CTA_TILES 0x8u   /* moe_grouped_ffn / moe_layer_fwd / moe_layer_bwd: run
+                                       the expert GEMMs on single-CTA 128-row tiles instead
+                                       of 256-row tiles on CTA pairs (same results, bit for
+                                       bit; for comparison) */
 
 /* Stages of moe_layer_fwd / moe_layer_bwd, for moe_trace_events. */
 typedef enum {
