@@ -132,12 +132,15 @@ def stage_work(wl, fp8=False):
     """Algorithmic work of one launch of each traced stage: (kind, amount).
 
     kind "tflop": FLOPs of real rows only (no padding); "gb": bytes that must
-    move to or from HBM at least once (reads of inputs + writes of outputs).
+    move to or from HBM at least once (reads of inputs + writes of outputs);
+    "tflop3": the gate projection x W_g on the tensor cores as three bf16
+    products (W_g split into hi + mid + lo), so the pipe executes 3x the
+    algorithmic FLOPs counted here; "alu": the FP32 FMA gate (d % 64 != 0).
     """
     T, d, E, R, f = wl.T, wl.d, wl.E, wl.R, wl.f
     N = T * R
     w = {
-        "gate": ("alu", 2.0 * T * d * E),
+        "gate": ("tflop3" if d % 64 == 0 else "alu", 2.0 * T * d * E),
         "topk": ("gb", 4.0 * T * E + 8.0 * N),
         "dispatch": ("gb", 2.0 * T * d + (N * d + 4.0 * N * d / 128 if fp8 else 2.0 * N * d)
                      + 4.0 * N * 3),
@@ -335,6 +338,11 @@ def run_ours(args, rank, world, device):
             ach = amount / (ms / 1e3) / 1e9
             stages[name] = {"ms": round(ms, 4), "gbs": round(ach, 1),
                             "frac": round(ach / pk["hbm_gbs"], 4)}
+        elif kind == "tflop3":
+            ach = amount / (ms / 1e3) / 1e12
+            stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 1),
+                            "tensor_tflops": round(3 * ach, 1),
+                            "frac": round(3 * ach / pk["bf16_tflops_sustained"], 4)}
         else:
             ach = amount / (ms / 1e3) / 1e12
             stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 2),
@@ -342,8 +350,9 @@ def run_ours(args, rank, world, device):
     dom = max(stages, key=lambda n: stages[n]["ms"])
     kind, amount = work[dom]
     traffic = profiled_traffic(wl.name, dom)
-    if kind == "tflop":
-        roof = {"bound": "tensor", "kernel": dom, "achieved": stages[dom]["tflops"],
+    if kind in ("tflop", "tflop3"):
+        roof = {"bound": "tensor", "kernel": dom,
+                "achieved": stages[dom].get("tensor_tflops", stages[dom]["tflops"]),
                 "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": stages[dom]["frac"], "traffic": traffic,
                 "peak_source": f"{pk_src} bf16 sustained (kernel timed inside a long step)"}
