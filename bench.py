@@ -60,6 +60,12 @@ def parse():
     p.add_argument("--single-cta", action="store_true",
                    help="expert GEMMs on single-CTA 128-row tiles instead of 256-row tiles on "
                         "CTA pairs")
+    p.add_argument("--shared-expert", type=int, default=0, metavar="FS",
+                   help="layer workloads: add one shared expert of hidden size FS (0: none), run "
+                        "on the library's side stream beside route, dispatch and the routed FFN")
+    p.add_argument("--shared-serial", action="store_true",
+                   help="run the shared expert on the caller's stream after the routed path "
+                        "(MOE_SHARED_SERIAL), for comparison")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -128,10 +134,11 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- work model
-def stage_work(wl, fp8=False):
+def stage_work(wl, fp8=False, shared_fs=0):
     """Algorithmic work of one launch of each traced stage: (kind, amount).
 
-    kind "tflop": FLOPs of real rows only (no padding); "gb": bytes that must
+    kind "tflop": FLOPs of real rows only (no padding); "side": the same for the
+    shared expert's GEMMs (overlapping other stages); "gb": bytes that must
     move to or from HBM at least once (reads of inputs + writes of outputs);
     "tflop3": the gate projection x W_g on the tensor cores as three bf16
     products (W_g split into hi + mid + lo), so the pipe executes 3x the
@@ -158,6 +165,11 @@ def stage_work(wl, fp8=False):
             "bwd_dwg": ("gb", 2.0 * N * d + 4.0 * N + 4.0 * d * E),
             "bwd_dxc": ("gb", 2.0 * N * d + 2.0 * T * d + 8.0 * E * d),
         })
+    if f and shared_fs:
+        # the shared expert on the side stream: reported, but its time overlaps
+        # other stages, so it stays out of the GEMM summary and the dominant kernel
+        w.update({"shared_fwd": ("side", 6.0 * T * d * shared_fs),
+                  "shared_bwd": ("side", 12.0 * T * d * shared_fs)})
     return w
 
 
@@ -247,7 +259,21 @@ def run_ours(args, rank, world, device):
                 inp[k] = t
             fwd_flags |= B.MOE_WEIGHTS_PREPACKED
             weights_note = "prepacked tiles (moe_prepack_weights once, before timing)"
-        layer = B.Layer(inp["w_gate"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], wl.R, wl.T)
+        shared = None
+        if args.shared_expert:
+            fs = args.shared_expert
+            sw = {k: v.to(device) for k, v in synth.shared_expert_inputs(wl, fs).items()}
+            sg = {}
+            if train:
+                sg = dict(dW1=torch.empty((fs, wl.d), dtype=torch.float32, device=device),
+                          dW3=torch.empty((fs, wl.d), dtype=torch.float32, device=device),
+                          dW2=torch.empty((wl.d, fs), dtype=torch.float32, device=device))
+            shared = B.Shared(sw["W1"], sw["W3"], sw["W2"], **sg)
+            if args.shared_serial:
+                gemm_flags |= B.MOE_SHARED_SERIAL
+                fwd_flags |= B.MOE_SHARED_SERIAL
+        layer = B.Layer(inp["w_gate"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], wl.R, wl.T,
+                        shared=shared)
         saved = B.Saved(layer, device, train=train)
         x = inp["x"]
         y = torch.empty_like(x)
@@ -318,13 +344,13 @@ def run_ours(args, rank, world, device):
         for name, ms in tr.elapsed_ms().items():
             stage_ms[name] = stage_ms.get(name, 0.0) + ms / args.steps
     pk, pk_src = load_peaks()
-    work = stage_work(wl, fp8=args.fp8)
+    work = stage_work(wl, fp8=args.fp8, shared_fs=args.shared_expert)
     if identity:
         ran = ("dispatch", "combine")
     elif train:
         ran = tuple(work)
     else:
-        ran = ("gate", "topk", "dispatch", "gateup", "down", "combine")
+        ran = ("gate", "topk", "dispatch", "gateup", "down", "combine", "shared_fwd")
     stages = {}
     for name, ms in stage_ms.items():
         if name not in ran or ms <= 0:
@@ -338,6 +364,11 @@ def run_ours(args, rank, world, device):
             ach = amount / (ms / 1e3) / 1e9
             stages[name] = {"ms": round(ms, 4), "gbs": round(ach, 1),
                             "frac": round(ach / pk["hbm_gbs"], 4)}
+        elif kind == "side":
+            ach = amount / (ms / 1e3) / 1e12
+            stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 1),
+                            "frac": round(ach / pk["bf16_tflops_sustained"], 4),
+                            "overlaps_other_stages": not args.shared_serial}
         elif kind == "tflop3":
             ach = amount / (ms / 1e3) / 1e12
             stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 1),
@@ -347,7 +378,7 @@ def run_ours(args, rank, world, device):
             ach = amount / (ms / 1e3) / 1e12
             stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 2),
                             "frac": round(ach / alu_peak_tflops(clk.get("sm_mhz")), 4)}
-    dom = max(stages, key=lambda n: stages[n]["ms"])
+    dom = max((n for n in stages if work[n][0] != "side"), key=lambda n: stages[n]["ms"])
     kind, amount = work[dom]
     traffic = profiled_traffic(wl.name, dom)
     if kind in ("tflop", "tflop3"):
@@ -436,7 +467,11 @@ def run_ours(args, rank, world, device):
                    "l2": "inputs larger than L2 every step (no flush)",
                    "weights": weights_note,
                    "gemm_tiles": None if identity else
-                   ("128-row, one CTA" if args.single_cta else "256-row, CTA pairs")},
+                   ("128-row, one CTA" if args.single_cta else "256-row, CTA pairs"),
+                   "shared_expert": (None if not args.shared_expert else
+                                     {"fs": args.shared_expert,
+                                      "stream": "caller's, after the routed path"
+                                      if args.shared_serial else "side stream, overlapped"})},
         "roofline": roof,
         "summary": summary,
         "stages": stages,
@@ -457,7 +492,7 @@ class LazyExperts:
         return self.bits(self.t[e])
 
 
-def cpu_oracle_sample(wl, device, n_tokens, steps=1):
+def cpu_oracle_sample(wl, device, n_tokens, steps=1, shared_fs=0):
     """Times the CPU oracle (fwd, and bwd for training) on the first n_tokens tokens."""
     import numpy as np
     import torch
@@ -490,11 +525,15 @@ def cpu_oracle_sample(wl, device, n_tokens, steps=1):
         wg = inp["w_gate"].cpu().numpy()
         bias = None if inp["bias"] is None else inp["bias"].cpu().numpy()
         g = bits(inp["g"])[:n] if wl.train else None
+        shared = None
+        if shared_fs:
+            sw = synth.shared_expert_inputs(wl, shared_fs)
+            shared = tuple(bits(sw[k]) for k in ("W1", "W3", "W2"))
         t0 = time.perf_counter()
         for _ in range(steps):
-            fw = O.layer_fwd(x, wg, bias, W1, W3, W2, wl.R)
+            fw = O.layer_fwd(x, wg, bias, W1, W3, W2, wl.R, shared=shared)
             if wl.train:
-                O.layer_bwd(fw, x, wg, W1, W3, W2, g, wl.R)
+                O.layer_bwd(fw, x, wg, W1, W3, W2, g, wl.R, shared=shared)
         dt = time.perf_counter() - t0
     return n * steps / dt, dt, n
 
@@ -558,11 +597,11 @@ def main():
         except ImportError:
             device = "cpu"
         for _ in range(args.warmup):
-            cpu_oracle_sample(wl, device, n)
+            cpu_oracle_sample(wl, device, n, shared_fs=args.shared_expert)
         rates = []
         t_all = 0.0
         for _ in range(args.steps):
-            rate, dt, _ = cpu_oracle_sample(wl, device, n)
+            rate, dt, _ = cpu_oracle_sample(wl, device, n, shared_fs=args.shared_expert)
             rates.append(rate)
             t_all += dt
         value = n * args.steps / t_all
@@ -593,7 +632,7 @@ def main():
     result, wl = run_ours(args, rank, world, device)
     if rank == 0 and not args.no_cpu_baseline:
         n = args.cpu_tokens or default_cpu_tokens(wl)
-        rate, dt, n = cpu_oracle_sample(wl, device, n)
+        rate, dt, n = cpu_oracle_sample(wl, device, n, shared_fs=args.shared_expert)
         result["cpu_baseline"] = {
             "value": round(rate, 2), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"the oracle ({'fwd+bwd' if wl.train else 'fwd'}) on the first {n} of "

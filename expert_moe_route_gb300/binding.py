@@ -19,25 +19,28 @@ MOE_LOGITS_IN = 0x1
 MOE_CHECK = 0x2
 MOE_WEIGHTS_PREPACKED = 0x4
 MOE_SINGLE_CTA_TILES = 0x8
+MOE_SHARED_SERIAL = 0x10
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CUDA"}
 
 # the C ABI's exported symbols (checked against include/moe.h by the tests)
-SYMBOLS = ("moe_status_string", "moe_version", "moe_trace_events", "moe_kernel_launches",
-           "moe_selftest_wait_timeout",
+SYMBOLS = ("moe_status_string", "moe_version", "moe_last_cuda_error", "moe_trace_events",
+           "moe_kernel_launches", "moe_selftest_wait_timeout",
            "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_dispatch_fp8",
            "moe_dequant_fp8", "moe_prepack_weights", "moe_grouped_ffn",
            "moe_combine", "moe_layer_fwd", "moe_layer_bwd")
 
 # moe_stage_t
 STAGES = ("gate", "topk", "dispatch", "gateup", "down", "combine", "bwd_route", "bwd_dh", "bwd_dx",
-          "bwd_wg2", "bwd_wg13", "bwd_dwg", "bwd_dxc")
+          "bwd_wg2", "bwd_wg13", "bwd_dwg", "bwd_dxc", "shared_fwd", "shared_bwd")
 
 
 class MoeError(RuntimeError):
-    def __init__(self, status: int, where: str):
-        super().__init__(f"{where}: {STATUS.get(status, status)}")
+    def __init__(self, status: int, where: str, cuda_error: int = 0):
+        extra = f" (cudaError {cuda_error})" if cuda_error else ""
+        super().__init__(f"{where}: {STATUS.get(status, status)}{extra}")
         self.status = status
+        self.cuda_error = cuda_error
 
 
 _vp = ctypes.c_void_p
@@ -46,14 +49,20 @@ _u = ctypes.c_uint
 _szp = ctypes.POINTER(ctypes.c_size_t)
 
 
+class moe_shared_t(ctypes.Structure):
+    _fields_ = [("fs", _i), ("W1", _vp), ("W3", _vp), ("W2", _vp), ("dW1", _vp), ("dW3", _vp),
+                ("dW2", _vp)]
+
+
 class moe_layer_t(ctypes.Structure):
     _fields_ = [("T", _i), ("d", _i), ("E", _i), ("R", _i), ("f", _i), ("w_gate", _vp),
-                ("bias", _vp), ("W1", _vp), ("W3", _vp), ("W2", _vp)]
+                ("bias", _vp), ("W1", _vp), ("W3", _vp), ("W2", _vp),
+                ("shared", ctypes.POINTER(moe_shared_t))]
 
 
 class moe_saved_t(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("logits", "topk_idx", "topk_w", "counts", "offsets", "row_slot",
-                                   "slot_row", "x_perm", "a", "b", "h", "o")]
+                                   "slot_row", "x_perm", "a", "b", "h", "o", "sa", "sb", "sh")]
 
 
 def _declare(lib):
@@ -131,7 +140,7 @@ def _stream(stream):
 
 def _check(st, where):
     if st != MOE_OK:
-        raise MoeError(st, where)
+        raise MoeError(st, where, int(lib().moe_last_cuda_error()) if st == 6 else 0)
 
 
 def _dt(t, dtype, name):
@@ -263,18 +272,30 @@ def moe_combine(expert_out, slot_row, topk_w, y, R, stream=None):
 
 
 # ---------------------------------------------------------------- layer
+class Shared:
+    """A shared expert (moe_shared_t): bf16 weights W1, W3 [fs, d], W2 [d, fs]
+    and, for moe_layer_bwd, fp32 gradient buffers of the same shapes."""
+
+    def __init__(self, W1, W3, W2, dW1=None, dW3=None, dW2=None):
+        self.W1, self.W3, self.W2 = W1, W3, W2
+        self.dW1, self.dW3, self.dW2 = dW1, dW3, dW2
+        self.fs = W1.shape[0]
+        self.c = moe_shared_t(self.fs, _p(W1), _p(W3), _p(W2), _p(dW1), _p(dW3), _p(dW2))
+
+
 class Layer:
     """Parameters of one MoE layer (device tensors) and their C struct."""
 
-    def __init__(self, w_gate, bias, W1, W3, W2, R, T):
+    def __init__(self, w_gate, bias, W1, W3, W2, R, T, shared: Shared = None):
         self.w_gate, self.bias, self.W1, self.W3, self.W2 = w_gate, bias, W1, W3, W2
         self.E, self.f, self.d = W1.shape
         self.R, self.T = R, T
+        self.shared = shared
         self.c = moe_layer_t(T, self.d, self.E, R, self.f, _p(w_gate), _p(bias), _p(W1), _p(W3),
-                             _p(W2))
+                             _p(W2), ctypes.pointer(shared.c) if shared is not None else None)
 
     def with_tokens(self, T):
-        return Layer(self.w_gate, self.bias, self.W1, self.W3, self.W2, self.R, T)
+        return Layer(self.w_gate, self.bias, self.W1, self.W3, self.W2, self.R, T, self.shared)
 
 
 class Saved:
@@ -296,6 +317,10 @@ class Saved:
         self.b = torch.empty((N, f), dtype=torch.bfloat16, **z) if train else None
         self.h = torch.empty((N, f), dtype=torch.bfloat16, **z)
         self.o = torch.empty((N, d), dtype=torch.bfloat16, **z)
+        fs = layer.shared.fs if layer.shared is not None else 0
+        for n in ("sa", "sb", "sh"):
+            setattr(self, n, torch.empty((T, fs), dtype=torch.bfloat16, **z)
+                    if fs and train else None)
         self.c = moe_saved_t(*[_p(getattr(self, n)) for n, _ in moe_saved_t._fields_])
 
 

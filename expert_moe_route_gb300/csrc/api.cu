@@ -3,6 +3,7 @@
 #include <stdio.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -10,9 +11,13 @@
 namespace moe {
 static std::atomic<unsigned long long> g_launches{0};
 static std::atomic<void* const*> g_trace{nullptr};
+// > 0 while this thread launches the shared expert's GEMMs, whose per-GEMM
+// stages would otherwise overwrite the routed GEMMs' trace events.
+static thread_local int g_trace_mute = 0;
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 // A failed trace record must not surface later as a launch error: clear it.
 static void trace_record(int slot, cudaStream_t s) {
+  if (g_trace_mute) return;
   void* const* ev = g_trace.load(std::memory_order_relaxed);
   if (ev && ev[slot] && cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[slot]), s) != cudaSuccess)
     (void)cudaGetLastError();
@@ -52,15 +57,24 @@ bool init_once() {
   return true;
 }
 
+// The CUDA error behind this thread's last MOE_ERR_CUDA (moe_last_cuda_error).
+thread_local int g_last_cuda = 0;
+
+moe_status_t cuda_failed(cudaError_t e) {
+  g_last_cuda = (int)e;
+  return MOE_ERR_CUDA;
+}
+
 // Optionally wait for the stream and translate the device error word.
 moe_status_t finish(cudaError_t launched, const int* err_dev, unsigned flags, cudaStream_t s) {
-  if (launched != cudaSuccess) return MOE_ERR_CUDA;
+  if (launched != cudaSuccess) return cuda_failed(launched);
   if (!(flags & MOE_CHECK)) return MOE_OK;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_failed(e);
   if (!err_dev) return MOE_OK;
   int h = 0;
-  if (cudaMemcpy(&h, err_dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  e = cudaMemcpy(&h, err_dev, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_failed(e);
   if (h & kErrTimeout) return MOE_ERR_TIMEOUT;
   if (h & kErrBadRouting) return MOE_ERR_BAD_ROUTING;
   return MOE_OK;
@@ -83,6 +97,51 @@ struct Stage {
   int i;
   Stage(cudaStream_t s_, int stage) : s(s_), i(stage) { trace_begin(i, s); }
   ~Stage() { trace_end(i, s); }
+};
+
+struct TraceMute {
+  TraceMute() { ++g_trace_mute; }
+  ~TraceMute() { --g_trace_mute; }
+};
+
+// The shared expert's stream: one per device, created on first use and kept
+// for the life of the process.
+cudaStream_t side_stream() {
+  static std::mutex mu;
+  static cudaStream_t st[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!st[dev] && cudaStreamCreateWithFlags(&st[dev], cudaStreamNonBlocking) != cudaSuccess)
+    st[dev] = nullptr;
+  return st[dev];
+}
+
+// `to` waits for the work enqueued on `from` so far.
+cudaError_t stream_wait(cudaStream_t to, cudaStream_t from) {
+  if (to == from) return cudaSuccess;
+  cudaEvent_t ev;
+  cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return e;
+  e = cudaEventRecord(ev, from);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(to, ev, 0);
+  cudaEventDestroy(ev);   // released once the recorded work completes
+  return e;
+}
+
+// Joins the side stream back into the caller's stream when it goes out of
+// scope, so that no return path leaves shared-expert work unordered with
+// the caller's later work.
+struct Join {
+  cudaStream_t to, from;
+  bool armed = false;
+  ~Join() {
+    if (armed) (void)stream_wait(to, from);
+  }
+  cudaError_t now() {
+    armed = false;
+    return stream_wait(to, from);
+  }
 };
 
 #define MOE_TRY(expr)                        \
@@ -109,6 +168,8 @@ const char* moe_status_string(moe_status_t st) {
 }
 
 int moe_version(void) { return 100; }
+
+int moe_last_cuda_error(void) { return g_last_cuda; }
 
 moe_status_t moe_trace_events(void* const* events) {
   g_trace.store(events, std::memory_order_relaxed);
@@ -323,13 +384,25 @@ static moe_status_t check_layer(const moe_layer_t* L) {
   if (L->f % 8) return MOE_ERR_UNSUPPORTED;
   if (!L->w_gate || !L->W1 || !L->W3 || !L->W2) return MOE_ERR_INVALID_ARG;
   if (!al16(L->W1) || !al16(L->W3) || !al16(L->W2)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_shared_t* sh = L->shared) {
+    if (sh->fs <= 0 || !sh->W1 || !sh->W3 || !sh->W2) return MOE_ERR_INVALID_ARG;
+    if (sh->fs % 8 || !al16(sh->W1) || !al16(sh->W3) || !al16(sh->W2)) return MOE_ERR_UNSUPPORTED;
+  }
   return MOE_OK;
+}
+
+// Workspace of the shared expert's forward: offsets {0, T}, its tile list,
+// its output rows [T,d] and (inference) its hidden rows [T,fs].
+static size_t shared_fwd_ws(const moe_layer_t* L) {
+  if (!L->shared) return 0;
+  const size_t T = L->T, d = L->d, fs = L->shared->fs;
+  return 256 + tiles_ws_bytes((int)T, 1) + align_up(T * d * 2, 256) + align_up(T * fs * 2, 256);
 }
 
 static size_t layer_fwd_ws(const moe_layer_t* L) {
   const int N = L->T * L->R;
   return kErrBytes + align_up(dispatch_ws_bytes(L->T, L->E), 256) + tiles_ws_bytes(N, L->E) +
-         align_up(gate_ws_bytes(L->d, L->E), 256);
+         align_up(gate_ws_bytes(L->d, L->E), 256) + shared_fwd_ws(L);
 }
 
 moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
@@ -351,21 +424,55 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
       !sv->row_slot || !sv->slot_row || !sv->x_perm || !sv->h || !sv->o)
     return MOE_ERR_INVALID_ARG;
   if ((sv->a == nullptr) != (sv->b == nullptr)) return MOE_ERR_INVALID_ARG;
-  const void* ps[] = {x, y, sv->x_perm, sv->a, sv->b, sv->h, sv->o};
+  const moe_shared_t* SH = L->shared;
+  if (SH && ((sv->sa == nullptr) != (sv->sb == nullptr) || (sv->sa && !sv->sh)))
+    return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {x, y, sv->x_perm, sv->a, sv->b, sv->h, sv->o,
+                      SH ? sv->sa : nullptr, SH ? sv->sb : nullptr, SH ? sv->sh : nullptr};
   for (const void* p : ps)
     if (p && !al16(p)) return MOE_ERR_UNSUPPORTED;
   if (!init_once()) return MOE_ERR_CUDA;
   const int T = L->T, d = L->d, E = L->E, R = L->R, f = L->f, N = T * R;
+  const bool pairs = !(flags & MOE_SINGLE_CTA_TILES);
   cudaStream_t s = S(stream);
+  const bool side = SH && !(flags & MOE_SHARED_SERIAL);
+  cudaStream_t s2 = side ? side_stream() : s;
+  if (side && !s2) return MOE_ERR_CUDA;   // (the caller's stream may be the null stream)
   Carve c(ws);
   int* err = static_cast<int*>(c.take(kErrBytes));
   void* dws = c.take(dispatch_ws_bytes(T, E));
   void* tws = c.take(tiles_ws_bytes(N, E));
   void* gws = c.take(gate_ws_bytes(d, E));
+  int32_t* s_off = nullptr;
+  void* s_tws = nullptr;
+  uint16_t *s_out = nullptr, *s_h = nullptr;
+  if (SH) {
+    s_off = static_cast<int32_t*>(c.take(256));
+    s_tws = c.take(tiles_ws_bytes(T, 1));
+    s_out = static_cast<uint16_t*>(c.take((size_t)T * d * 2));
+    s_h = static_cast<uint16_t*>(c.take((size_t)T * SH->fs * 2));
+    if (sv->sh) s_h = sv->sh;
+  }
+  // the shared expert: SwiGLU of every token (one expert holding all T rows)
+  auto shared_fwd = [&]() -> cudaError_t {
+    Stage st_(s2, MOE_STAGE_SHARED_FWD);
+    TraceMute mute_;
+    cudaError_t e = launch_one_expert_offsets(s_off, T, s2);
+    if (e == cudaSuccess)
+      e = launch_ffn_fwd(x, s_off, T, d, SH->fs, 1, SH->W1, SH->W3, SH->W2, sv->sa, sv->sb, s_h,
+                         s_out, s_tws, err, false, pairs, s2);
+    return e;
+  };
+  Join join{s, s2};
   MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
   {
     Stage st_(s, MOE_STAGE_GATE);
     MOE_TRY(launch_gate(x, L->w_gate, L->bias, T, d, E, sv->logits, gws, err, s));
+  }
+  if (side) {   // fork: the shared expert overlaps top-R, dispatch and the routed FFN
+    MOE_TRY(stream_wait(s2, s));
+    join.armed = true;
+    MOE_TRY(shared_fwd());
   }
   {
     Stage st_(s, MOE_STAGE_TOPK);
@@ -377,12 +484,13 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
                             sv->slot_row, sv->x_perm, dws, err, s));
   }
   MOE_TRY(launch_ffn_fwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
-                         sv->h, sv->o, tws, err, (flags & MOE_WEIGHTS_PREPACKED) != 0,
-                         !(flags & MOE_SINGLE_CTA_TILES), s));
+                         sv->h, sv->o, tws, err, (flags & MOE_WEIGHTS_PREPACKED) != 0, pairs, s));
+  if (SH && !side) MOE_TRY(shared_fwd());
+  if (side) MOE_TRY(join.now());
   cudaError_t e;
   {
     Stage st_(s, MOE_STAGE_COMBINE);
-    e = launch_combine(sv->o, sv->slot_row, sv->topk_w, T, d, R, y, s);
+    e = launch_combine(sv->o, sv->slot_row, sv->topk_w, T, d, R, y, s, s_out);
   }
   return finish(e, err, flags, s);
 }
@@ -398,6 +506,10 @@ static size_t layer_bwd_ws(const moe_layer_t* L) {
   n += align_up(N * 4, 256);            // dlogits per row
   n += align_up(E * d * 4, 256);        // W_g^T
   n += dwg_ws_bytes((int)d, (int)E);    // router weight-gradient partials
+  if (L->shared) {                      // shared expert: offsets, tiles, [das | dbs], dxs
+    const size_t fs = L->shared->fs;
+    n += 256 + tiles_ws_bytes((int)T, 1) + align_up(T * 2 * fs * 2, 256) + align_up(T * d * 2, 256);
+  }
   return n;
 }
 
@@ -408,6 +520,8 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
   moe_status_t st = check_layer(L);
   if (st != MOE_OK) return st;
   if (L->d % 64 || L->f % 64 || (flags & MOE_WEIGHTS_PREPACKED)) return MOE_ERR_UNSUPPORTED;
+  const moe_shared_t* SH = L->shared;
+  if (SH && SH->fs % 64) return MOE_ERR_UNSUPPORTED;
   if (!ws_bytes) return MOE_ERR_INVALID_ARG;
   const size_t need = layer_bwd_ws(L);
   if (!ws) {
@@ -416,11 +530,19 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
   }
   if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
   if (!dW_gate || !dW1 || !dW3 || !dW2) return MOE_ERR_INVALID_ARG;
+  if (SH && (!SH->dW1 || !SH->dW3 || !SH->dW2)) return MOE_ERR_INVALID_ARG;
+  if (SH && (!al16(SH->dW1) || !al16(SH->dW3) || !al16(SH->dW2))) return MOE_ERR_UNSUPPORTED;
   if (L->T == 0) {   // no tokens: every gradient is zero
     if (!al16(dW_gate) || !al16(dW1) || !al16(dW3) || !al16(dW2)) return MOE_ERR_UNSUPPORTED;
     if (!init_once()) return MOE_ERR_CUDA;
     cudaStream_t s0 = S(stream);
     const size_t d = L->d, E = L->E, f = L->f;
+    if (SH) {
+      const size_t fs = SH->fs;
+      MOE_TRY(cudaMemsetAsync(SH->dW1, 0, sizeof(float) * fs * d, s0));
+      MOE_TRY(cudaMemsetAsync(SH->dW3, 0, sizeof(float) * fs * d, s0));
+      MOE_TRY(cudaMemsetAsync(SH->dW2, 0, sizeof(float) * fs * d, s0));
+    }
     MOE_TRY(cudaMemsetAsync(dW_gate, 0, sizeof(float) * d * E, s0));
     MOE_TRY(cudaMemsetAsync(dW1, 0, sizeof(float) * E * f * d, s0));
     MOE_TRY(cudaMemsetAsync(dW3, 0, sizeof(float) * E * f * d, s0));
@@ -430,12 +552,18 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
   if (!sv->a || !sv->b || !sv->h || !sv->o || !sv->x_perm || !sv->topk_idx || !sv->topk_w ||
       !sv->offsets || !sv->slot_row)
     return MOE_ERR_INVALID_ARG;
+  if (SH && (!sv->sa || !sv->sb || !sv->sh)) return MOE_ERR_INVALID_ARG;
   const void* ps[] = {x, dy, dx, dW_gate, dW1, dW3, dW2, sv->a, sv->b, sv->h, sv->o, sv->x_perm};
   for (const void* p : ps)
     if (!al16(p)) return MOE_ERR_UNSUPPORTED;
+  if (SH && (!al16(sv->sa) || !al16(sv->sb) || !al16(sv->sh))) return MOE_ERR_UNSUPPORTED;
   if (!init_once()) return MOE_ERR_CUDA;
   const int T = L->T, d = L->d, E = L->E, R = L->R, f = L->f, N = T * R;
+  const bool pairs = !(flags & MOE_SINGLE_CTA_TILES);
   cudaStream_t s = S(stream);
+  const bool side = SH && !(flags & MOE_SHARED_SERIAL);
+  cudaStream_t s2 = side ? side_stream() : s;
+  if (side && !s2) return MOE_ERR_CUDA;   // (the caller's stream may be the null stream)
   Carve c(ws);
   int* err = static_cast<int*>(c.take(kErrBytes));
   void* tws = c.take(tiles_ws_bytes(N, E));
@@ -446,7 +574,32 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
   float* dsel_row = static_cast<float*>(c.take((size_t)N * 4));
   float* wgT = static_cast<float*>(c.take((size_t)E * d * 4));
   void* dwg_ws = c.take(dwg_ws_bytes(d, E));
+  int32_t* s_off = nullptr;
+  void* s_tws = nullptr;
+  uint16_t *s_dab = nullptr, *s_dx = nullptr;
+  if (SH) {
+    s_off = static_cast<int32_t*>(c.take(256));
+    s_tws = c.take(tiles_ws_bytes(T, 1));
+    s_dab = static_cast<uint16_t*>(c.take((size_t)T * 2 * SH->fs * 2));
+    s_dx = static_cast<uint16_t*>(c.take((size_t)T * d * 2));
+  }
+  // the shared expert's backward, with dy as its output gradient
+  auto shared_bwd = [&]() -> cudaError_t {
+    Stage st_(s2, MOE_STAGE_SHARED_BWD);
+    TraceMute mute_;
+    cudaError_t e = launch_one_expert_offsets(s_off, T, s2);
+    if (e == cudaSuccess)
+      e = launch_ffn_bwd(x, s_off, T, d, SH->fs, 1, SH->W1, SH->W3, SH->W2, sv->sa, sv->sb, sv->sh,
+                         dy, s_dab, s_dx, SH->dW1, SH->dW3, SH->dW2, s_tws, err, pairs, s2);
+    return e;
+  };
+  Join join{s, s2};
   MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  if (side) {   // fork: the shared expert's backward overlaps the routed one
+    MOE_TRY(stream_wait(s2, s));
+    join.armed = true;
+    MOE_TRY(shared_bwd());
+  }
   if (N == 0) {
     MOE_TRY(cudaMemsetAsync(dW_gate, 0, sizeof(float) * d * E, s));
     MOE_TRY(cudaMemsetAsync(dW1, 0, sizeof(float) * E * f * d, s));
@@ -459,18 +612,20 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
                              s));
   }
   MOE_TRY(launch_ffn_bwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
-                         sv->h, dO, dab, dxp, dW1, dW3, dW2, tws, err,
-                         !(flags & MOE_SINGLE_CTA_TILES), s));
+                         sv->h, dO, dab, dxp, dW1, dW3, dW2, tws, err, pairs, s));
   {
     Stage st_(s, MOE_STAGE_BWD_DWG);
     MOE_TRY(launch_dwg(sv->x_perm, sv->offsets, dsel_row, d, E, dW_gate, dwg_ws, s));
   }
+  if (SH && !side) MOE_TRY(shared_bwd());
+  if (side) MOE_TRY(join.now());
   cudaError_t e;
   {
     Stage st_(s, MOE_STAGE_BWD_DXC);
     e = launch_wg_transpose(L->w_gate, d, E, wgT, s);
     if (e == cudaSuccess)
-      e = launch_dx_combine(dxp, sv->slot_row, sv->topk_idx, dsel_tok, wgT, T, d, E, R, dx, s);
+      e = launch_dx_combine(dxp, sv->slot_row, sv->topk_idx, dsel_tok, wgT, T, d, E, R, dx, s,
+                            s_dx);
   }
   return finish(e, err, flags, s);
 }

@@ -176,7 +176,8 @@ __global__ void dwg_reduce_kernel(const float* __restrict__ part, int d, int E,
 __global__ void __launch_bounds__(BW * 32) dx_combine_kernel(
     const uint16_t* __restrict__ dx_perm, const int32_t* __restrict__ slot_row,
     const int32_t* __restrict__ idx, const float* __restrict__ dsel, const float* __restrict__ wgT,
-    int T, int d, int E, int R, int N, uint16_t* __restrict__ dx) {
+    int T, int d, int E, int R, int N, const uint16_t* __restrict__ add,
+    uint16_t* __restrict__ dx) {
   __shared__ int rows_s[BW][32];
   __shared__ int exp_s[BW][32];
   __shared__ float ds_s[BW][32];
@@ -235,6 +236,12 @@ __global__ void __launch_bounds__(BW * 32) dx_combine_kernel(
           acc[6] = fmaf(ds, b[u].z, acc[6]); acc[7] = fmaf(ds, b[u].w, acc[7]);
         }
       }
+      if (add) {   // + the shared expert's dx
+        float f[8];
+        unpack8(ldg_nc_v4(add + (size_t)t * d + (size_t)v * 8), f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += f[j];
+      }
       reinterpret_cast<uint4*>(dx + (size_t)t * d)[v] = pack8(acc);
     }
     __syncwarp();
@@ -279,10 +286,11 @@ cudaError_t launch_dwg(const uint16_t* x_perm, const int32_t* offsets, const flo
 
 cudaError_t launch_dx_combine(const uint16_t* dx_perm, const int32_t* slot_row,
                               const int32_t* idx, const float* dsel_tok, const float* wgT, int T,
-                              int d, int E, int R, uint16_t* dx, cudaStream_t s) {
+                              int d, int E, int R, uint16_t* dx, cudaStream_t s,
+                              const uint16_t* add) {
   if (T == 0) return cudaSuccess;
   dx_combine_kernel<<<grid_for(T, BW), BW * 32, 0, s>>>(dx_perm, slot_row, idx, dsel_tok, wgT, T,
-                                                       d, E, R, T * R, dx);
+                                                       d, E, R, T * R, add, dx);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(CW * 32) combine_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ slot_row,
                                                           const float* __restrict__ w, int T,
                                                           int d, int R, int N,
+                                                          const uint16_t* __restrict__ add,
                                                           uint16_t* __restrict__ y) {
   __shared__ int rows_s[CW][32];
   __shared__ float w_s[CW][32];
@@ -33,6 +34,7 @@ __global__ void __launch_bounds__(CW * 32) combine_kernel(const uint16_t* __rest
     __syncwarp();
     for (int v = lane; v < nv; v += 32) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (add) unpack8(ldg_nc_v4(add + (size_t)t * d + (size_t)v * 8), acc);   // shared expert first
       for (int r0 = 0; r0 < R; r0 += 4) {
         uint4 q[4];
 #pragma unroll
@@ -77,10 +79,23 @@ cudaError_t launch_selftest_wait(unsigned limit_us, int* err, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const float* w, int T,
-                           int d, int R, uint16_t* y, cudaStream_t s) {
+                           int d, int R, uint16_t* y, cudaStream_t s, const uint16_t* add) {
   if (T == 0) return cudaSuccess;
   const int blocks = ceil_div(T, CW) < 152 * 8 ? ceil_div(T, CW) : 152 * 8;
-  combine_kernel<<<blocks, CW * 32, 0, s>>>(o, slot_row, w, T, d, R, T * R, y);
+  combine_kernel<<<blocks, CW * 32, 0, s>>>(o, slot_row, w, T, d, R, T * R, add, y);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+namespace {
+__global__ void one_expert_offsets_kernel(int32_t* offsets, int T) {
+  offsets[0] = 0;
+  offsets[1] = T;
+}
+}  // namespace
+
+cudaError_t launch_one_expert_offsets(int32_t* offsets, int T, cudaStream_t s) {
+  one_expert_offsets_kernel<<<1, 1, 0, s>>>(offsets, T);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -61,8 +61,12 @@ cudaError_t launch_dispatch_fp8(const uint16_t* x, const int32_t* idx, int T, in
 cudaError_t launch_dequant_fp8(const uint8_t* xq, const float* xs, long long N, int d,
                                uint16_t* out, cudaStream_t s);
 
+// y = bf16(add + sum_r w o); add (bf16 [T,d], the shared expert's output) may be null.
 cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const float* w, int T,
-                           int d, int R, uint16_t* y, cudaStream_t s);
+                           int d, int R, uint16_t* y, cudaStream_t s,
+                           const uint16_t* add = nullptr);
+// offsets = {0, T}: every token in one expert (the shared expert).
+cudaError_t launch_one_expert_offsets(int32_t* offsets, int T, cudaStream_t s);
 
 size_t tiles_ws_bytes(int N, int E);
 cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
@@ -93,6 +97,7 @@ cudaError_t launch_dwg(const uint16_t* x_perm, const int32_t* offsets, const flo
                        int d, int E, float* dW_gate, void* ws, cudaStream_t s);
 cudaError_t launch_dx_combine(const uint16_t* dx_perm, const int32_t* slot_row,
                               const int32_t* idx, const float* dsel_tok, const float* wgT, int T,
-                              int d, int E, int R, uint16_t* dx, cudaStream_t s);
+                              int d, int E, int R, uint16_t* dx, cudaStream_t s,
+                              const uint16_t* add = nullptr);
 
 }  // namespace moe

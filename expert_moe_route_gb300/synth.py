@@ -164,6 +164,15 @@ def layer_inputs(wl: Workload, device="cpu", weight_device=None, with_grad=None)
     return out
 
 
+def shared_expert_inputs(wl: Workload, fs: int, device="cpu"):
+    """Seeded weights of one shared expert: W1, W3 bf16 [fs, d], W2 bf16 [d, fs],
+    ~N(0, 0.02) like the routed experts'."""
+    base = wl.index * 1000 + 500
+    return {"W1": _normal_bf16((fs, wl.d), 0.02, device, base + _W1),
+            "W3": _normal_bf16((fs, wl.d), 0.02, device, base + _W3),
+            "W2": _normal_bf16((wl.d, fs), 0.02, device, base + _W2)}
+
+
 def drawn_routing(wl: Workload, device="cpu"):
     """Routing drawn directly (dispatch-only workloads): idx int32 [T,R], w fp32 [T,R].
 

@@ -70,6 +70,10 @@ typedef void* moe_stream_t;  /* cudaStream_t */
                                        the expert GEMMs on single-CTA 128-row tiles instead
                                        of 256-row tiles on CTA pairs (same results, bit for
                                        bit; for comparison) */
+#define MOE_SHARED_SERIAL 0x10u     /* moe_layer_fwd / moe_layer_bwd: run the shared expert on the
+                                       caller's stream after the routed path instead of on the
+                                       library's side stream beside it (same results, bit for
+                                       bit; for comparison) */
 
 /* Stages of moe_layer_fwd / moe_layer_bwd, for moe_trace_events. */
 typedef enum {
@@ -86,6 +90,8 @@ typedef enum {
   MOE_STAGE_BWD_WG13,      /* [dW1;dW3] = [da|db]^T x_perm per expert */
   MOE_STAGE_BWD_DWG,       /* router weight gradient */
   MOE_STAGE_BWD_DXC,       /* W_g transpose + dx gather-sum */
+  MOE_STAGE_SHARED_FWD,    /* shared expert forward (side stream unless MOE_SHARED_SERIAL) */
+  MOE_STAGE_SHARED_BWD,    /* shared expert backward (same stream rule) */
   MOE_STAGE_COUNT
 } moe_stage_t;
 
@@ -94,7 +100,8 @@ typedef enum {
  * events: NULL to disable, else 2*MOE_STAGE_COUNT cudaEvent_t handles created
  * by the caller on the current device; while set, moe_layer_fwd and
  * moe_layer_bwd record events[2*i] on their stream just before stage i and
- * events[2*i+1] just after it.  The pointer is kept (not copied) until the
+ * events[2*i+1] just after it (the shared-expert stages on the stream that
+ * runs them).  The pointer is kept (not copied) until the
  * next call; one setting is shared by all threads of the process.
  */
 moe_status_t moe_trace_events(void* const* events);
@@ -119,6 +126,10 @@ const char* moe_status_string(moe_status_t status);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int moe_version(void);
+
+/* The cudaError_t behind the calling thread's most recent MOE_ERR_CUDA (0 if
+ * none yet); for diagnostics. */
+int moe_last_cuda_error(void);
 
 /*
  * moe_route -- the router: a small linear layer scores the experts and the R
@@ -259,6 +270,29 @@ moe_status_t moe_dispatch_noalloc(const uint16_t* x, const int32_t* topk_idx, in
                                   moe_stream_t stream);
 
 /* Layer parameters (device pointers, caller-owned). */
+/*
+ * Optional shared expert (section "Introduction": while dispatch is in
+ * flight the GPU can do other work, such as the shared expert's
+ * multiplication).  A SwiGLU FFN that every token passes through, added to
+ * the routed experts' weighted sum with weight 1:
+ *   s_t = bf16( bf16(silu(x_t Ws1^T) * (x_t Ws3^T)) Ws2^T ),
+ *   y_t = bf16( s_t + sum_r w[t,r] o[slot_row[t*R+r]] ).
+ * The forward runs it on a side stream the library owns (one per device),
+ * forked from the caller's stream after the gate projection and joined before
+ * combine, so it overlaps top-R and dispatch; the backward forks it at the
+ * start and joins it before the dx gather.  Callers see ordinary stream
+ * semantics on their stream.
+ */
+typedef struct {
+  int fs;               /* hidden size; multiple of 8 (of 64 for the backward) */
+  const uint16_t* W1;   /* bf16 [fs,d] */
+  const uint16_t* W3;   /* bf16 [fs,d] */
+  const uint16_t* W2;   /* bf16 [d,fs] */
+  float* dW1;           /* moe_layer_bwd outputs, fp32 [fs,d], [fs,d], [d,fs]; */
+  float* dW3;           /*   unused by the forward (may be NULL there)        */
+  float* dW2;
+} moe_shared_t;
+
 typedef struct {
   int T, d, E, R, f;
   const float* w_gate;  /* fp32 [d,E] */
@@ -266,6 +300,7 @@ typedef struct {
   const uint16_t* W1;   /* bf16 [E,f,d] */
   const uint16_t* W3;   /* bf16 [E,f,d] */
   const uint16_t* W2;   /* bf16 [E,d,f] */
+  const moe_shared_t* shared;   /* NULL: no shared expert */
 } moe_layer_t;
 
 /* Forward intermediates (caller-owned device buffers, written by the forward,
@@ -283,12 +318,20 @@ typedef struct {
   uint16_t* b;         /* bf16 [N,f] or NULL (must be NULL iff a is) */
   uint16_t* h;         /* bf16 [N,f] */
   uint16_t* o;         /* bf16 [N,d] expert outputs */
+  /* shared expert (only read when the layer has one): its pre-activations
+   * and hidden rows for the backward, bf16 [T,fs]; all three NULL for
+   * inference (the forward then keeps its hidden rows in the workspace) */
+  uint16_t* sa;
+  uint16_t* sb;
+  uint16_t* sh;
 } moe_saved_t;
 
 /*
  * moe_layer_fwd -- y = combine(FFN(dispatch(x, route(x)))): route, dispatch,
  * grouped SwiGLU FFN and combine, as the entry points above define them.
  * x: bf16 [T,d]; y: bf16 [T,d]; saved: all intermediates (a and b may be NULL).
+ * With layer->shared, y also adds the shared expert's output (moe_shared_t);
+ * saved->sa, sb, sh then hold its intermediates (all NULL for inference).
  */
 moe_status_t moe_layer_fwd(const moe_layer_t* layer, const uint16_t* x, uint16_t* y,
                            const moe_saved_t* saved, void* ws, size_t* ws_bytes, unsigned flags,
@@ -303,7 +346,11 @@ moe_status_t moe_layer_fwd(const moe_layer_t* layer, const uint16_t* x, uint16_t
  *               dW2[e] = do^T h,  dW1[e] = da^T x_perm,  dW3[e] = db^T x_perm
  *   router:  dlogits[t, idx[t,q]] = w_q (dw_q - sum_r w_r dw_r), 0 for unchosen experts
  *            dW_gate = x^T dlogits
- *   dx_t = bf16( sum_r dx_perm[row(t,r)] + dlogits_t W_g^T )
+ *   dx_t = bf16( sum_r dx_perm[row(t,r)] + dlogits_t W_g^T [+ dxs_t] )
+ *   shared expert (layer->shared; saved->sa, sb, sh required), with dy as its
+ *   output gradient:  dhs = dy Ws2;  das = bf16(dhs * sb * silu'(sa)),
+ *   dbs = bf16(dhs * silu(sa));  dxs = bf16(das Ws1 + dbs Ws3);
+ *   shared->dW2 = dy^T sh,  shared->dW1 = das^T x,  shared->dW3 = dbs^T x
  * (a, b as saved in bf16; silu'(a) = s(a)(1 + a(1 - s(a))), s the logistic
  * function.)  x: bf16 [T,d]; dx: bf16 [T,d]; dW_gate: fp32 [d,E]; dW1, dW3:
  * fp32 [E,f,d]; dW2: fp32 [E,d,f] -- all overwritten (experts with no rows get

@@ -27,7 +27,12 @@ Readings where the page is silent (all listed in the design notes):
   * expert FFN: SwiGLU, h = silu(x W1^T) * (x W3^T), o = h W2^T;
   * bf16 round-to-nearest-even at h, o, y (forward) and at do, da, db,
     dx_perm, dx (backward); a and b are kept for the backward as bf16;
-  * loss L = sum(y * g); no auxiliary loss; the router bias is a constant.
+  * loss L = sum(y * g); no auxiliary loss; the router bias is a constant;
+  * shared expert (section "Introduction": the GPU multiplies the shared
+    expert while dispatch is in flight): a SwiGLU FFN that every token passes
+    through, its output s = bf16(h_s Ws2^T) added to the routed experts'
+    weighted sum with weight 1, y = bf16(s + sum_r w_r o_r); its backward
+    takes dy as the output gradient.
 
 Parity pins for every function live in tests/test_oracle.py.
 """
@@ -201,13 +206,14 @@ def expert_ffn(x_perm, offsets, W1, W3, W2, rounding=True):
 # the gate weights (section "Introduction"); the sum is taken at the token's
 # side (section "Dispatch and combine").
 # ----------------------------------------------------------------------------
-def combine(o, slot_row, w, T, R, rounding=True):
-    """y[t] = bf16( sum_{r=0..R-1} w[t,r] * o[slot_row[t*R+r]] ), summed in r order.
+def combine(o, slot_row, w, T, R, rounding=True, add=None):
+    """y[t] = bf16( add[t] + sum_{r=0..R-1} w[t,r] * o[slot_row[t*R+r]] ), summed in r order.
 
-    ``o`` holds float64 values; ``w`` None means unweighted (all ones).
+    ``o`` holds float64 values; ``w`` None means unweighted (all ones); ``add``
+    (the shared expert's output rows, [T, d]) None means zero.
     """
     o = np.asarray(o, dtype=np.float64)
-    y = np.zeros((T, o.shape[1]))
+    y = np.zeros((T, o.shape[1])) if add is None else np.array(add, dtype=np.float64)
     sr = np.asarray(slot_row).reshape(T, R)
     for r in range(R):
         wr = 1.0 if w is None else np.asarray(w, dtype=np.float64)[:, r:r + 1]
@@ -294,13 +300,23 @@ def dequantize_fp8_blocks(codes, scales):
 # ----------------------------------------------------------------------------
 # Whole layer.
 # ----------------------------------------------------------------------------
+def shared_expert_fwd(x, Ws1, Ws3, Ws2, rounding=True):
+    """The shared expert: the expert FFN with one expert holding every token,
+    rows in token order.  Returns (a, b, h, s) as ``expert_ffn`` does."""
+    T = np.asarray(x).shape[0]
+    offsets = np.array([0, T], dtype=np.int64)
+    return expert_ffn(x, offsets, np.asarray(Ws1)[None], np.asarray(Ws3)[None],
+                      np.asarray(Ws2)[None], rounding)
+
+
 def layer_fwd(x, w_gate, bias, W1, W3, W2, R, rounding=True,
-              forced_idx=None, forced_w=None):
+              forced_idx=None, forced_w=None, shared=None):
     """Forward pass of the MoE layer: route -> dispatch -> expert FFN -> combine.
 
     ``forced_idx``/``forced_w`` replace the router's choice (used to compare the
-    later stages with a GPU run whose routing is fixed).  Returns a dict of all
-    intermediates; bf16 tensors are float64 arrays holding bf16 values.
+    later stages with a GPU run whose routing is fixed).  ``shared`` = (Ws1,
+    Ws3, Ws2) adds a shared expert.  Returns a dict of all intermediates; bf16
+    tensors are float64 arrays holding bf16 values.
     """
     x = np.asarray(x)
     T = x.shape[0]
@@ -313,9 +329,15 @@ def layer_fwd(x, w_gate, bias, W1, W3, W2, R, rounding=True,
     counts, offsets, row_slot, slot_row = dispatch_plan(idx, E)
     x_perm = permute_rows(x, row_slot, R)
     a, b, h, o = expert_ffn(x_perm, offsets, W1, W3, W2, rounding)
-    y = combine(o, slot_row, w, T, R, rounding)
-    return dict(logits=logits, idx=idx, w=w, counts=counts, offsets=offsets,
-                row_slot=row_slot, slot_row=slot_row, x_perm=x_perm, a=a, b=b, h=h, o=o, y=y)
+    out = {}
+    s_out = None
+    if shared is not None:
+        sa, sb, sh, s_out = shared_expert_fwd(x, *shared, rounding=rounding)
+        out.update(sa=sa, sb=sb, sh=sh, s=s_out)
+    y = combine(o, slot_row, w, T, R, rounding, add=s_out)
+    out.update(logits=logits, idx=idx, w=w, counts=counts, offsets=offsets, row_slot=row_slot,
+               slot_row=slot_row, x_perm=x_perm, a=a, b=b, h=h, o=o, y=y)
+    return out
 
 
 def expert_bwd(x_rows, a, b, h, do, W1e, W3e, W2e, rounding=True):
@@ -342,7 +364,7 @@ def expert_bwd(x_rows, a, b, h, do, W1e, W3e, W2e, rounding=True):
                 dW2=do.T @ h, dW1=da.T @ x_rows, dW3=db.T @ x_rows)
 
 
-def layer_bwd(fwd, x, w_gate, W1, W3, W2, dy, R, rounding=True):
+def layer_bwd(fwd, x, w_gate, W1, W3, W2, dy, R, rounding=True, shared=None):
     """Backward pass for L = sum(y * g) with dy = g (bf16 bits or float64 values).
 
     Per token t and slot r (row = slot_row[t*R+r], expert e = idx[t,r]):
@@ -357,7 +379,9 @@ def layer_bwd(fwd, x, w_gate, W1, W3, W2, dy, R, rounding=True):
     Router (softmax over the chosen logits; unchosen logits get no gradient):
         dlogits[t, idx[t,q]] = w_q (dw_q - sum_r w_r dw_r)
         dW_g      = x^T dlogits
-        dx_t      = bf16( sum_r dx_perm[row(t,r)] + dlogits_t W_g^T )
+        dx_t      = bf16( sum_r dx_perm[row(t,r)] + dlogits_t W_g^T [+ dxs_t] )
+    Shared expert (``shared`` = (Ws1, Ws3, Ws2); its output gradient is dy):
+        dxs, dWs1, dWs3, dWs2 as ``expert_bwd`` over all T rows with do = dy.
     Returns dict with dx, dW_gate, dW1, dW3, dW2 (float64) and intermediates.
     """
     x = values(x)
@@ -404,9 +428,17 @@ def layer_bwd(fwd, x, w_gate, W1, W3, W2, dy, R, rounding=True):
     dx = np.zeros((T, d))
     for r in range(R):
         dx = dx + dx_perm[sr[:, r]]
-    dx = bf16_round(dx + dlogits @ wg.T, rounding)
-    return dict(dx=dx, dW_gate=dW_gate, dW1=dW1, dW3=dW3, dW2=dW2, dw=dw, do=do,
-                da=da, db=db, dx_perm=dx_perm, dlogits=dlogits)
+    dx = dx + dlogits @ wg.T
+    out = {}
+    if shared is not None:
+        sb_ = expert_bwd(x, fwd["sa"], fwd["sb"], fwd["sh"], dy, *shared, rounding=rounding)
+        dx = dx + sb_["dx_perm"]
+        out.update(dxs=sb_["dx_perm"], dWs1=sb_["dW1"], dWs3=sb_["dW3"], dWs2=sb_["dW2"],
+                   das=sb_["da"], dbs=sb_["db"])
+    dx = bf16_round(dx, rounding)
+    out.update(dx=dx, dW_gate=dW_gate, dW1=dW1, dW3=dW3, dW2=dW2, dw=dw, do=do, da=da, db=db,
+               dx_perm=dx_perm, dlogits=dlogits)
+    return out
 
 
 def loss(y, g):

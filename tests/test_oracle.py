@@ -367,6 +367,101 @@ def test_backward_rounding_points_applied():
         assert np.array_equal(bw[key], O.bf16_round(bw[key]))
 
 
+# ---------------------------------------------------------------- shared expert
+def _shared_weights(seed, d, fs):
+    r = _rng(seed)
+    return (r.standard_normal((fs, d)) * 0.4, r.standard_normal((fs, d)) * 0.4,
+            r.standard_normal((d, fs)) * 0.4)
+
+
+def test_shared_expert_is_an_extra_expert_every_token_takes_with_weight_one():
+    # Pinned against the routed path (itself pinned above): a shared expert is
+    # expert E of an (E+1)-expert layer that every token is forced onto with
+    # weight 1 next to its R routed experts.  Only the order of the fp64 sum
+    # differs (shared first vs last); the expert gradients are the same
+    # arithmetic.
+    x, wg, bias, W1, W3, W2, g, R = _tiny_layer(21, T=11, d=12, E=5, R=2, f=8)
+    Ws = _shared_weights(22, d=12, fs=6)
+    fw = O.layer_fwd(x, wg, bias, W1, W3, W2, R, rounding=False, shared=Ws)
+    T, E = x.shape[0], W1.shape[0]
+    fs, f = Ws[0].shape[0], W1.shape[1]
+    # widen both to a common hidden size (zero rows / columns add nothing)
+    k = max(f, fs)
+    def widen(W, axis):
+        pad_w = [(0, 0)] * W.ndim
+        pad_w[axis] = (0, k - W.shape[axis])
+        return np.pad(W, pad_w)
+    W1x = np.concatenate([widen(W1, 1), widen(Ws[0], 0)[None]])
+    W3x = np.concatenate([widen(W3, 1), widen(Ws[1], 0)[None]])
+    W2x = np.concatenate([widen(W2, 2), widen(Ws[2], 1)[None]])
+    idx = np.concatenate([fw["idx"], np.full((T, 1), E, np.int32)], axis=1)
+    w = np.concatenate([fw["w"].astype(np.float64), np.ones((T, 1))], axis=1)
+    ext = O.layer_fwd(x, np.zeros((12, E + 1)), None, W1x, W3x, W2x, R + 1, rounding=False,
+                      forced_idx=idx, forced_w=w)
+    np.testing.assert_allclose(fw["y"], ext["y"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(fw["s"], ext["o"][ext["offsets"][E]:ext["offsets"][E + 1]],
+                               rtol=1e-13, atol=1e-13)
+    bw = O.layer_bwd(fw, x, wg, W1, W3, W2, g, R, rounding=False, shared=Ws)
+    bx = O.layer_bwd(ext, x, np.zeros((12, E + 1)), W1x, W3x, W2x, g, R + 1, rounding=False)
+    np.testing.assert_allclose(bw["dWs1"], bx["dW1"][E][:fs], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(bw["dWs3"], bx["dW3"][E][:fs], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(bw["dWs2"], bx["dW2"][E][:, :fs], rtol=1e-12, atol=1e-12)
+
+
+def test_shared_expert_backward_matches_torch_autograd():
+    x, wg, bias, W1, W3, W2, g, R = _tiny_layer(23, T=9, d=10, E=5, R=3, f=7)
+    Ws = _shared_weights(24, d=10, fs=5)
+    fw = O.layer_fwd(x, wg, bias, W1, W3, W2, R, rounding=False, shared=Ws)
+    bw = O.layer_bwd(fw, x, wg, W1, W3, W2, g, R, rounding=False, shared=Ws)
+    idx = torch.tensor(fw["idx"], dtype=torch.int64)
+    tx, twg = torch.tensor(x, requires_grad=True), torch.tensor(wg, requires_grad=True)
+    tW1, tW3, tW2 = (torch.tensor(a, requires_grad=True) for a in (W1, W3, W2))
+    tS1, tS3, tS2 = (torch.tensor(a, requires_grad=True) for a in Ws)
+    logits = tx @ twg + torch.tensor(bias)
+    wsel = torch.softmax(torch.gather(logits, 1, idx), dim=1)
+    silu = torch.nn.functional.silu
+    y = (silu(tx @ tS1.T) * (tx @ tS3.T)) @ tS2.T
+    for q in range(R):
+        e = idx[:, q]
+        a = torch.einsum("td,tfd->tf", tx, tW1[e])
+        b = torch.einsum("td,tfd->tf", tx, tW3[e])
+        o = torch.einsum("tf,tdf->td", silu(a) * b, tW2[e])
+        y = y + wsel[:, q:q + 1] * o
+    np.testing.assert_allclose(fw["y"], y.detach().numpy(), rtol=1e-10, atol=1e-12)
+    (y * torch.tensor(g)).sum().backward()
+    for got, t in ((bw["dx"], tx), (bw["dW_gate"], twg), (bw["dW1"], tW1), (bw["dW3"], tW3),
+                   (bw["dW2"], tW2), (bw["dWs1"], tS1), (bw["dWs3"], tS3), (bw["dWs2"], tS2)):
+        np.testing.assert_allclose(got, t.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_shared_expert_finite_differences_and_rounding_points():
+    x, wg, bias, W1, W3, W2, g, R = _tiny_layer(25)
+    Ws = _shared_weights(26, d=x.shape[1], fs=4)
+    fw = O.layer_fwd(x, wg, bias, W1, W3, W2, R, rounding=False, shared=Ws)
+    bw = O.layer_bwd(fw, x, wg, W1, W3, W2, g, R, rounding=False, shared=Ws)
+    r = _rng(27)
+    eps = 1e-6
+    for i, key in enumerate(("dWs1", "dWs3", "dWs2")):
+        v = r.standard_normal(Ws[i].shape)
+        Lpm = []
+        for sgn in (1, -1):
+            Wp = list(Ws)
+            Wp[i] = Ws[i] + sgn * eps * v
+            f2 = O.layer_fwd(x, wg, bias, W1, W3, W2, R, rounding=False, shared=tuple(Wp))
+            Lpm.append(O.loss(f2["y"], g))
+        fd = (Lpm[0] - Lpm[1]) / (2 * eps)
+        an = float(np.sum(bw[key] * v))
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (key, fd, an)
+    # rounding on: the shared expert's storage points hold bf16 values
+    xb = O.bf16_round(x)
+    fw = O.layer_fwd(xb, wg, bias, W1, W3, W2, R, shared=Ws)
+    bw = O.layer_bwd(fw, xb, wg, W1, W3, W2, O.bf16_round(g), R, shared=Ws)
+    for key in ("sh", "s", "y"):
+        assert np.array_equal(fw[key], O.bf16_round(fw[key]))
+    for key in ("dxs", "das", "dbs", "dx"):
+        assert np.array_equal(bw[key], O.bf16_round(bw[key]))
+
+
 # ---------------------------------------------------------------- fp8 (E4M3) dispatch
 def test_e4m3_decode_definition_cases():
     cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
