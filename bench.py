@@ -353,7 +353,7 @@ def run_ours(args, rank, world, device):
         ran = ("gate", "topk", "dispatch", "gateup", "down", "combine", "shared_fwd")
     stages = {}
     for name, ms in stage_ms.items():
-        if name not in ran or ms <= 0:
+        if name not in ran or name not in work or ms <= 0:
             continue
         kind, amount = work[name]
         if kind == "tflop":
@@ -410,42 +410,78 @@ def run_ours(args, rank, world, device):
             summary[f"{n}_frac_of_hbm"] = stages[n]["frac"]
 
     # ---- end to end through the public API with host buffers
+    # Every step copies its inputs in from pinned host memory and its results
+    # out to pinned host memory, all inside the timed region.  As a caller
+    # would, the copies run on two copy streams with double-buffered device
+    # copies, so step k+1's inputs upload and step k's results download while
+    # the layer computes.
     e2e = None
     if not args.no_e2e:
         pin_in = {n: t.detach().cpu().pin_memory() for n, t in host_in}
         pin_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in host_out}
-        dev_in = {n: torch.empty_like(t) for n, t in host_in}
-        dev_out = {n: torch.empty_like(t) for n, t in host_out}
+        dev_in = [{n: torch.empty_like(t) for n, t in host_in} for _ in range(2)]
+        dev_out = [{n: torch.empty_like(t) for n, t in host_out} for _ in range(2)]
         bi = sum(t.numel() * t.element_size() for t in pin_in.values())
         bo = sum(t.numel() * t.element_size() for t in pin_out.values())
+        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
 
-        def e2e_step():
-            for n, t in pin_in.items():
-                dev_in[n].copy_(t, non_blocking=True)
-            if identity:
-                step(xin=dev_in["x"], yout=dev_out["y"])
-            elif train:
-                step(xin=dev_in["x"], yout=dev_out["y"], gin=dev_in["g"], dxout=dev_out["dx"])
-            else:
-                step(xin=dev_in["x"], yout=dev_out["y"])
-            for n, t in pin_out.items():
-                t.copy_(dev_out[n], non_blocking=True)
+        def ev():
+            return torch.cuda.Event()
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
-        torch.cuda.synchronize()
+        def run_e2e(n_steps):
+            in_ready, comp_done, out_done = [None, None], [None, None], [None, None]
+
+            def upload(k):
+                b = k % 2
+                with torch.cuda.stream(h2d_s):
+                    if comp_done[b] is not None:      # step k-2 has finished reading it
+                        h2d_s.wait_event(comp_done[b])
+                    for n, t in pin_in.items():
+                        dev_in[b][n].copy_(t, non_blocking=True)
+                    in_ready[b] = ev()
+                    in_ready[b].record(h2d_s)
+
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            h2d_s.wait_event(t0)
+            d2h_s.wait_event(t0)
+            upload(0)
+            for k in range(n_steps):
+                b = k % 2
+                if k + 1 < n_steps:
+                    upload(k + 1)
+                stream.wait_event(in_ready[b])
+                if out_done[b] is not None:           # step k-2's results are downloaded
+                    stream.wait_event(out_done[b])
+                di, do = dev_in[b], dev_out[b]
+                if identity or not train:
+                    step(xin=di["x"], yout=do["y"])
+                else:
+                    step(xin=di["x"], yout=do["y"], gin=di["g"], dxout=do["dx"])
+                comp_done[b] = ev()
+                comp_done[b].record(stream)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(comp_done[b])
+                    for n, t in pin_out.items():
+                        t.copy_(do[n], non_blocking=True)
+                    out_done[b] = ev()
+                    out_done[b].record(d2h_s)
+            for e in out_done:
+                if e is not None:
+                    stream.wait_event(e)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1)
+
+        run_e2e(max(1, args.warmup))
         world_barrier(world)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ems = world_max(e0.elapsed_time(e1), world, device)
+        ems = world_max(run_e2e(args.steps), world, device)
         e2e = {"value": round(job_tokens_per_s(tokens_per_step, world, args.steps, ems), 1),
                "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "ms_per_step": round(ems / args.steps, 4)}
+               "ms_per_step": round(ems / args.steps, 4),
+               "copies": "pinned host <-> device on two copy streams, double-buffered, "
+                         "overlapping the layer's compute"}
 
     result = {
         "metric": METRIC,
