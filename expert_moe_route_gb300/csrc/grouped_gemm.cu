@@ -719,47 +719,73 @@ __global__ void prepack_kernel(const uint16_t* __restrict__ W, long long rows, i
   }
 }
 
-// Ragged M tiles: expert e's rows [offsets[e], offsets[e+1]) split into
-// tile_rows-row tiles (128, or 256 for the paired modes); tiles[i] = {first row,
-// expert}, ordered by expert then row.
-__global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
-                                                           int E, int tile_rows,
-                                                           int2* __restrict__ tiles,
-                                                           int32_t* __restrict__ tile_count) {
-  __shared__ int warp_sums[32];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  int carry = 0;
-  for (int e0 = 0; e0 < E; e0 += 1024) {
-    const int e = e0 + tid;
-    int r0 = 0, n = 0;
-    if (e < E) {
-      r0 = offsets[e];
-      n = ceil_div(offsets[e + 1] - r0, tile_rows);
-    }
-    int incl = n;
+// Exclusive prefix sum of v over the block's 1024 threads; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int ws = warp_sums[lane];
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(kFull, incl, off);
-      if (lane >= off) incl += o;
+      const int o = __shfl_up_sync(kFull, ws, off);
+      if (lane >= off) ws += o;
     }
-    if (lane == 31) warp_sums[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      int ws = warp_sums[lane];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(kFull, ws, off);
-        if (lane >= off) ws += o;
-      }
-      warp_sums[lane] = ws;
-    }
-    __syncthreads();
-    const int start = carry + (wid > 0 ? warp_sums[wid - 1] : 0) + incl - n;
-    for (int i = 0; i < n; ++i) tiles[start + i] = make_int2(r0 + i * tile_rows, e);
-    carry += warp_sums[31];
-    __syncthreads();
+    warp_sums[lane] = ws;
   }
-  if (tid == 0) *tile_count = carry;
+  __syncthreads();
+  const int excl = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - v;
+  *total = warp_sums[31];
+  __syncthreads();
+  return excl;
+}
+
+// Ragged M tiles: expert e's rows [offsets[e], offsets[e+1]) split into
+// tile_rows-row tiles (128, or 256 for CTA pairs and the paired modes);
+// tiles[i] = {first row, expert}, ordered by expert then row.  With
+// tail_rows > 0, an expert's last tile goes to the second list `tails`
+// instead when it holds at most tail_rows rows (the single-CTA kernels run
+// those tiles: on a pair the other CTA would load and multiply a whole tile
+// of rows that are not the expert's).
+__global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
+                                                           int E, int tile_rows, int tail_rows,
+                                                           int2* __restrict__ tiles,
+                                                           int32_t* __restrict__ tile_count,
+                                                           int2* __restrict__ tails,
+                                                           int32_t* __restrict__ tail_count) {
+  __shared__ int warp_sums[32];
+  int carry = 0, carry_t = 0;
+  for (int e0 = 0; e0 < E; e0 += 1024) {
+    const int e = e0 + threadIdx.x;
+    int r0 = 0, n = 0, nt = 0;
+    if (e < E) {
+      r0 = offsets[e];
+      const int rows = offsets[e + 1] - r0;
+      n = ceil_div(rows, tile_rows);
+      const int rem = rows % tile_rows;
+      if (tail_rows > 0 && rem > 0 && rem <= tail_rows) {
+        n -= 1;
+        nt = 1;
+      }
+    }
+    int tot = 0, tot_t = 0;
+    const int start = carry + block_exclusive_scan(n, warp_sums, &tot);
+    const int start_t = carry_t + block_exclusive_scan(nt, warp_sums, &tot_t);
+    for (int i = 0; i < n; ++i) tiles[start + i] = make_int2(r0 + i * tile_rows, e);
+    if (nt) tails[start_t] = make_int2(r0 + n * tile_rows, e);
+    carry += tot;
+    carry_t += tot_t;
+  }
+  if (threadIdx.x == 0) {
+    *tile_count = carry;
+    if (tail_count) *tail_count = carry_t;
+  }
 }
 }  // namespace
 
@@ -914,15 +940,32 @@ cudaError_t launch_prepack(const uint16_t* W1, const uint16_t* W3, const uint16_
   return cudaGetLastError();
 }
 
+// Tile-list workspace: [tile count, tail count | E tail entries | tiles].
 size_t tiles_ws_bytes(int N, int E) {
-  return align_up(sizeof(int2) * ((size_t)ceil_div(N, BM) + E) + 16, 256);
+  return align_up(16 + sizeof(int2) * ((size_t)E + ceil_div(N, BM) + E), 256);
+}
+
+struct TileLists {
+  const int32_t* count;
+  const int2* tiles;
+  const int32_t* tail_count;
+  const int2* tails;
+};
+
+TileLists tile_lists(void* ws, int E) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  return {reinterpret_cast<const int32_t*>(b), reinterpret_cast<const int2*>(b + 16 + 8 * (size_t)E),
+          reinterpret_cast<const int32_t*>(b + 4), reinterpret_cast<const int2*>(b + 16)};
 }
 
 cudaError_t launch_build_tiles(const int32_t* offsets, int E, void* ws, cudaStream_t s,
-                               int tile_rows = BM) {
-  int32_t* count = static_cast<int32_t*>(ws);
-  int2* tiles = reinterpret_cast<int2*>(static_cast<uint8_t*>(ws) + 16);
-  build_tiles_kernel<<<1, 1024, 0, s>>>(offsets, E, tile_rows, tiles, count);
+                               int tile_rows = BM, int tail_rows = 0) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(offsets, E, tile_rows, tail_rows,
+                                        reinterpret_cast<int2*>(b + 16 + 8 * (size_t)E),
+                                        reinterpret_cast<int32_t*>(b),
+                                        reinterpret_cast<int2*>(b + 16),
+                                        reinterpret_cast<int32_t*>(b + 4));
   count_launches(1);
   return cudaGetLastError();
 }
@@ -940,15 +983,28 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   // a 256-row block to share each weight tile (GATEUP2 / DOWN2).
   const bool pair = !cta_pairs && (long long)N <= 2LL * BM * E;
   const int tile_rows = (pair || cta_pairs) ? 2 * BM : BM;
+  // On pairs with few rows per expert (on average at most one 256-row tile),
+  // an expert's last tile of at most 128 rows runs on one CTA after the pairs
+  // (measured: it pays there; with more rows per expert the extra launch costs
+  // more than the tails' second CTA).
+  const bool split_tails = cta_pairs && (long long)N <= 2LL * BM * E;
   trace_begin(MOE_STAGE_GATEUP, s);
-  cudaError_t e = launch_build_tiles(offsets, E, tiles_ws, s, tile_rows);
+  cudaError_t e = launch_build_tiles(offsets, E, tiles_ws, s, tile_rows, split_tails ? BM : 0);
   if (e != cudaSuccess) return e;
+  const TileLists tl = tile_lists(tiles_ws, E);
   GemmArgs g{};
   g.E = E; g.N = N; g.d = d; g.f = f;
   g.offsets = offsets;
-  g.tile_count = static_cast<const int32_t*>(tiles_ws);
-  g.tiles = reinterpret_cast<const int2*>(static_cast<const uint8_t*>(tiles_ws) + 16);
+  g.tile_count = tl.count;
+  g.tiles = tl.tiles;
   g.err = err;
+  GemmArgs gt = g;   // the tails' launch: one CTA per 128-row tile
+  auto tails = [&](GemmArgs& gg) {
+    gg = g;
+    gg.tile_count = tl.tail_count;
+    gg.tiles = tl.tails;
+    return (long long)E * g.n_tiles_n;
+  };
   const long long max_m_tiles = ceil_div(N, tile_rows) + E;
   CUtensorMap ma, mb, mb2;
   // gate-up: A = x_perm, B = W1 / W3 rows (128 per tile each)
@@ -973,6 +1029,11 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   e = cta_pairs ? launch_mode<GATEUP, true>(ma, mb, mb2, mh, msa, msb, g, items, s)
       : pair    ? launch_mode<GATEUP2>(ma, mb, mb2, mh, msa, msb, g, items, s)
                 : launch_mode<GATEUP>(ma, mb, mb2, mh, msa, msb, g, items, s);
+  if (e == cudaSuccess && split_tails) {
+    // one CTA loads a whole 128-row W1 and W3 tile: the same maps as the pairs
+    const long long n = tails(gt);
+    e = launch_mode<GATEUP>(ma, mb, mb2, mh, msa, msb, gt, n, s);
+  }
   trace_end(MOE_STAGE_GATEUP, s);
   if (e != cudaSuccess) return e;
   // down: A = h, B = W2 rows (256 per tile; each CTA of a pair loads 128)
@@ -992,6 +1053,15 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   e = cta_pairs ? launch_mode<DOWN, true>(ma, mb, mb, mo, mo, mo, g, items_down, s)
       : pair    ? launch_mode<DOWN2>(ma, mb, mb, mo, mo, mo, g, items_down, s)
                 : launch_mode<DOWN>(ma, mb, mb, mo, mo, mo, g, items_down, s);
+  if (e == cudaSuccess && split_tails) {
+    // the tails' CTA loads all 256 W2 rows of a column tile
+    CUtensorMap mb_full;
+    if (prepacked ? !make_map_tiles(&mb_full, W2, (long long)E * d / BN, f / 64, BN, BN)
+                  : !make_map(&mb_full, W2, (long long)E * d, f, BN))
+      return cudaErrorInvalidValue;
+    const long long n = tails(gt);
+    e = launch_mode<DOWN>(ma, mb_full, mb_full, mo, mo, mo, gt, n, s);
+  }
   trace_end(MOE_STAGE_DOWN, s);
   return e;
 }
@@ -1008,13 +1078,22 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
   GemmArgs g{};
   g.E = E; g.N = N; g.d = d; g.f = f;
   g.offsets = offsets;
-  g.tile_count = static_cast<const int32_t*>(tiles_ws);
-  g.tiles = reinterpret_cast<const int2*>(static_cast<const uint8_t*>(tiles_ws) + 16);
+  const TileLists tl = tile_lists(tiles_ws, E);
+  g.tile_count = tl.count;
+  g.tiles = tl.tiles;
   g.err = err;
+  GemmArgs gt;   // the tails' launches (pairs): one CTA per tile of at most 128 rows
+  auto tails = [&]() {
+    gt = g;
+    gt.tile_count = tl.tail_count;
+    gt.tiles = tl.tails;
+    return (long long)E * g.n_tiles_n;
+  };
   CUtensorMap ma, mb, mb2;
+  const bool split_tails = cta_pairs && (long long)N <= 2LL * BM * E;   // as in the forward
   if (N > 0) {
     trace_begin(MOE_STAGE_BWD_DH, s);
-    e = launch_build_tiles(offsets, E, tiles_ws, s, tile_m);
+    e = launch_build_tiles(offsets, E, tiles_ws, s, tile_m, split_tails ? BM : 0);
     if (e != cudaSuccess) return e;
     const long long max_m_tiles = ceil_div(N, tile_m) + E;
     // dh = do W2[e] (B MN-major: W2 viewed [E*d, f]); epilogue -> dab = [da | db]
@@ -1027,6 +1106,10 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
     if (!make_map(&mo, dab, N, 2LL * f, 32)) return cudaErrorInvalidValue;
     e = cta_pairs ? launch_mode<DH, true>(ma, mb, mb, mo, mo, mo, g, max_m_tiles * g.n_tiles_n, s)
                   : launch_mode<DH>(ma, mb, mb, mo, mo, mo, g, max_m_tiles * g.n_tiles_n, s);
+    if (e == cudaSuccess && split_tails) {
+      const long long n = tails();
+      e = launch_mode<DH>(ma, mb, mb, mo, mo, mo, gt, n, s);
+    }
     trace_end(MOE_STAGE_BWD_DH, s);
     if (e != cudaSuccess) return e;
     // dx_perm = [da | db] [W1[e]; W3[e]] (B MN-major: W1, W3 viewed [E*f, d])
@@ -1040,6 +1123,10 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
     trace_begin(MOE_STAGE_BWD_DX, s);
     e = cta_pairs ? launch_mode<DX, true>(ma, mb, mb2, mo, mo, mo, g, max_m_tiles * g.n_tiles_n, s)
                   : launch_mode<DX>(ma, mb, mb2, mo, mo, mo, g, max_m_tiles * g.n_tiles_n, s);
+    if (e == cudaSuccess && split_tails) {
+      const long long n = tails();
+      e = launch_mode<DX>(ma, mb, mb2, mo, mo, mo, gt, n, s);
+    }
     trace_end(MOE_STAGE_BWD_DX, s);
     if (e != cudaSuccess) return e;
   }
