@@ -162,7 +162,9 @@ def stage_work(wl, fp8=False, shared_fs=0):
             "bwd_dx": ("tflop", 4.0 * N * d * f),
             "bwd_wg2": ("tflop", 2.0 * N * d * f),
             "bwd_wg13": ("tflop", 4.0 * N * d * f),
-            "bwd_dwg": ("gb", 2.0 * N * d + 4.0 * N + 4.0 * d * E),
+            # x once (its rows are gathered through row_slot, the R reads of a
+            # row mostly from L2), row_slot and dsel per row, dW_g written
+            "bwd_dwg": ("gb", 2.0 * T * d + 8.0 * N + 4.0 * d * E),
             "bwd_dxc": ("gb", 2.0 * N * d + 2.0 * T * d + 8.0 * E * d),
         })
     if f and shared_fs:

@@ -550,7 +550,7 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
   }
   if (!sv || !x || !dy || !dx) return MOE_ERR_INVALID_ARG;
   if (!sv->a || !sv->b || !sv->h || !sv->o || !sv->x_perm || !sv->topk_idx || !sv->topk_w ||
-      !sv->offsets || !sv->slot_row)
+      !sv->offsets || !sv->slot_row || !sv->row_slot)
     return MOE_ERR_INVALID_ARG;
   if (SH && (!sv->sa || !sv->sb || !sv->sh)) return MOE_ERR_INVALID_ARG;
   const void* ps[] = {x, dy, dx, dW_gate, dW1, dW3, dW2, sv->a, sv->b, sv->h, sv->o, sv->x_perm};
@@ -615,7 +615,7 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
                          sv->h, dO, dab, dxp, dW1, dW3, dW2, tws, err, pairs, s));
   {
     Stage st_(s, MOE_STAGE_BWD_DWG);
-    MOE_TRY(launch_dwg(sv->x_perm, sv->offsets, dsel_row, d, E, dW_gate, dwg_ws, s));
+    MOE_TRY(launch_dwg(x, sv->row_slot, R, sv->offsets, dsel_row, d, E, dW_gate, dwg_ws, s));
   }
   if (SH && !side) MOE_TRY(shared_bwd());
   if (side) MOE_TRY(join.now());

@@ -115,9 +115,15 @@ __global__ void wg_transpose_kernel(const float* __restrict__ wg, int d, int E,
 // partials in s order and writes dW_g transposed through shared memory.
 constexpr int DWG_THREADS = 128;
 constexpr int DWG_SPLIT = 4;
+// dW_g column e, split over DWG_SPLIT row ranges: sum over the expert's rows of
+// dsel_row[row] * x[token(row)].  The rows are read from x through row_slot
+// (x_perm[row] == x[row_slot[row] / R]): every expert walks its tokens in
+// ascending order, so the R reads of a token's row come close together and
+// mostly hit L2 -- x (T*d) is read from HBM about once instead of x_perm (N*d).
 __global__ void __launch_bounds__(DWG_THREADS) dwg_partial_kernel(
-    const uint16_t* __restrict__ x_perm, const int32_t* __restrict__ offsets,
-    const float* __restrict__ dsel_row, int d, int E, float* __restrict__ part) {
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ row_slot, int R,
+    const int32_t* __restrict__ offsets, const float* __restrict__ dsel_row, int d, int E,
+    float* __restrict__ part) {
   const int e = blockIdx.y, sp = blockIdx.z;
   const int k0 = (blockIdx.x * DWG_THREADS + threadIdx.x) * 8;
   if (k0 >= d) return;
@@ -131,7 +137,7 @@ __global__ void __launch_bounds__(DWG_THREADS) dwg_partial_kernel(
     float s[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      q[u] = ldg_nc_v4(x_perm + (size_t)(row + u) * d + k0);
+      q[u] = ldg_nc_v4(x + (size_t)(row_slot[row + u] / R) * d + k0);
       s[u] = dsel_row[row + u];
     }
 #pragma unroll
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(DWG_THREADS) dwg_partial_kernel(
   }
   for (; row < r1; ++row) {
     float xv[8];
-    unpack8(ldg_nc_v4(x_perm + (size_t)row * d + k0), xv);
+    unpack8(ldg_nc_v4(x + (size_t)(row_slot[row] / R) * d + k0), xv);
     const float s = dsel_row[row];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = fmaf(s, xv[j], acc[j]);
@@ -273,11 +279,12 @@ cudaError_t launch_wg_transpose(const float* wg, int d, int E, float* wgT, cudaS
 
 size_t dwg_ws_bytes(int d, int E) { return align_up((size_t)DWG_SPLIT * E * d * 4, 256); }
 
-cudaError_t launch_dwg(const uint16_t* x_perm, const int32_t* offsets, const float* dsel_row,
-                       int d, int E, float* dW_gate, void* ws, cudaStream_t s) {
+cudaError_t launch_dwg(const uint16_t* x, const int32_t* row_slot, int R, const int32_t* offsets,
+                       const float* dsel_row, int d, int E, float* dW_gate, void* ws,
+                       cudaStream_t s) {
   float* part = static_cast<float*>(ws);
   dim3 grid(ceil_div(d, DWG_THREADS * 8), E, DWG_SPLIT);
-  dwg_partial_kernel<<<grid, DWG_THREADS, 0, s>>>(x_perm, offsets, dsel_row, d, E, part);
+  dwg_partial_kernel<<<grid, DWG_THREADS, 0, s>>>(x, row_slot, R, offsets, dsel_row, d, E, part);
   dwg_reduce_kernel<<<dim3(ceil_div(d, 32), ceil_div(E, 32)), dim3(32, 8), 0, s>>>(part, d, E,
                                                                                   dW_gate);
   count_launches(2);

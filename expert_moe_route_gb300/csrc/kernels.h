@@ -93,8 +93,9 @@ cudaError_t launch_bwd_route(const uint16_t* dy, const uint16_t* o, const int32_
                              float* dsel_row, cudaStream_t s);
 cudaError_t launch_wg_transpose(const float* wg, int d, int E, float* wgT, cudaStream_t s);
 size_t dwg_ws_bytes(int d, int E);
-cudaError_t launch_dwg(const uint16_t* x_perm, const int32_t* offsets, const float* dsel_row,
-                       int d, int E, float* dW_gate, void* ws, cudaStream_t s);
+cudaError_t launch_dwg(const uint16_t* x, const int32_t* row_slot, int R, const int32_t* offsets,
+                       const float* dsel_row, int d, int E, float* dW_gate, void* ws,
+                       cudaStream_t s);
 cudaError_t launch_dx_combine(const uint16_t* dx_perm, const int32_t* slot_row,
                               const int32_t* idx, const float* dsel_tok, const float* wgT, int T,
                               int d, int E, int R, uint16_t* dx, cudaStream_t s,
