@@ -93,7 +93,7 @@ def _declare(lib):
     lib.moe_prepack_weights.argtypes = [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]
     lib.moe_grouped_ffn.restype = _i
     lib.moe_grouped_ffn.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                    _vp, _szp, _u, _vp]
+                                    _vp, _vp, _szp, _u, _vp]
     lib.moe_combine.restype = _i
     lib.moe_combine.argtypes = [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]
     lib.moe_layer_fwd.restype = _i
@@ -234,22 +234,23 @@ def moe_dequant_fp8(xq, xscale, out, stream=None):
 def grouped_ffn_ws_bytes(N, d, f, E) -> int:
     n = ctypes.c_size_t(0)
     _check(lib().moe_grouped_ffn(None, None, N, d, f, E, None, None, None, None, None, None, None,
-                                 None, ctypes.byref(n), 0, None), "moe_grouped_ffn(ws query)")
+                                 None, None, ctypes.byref(n), 0, None), "moe_grouped_ffn(ws query)")
     return n.value
 
 
 def moe_grouped_ffn(x_perm, offsets, W1, W3, W2, h, out, ws, a_save=None, b_save=None, flags=0,
-                    stream=None):
+                    stream=None, row_scale=None):
     N, d = x_perm.shape
     E, f, _ = W1.shape
     for name, t in (("x_perm", x_perm), ("W1", W1), ("W3", W3), ("W2", W2), ("h", h),
                     ("out", out), ("a_save", a_save), ("b_save", b_save)):
         _dt(t, torch.bfloat16, name)
     _dt(offsets, torch.int32, "offsets")
+    _dt(row_scale, torch.float32, "row_scale")
     n = ctypes.c_size_t(ws.numel())
     st = lib().moe_grouped_ffn(_p(x_perm), _p(offsets), N, d, f, E, _p(W1), _p(W3), _p(W2),
-                               _p(a_save), _p(b_save), _p(h), _p(out), _p(ws), ctypes.byref(n),
-                               flags, _stream(stream))
+                               _p(row_scale), _p(a_save), _p(b_save), _p(h), _p(out), _p(ws),
+                               ctypes.byref(n), flags, _stream(stream))
     _check(st, "moe_grouped_ffn")
 
 

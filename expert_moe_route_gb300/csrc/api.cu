@@ -316,8 +316,9 @@ moe_status_t moe_dequant_fp8(const uint8_t* xq, const float* xscale, int N, int 
 
 moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
                              int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
-                             uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
-                             void* ws, size_t* ws_bytes, unsigned flags, moe_stream_t stream) {
+                             const float* row_scale, uint16_t* a_save, uint16_t* b_save,
+                             uint16_t* h, uint16_t* out, void* ws, size_t* ws_bytes,
+                             unsigned flags, moe_stream_t stream) {
   if (N < 0 || d <= 0 || f <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
   if (d % 8 || f % 8 || E > 1024) return MOE_ERR_UNSUPPORTED;
   if ((flags & MOE_WEIGHTS_PREPACKED) && !prepack_supported(d, f)) return MOE_ERR_UNSUPPORTED;
@@ -341,7 +342,7 @@ moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int
   cudaError_t e = launch_ffn_fwd(x_perm, offsets, N, d, f, E, W1, W3, W2, a_save, b_save, h, out,
                                  static_cast<uint8_t*>(ws) + kErrBytes, err,
                                  (flags & MOE_WEIGHTS_PREPACKED) != 0,
-                                 !(flags & MOE_SINGLE_CTA_TILES), s);
+                                 !(flags & MOE_SINGLE_CTA_TILES), s, row_scale);
   return finish(e, err, flags, s);
 }
 

@@ -536,6 +536,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
           for (int k = 0; k < 4; ++k) tmem_ld16(t_row + c0 + 16 * k, v + 16 * k);
           tmem_ld_wait();
+          if (Tr::is_down && g.row_scale) {   // this lane's row's scale, before rounding
+            const float sc = g.row_scale[grow0 + lane];
+#pragma unroll
+            for (int u = 0; u < 64; ++u) v[u] *= sc;
+          }
           stage_begin();
 #pragma unroll
           for (int k = 0; k < 8; ++k) stage_put(k, pack8(v + 8 * k));
@@ -549,7 +554,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           tmem_ld16(t_row + c, v);
           tmem_ld_wait();
           const int col = it.nt * BN + c;
-          if (valid && col < g.d) store_bf16x16(g.out_bf16 + (size_t)row * g.d + col, v, g.d - col);
+          if (valid && col < g.d) {
+            if (Tr::is_down && g.row_scale) {
+              const float sc = g.row_scale[row];
+#pragma unroll
+              for (int u = 0; u < 16; ++u) v[u] *= sc;
+            }
+            store_bf16x16(g.out_bf16 + (size_t)row * g.d + col, v, g.d - col);
+          }
         }
       } else if (MODE == DH) {
         const int row = it.row0 + rrow + r_local;
@@ -975,7 +987,7 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
                            void* tiles_ws, int* err, bool prepacked, bool cta_pairs,
-                           cudaStream_t s) {
+                           cudaStream_t s, const float* row_scale) {
   if (N == 0) return cudaSuccess;
   // cta_pairs: 256-row tiles on CTA pairs (tcgen05 .cta_group::2).  Otherwise
   // single-CTA tiles; with few rows per expert (on average at most two 128-row
@@ -1045,6 +1057,7 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   g.kblocks = ceil_div(f, BK);
   g.n_tiles_n = ceil_div(d, BN);
   g.out_bf16 = out; g.save_a = g.save_b = nullptr;
+  g.row_scale = row_scale;
   CUtensorMap mo;
   if (!make_map(&mo, out, N, d, 32)) return cudaErrorInvalidValue;
 

@@ -207,16 +207,20 @@ moe_status_t moe_dequant_fp8(const uint8_t* xq, const float* xscale, int N, int 
  * e and row i in [offsets[e], offsets[e+1]):
  *   a = x_perm[i] W1[e]^T,  b = x_perm[i] W3[e]^T      (fp32 accumulation)
  *   h[i]   = bf16(silu(a) * b),   silu(a) = a / (1 + exp(-a))
- *   out[i] = bf16(h[i] W2[e]^T)
+ *   out[i] = bf16(s_i * (h[i] W2[e]^T)),   s_i = row_scale[i], or 1 when row_scale is NULL
  * x_perm: bf16 [N,d]; offsets: int32 [E+1] on the device with offsets[E] == N;
- * W1, W3: bf16 [E,f,d]; W2: bf16 [E,d,f]; h: bf16 [N,f] (written, kept for the
- * backward); a_save, b_save: bf16 [N,f] or NULL (bf16(a), bf16(b) for the
+ * W1, W3: bf16 [E,f,d]; W2: bf16 [E,d,f]; row_scale: fp32 [N] or NULL -- e.g.
+ * each row's gate weight, so that an unweighted moe_combine (topk_w NULL) of
+ * the outputs sums already-weighted rows (the weighting moved to the expert
+ * side, before the output's bf16 rounding); h: bf16 [N,f] (written, kept for
+ * the backward); a_save, b_save: bf16 [N,f] or NULL (bf16(a), bf16(b) for the
  * backward); out: bf16 [N,d].  Needs a workspace (tile list, error word).
  */
 moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
                              int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
-                             uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
-                             void* ws, size_t* ws_bytes, unsigned flags, moe_stream_t stream);
+                             const float* row_scale, uint16_t* a_save, uint16_t* b_save,
+                             uint16_t* h, uint16_t* out, void* ws, size_t* ws_bytes,
+                             unsigned flags, moe_stream_t stream);
 
 /*
  * moe_prepack_weights -- copy the expert weights into the tile layout the

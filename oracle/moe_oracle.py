@@ -169,12 +169,15 @@ def silu(a):
     return a / (1.0 + np.exp(-a))
 
 
-def expert_ffn(x_perm, offsets, W1, W3, W2, rounding=True):
+def expert_ffn(x_perm, offsets, W1, W3, W2, rounding=True, row_scale=None):
     """Per expert e over rows offsets[e]..offsets[e+1]-1 of x_perm:
 
         a = x W1[e]^T, b = x W3[e]^T      (float64)
         h = bf16(silu(a) * b)
-        o = bf16(h W2[e]^T)
+        o = bf16(s * (h W2[e]^T))         s = row_scale[row] (1 when None)
+
+    ``row_scale`` weights each output row before its rounding (e.g. by the
+    row's gate weight, so that an unweighted combine sums weighted rows).
 
     W1, W3: [E, f, d]; W2: [E, d, f] (bf16 bit patterns or float64 values; an
     expert's weights are decoded only when its rows are processed).
@@ -196,7 +199,10 @@ def expert_ffn(x_perm, offsets, W1, W3, W2, rounding=True):
         ae = xe @ values(W1[e]).T
         be = xe @ values(W3[e]).T
         he = bf16_round(silu(ae) * be, rounding)
-        oe = bf16_round(he @ values(W2[e]).T, rounding)
+        pe = he @ values(W2[e]).T
+        if row_scale is not None:
+            pe = np.asarray(row_scale, dtype=np.float64)[r0:r1, None] * pe
+        oe = bf16_round(pe, rounding)
         a[r0:r1], b[r0:r1], h[r0:r1], o[r0:r1] = ae, be, he, oe
     return a, b, h, o
 

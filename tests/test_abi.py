@@ -80,7 +80,7 @@ def test_host_argument_checks():
                            ctypes.c_void_p(4098), None) == 2
     # grouped ffn: f % 8
     assert lib.moe_grouped_ffn(None, None, 10, 64, 60, 4, None, None, None, None, None, None,
-                               None, None, ctypes.byref(n), 0, None) == 2
+                               None, None, None, ctypes.byref(n), 0, None) == 2
 
 
 def test_layer_ws_query_and_bwd_shape_limits():

@@ -144,3 +144,57 @@ def test_layer_backward(lib, name, T, E, f):
     for e in np.nonzero(ref["counts"] == 0)[0]:
         if keep[e]:
             assert not dW1[e].any() and not dW2[e].any() and not dWg[:, e].any()
+
+
+# ---------------------------------------------------------------- row scale
+@pytest.mark.parametrize("counts,d,f", [([64, 100, 0, 300, 37, 1, 0, 10], 512, 1024),
+                                        ([300, 0, 7], 200, 136), ([256, 257, 511, 129], 1024, 384)])
+def test_grouped_ffn_row_scale(lib, counts, d, f):
+    E = len(counts)
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    N = int(offsets[-1])
+    seed = N + d
+    x_perm = _bf16((N, d), 1.0, seed)
+    W = [_bf16(s, 0.02, seed + i) for i, s in enumerate(((E, f, d), (E, f, d), (E, d, f)), 1)]
+    sc = (torch.rand(N, generator=torch.Generator().manual_seed(seed)) + 0.1).float()
+    dev = [t.cuda() for t in [x_perm] + W]
+    off = torch.from_numpy(offsets).cuda()
+    outs = []
+    for flags in (0, lib.MOE_SINGLE_CTA_TILES):
+        h = torch.empty((N, f), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((N, d), dtype=torch.bfloat16, device="cuda")
+        lib.moe_grouped_ffn(dev[0], off, *dev[1:], h, out,
+                            lib.workspace(lib.grouped_ffn_ws_bytes(N, d, f, E)),
+                            flags=flags | lib.MOE_CHECK, row_scale=sc.cuda())
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    ro = O.expert_ffn(bits(x_perm), offsets, *(bits(w) for w in W), row_scale=sc.numpy())[3]
+    assert_close(f64(outs[0]), ro, "o scaled")
+
+
+def test_row_scaled_outputs_combine_unweighted(lib):
+    # the gate weighting moved to the expert side: the grouped FFN scales each
+    # row by its gate weight before the row's bf16 rounding, and an unweighted
+    # combine sums the rows; checked against the oracle with those rounding
+    # points, on the layer's own routing
+    wl = synth.workload("mid", T=256)
+    inp = synth.layer_inputs(wl)
+    _, layer, saved, y = _layer_run(lib, wl, inp, train=False)
+    torch.cuda.synchronize()
+    N = wl.T * wl.R
+    w_row = saved.topk_w.reshape(-1)[saved.row_slot.long()].contiguous()
+    out = torch.empty((N, wl.d), dtype=torch.bfloat16, device="cuda")
+    h = torch.empty((N, wl.f), dtype=torch.bfloat16, device="cuda")
+    lib.moe_grouped_ffn(saved.x_perm, saved.offsets, layer.W1, layer.W3, layer.W2, h, out,
+                        lib.workspace(lib.grouped_ffn_ws_bytes(N, wl.d, wl.f, wl.E)),
+                        flags=lib.MOE_CHECK, row_scale=w_row)
+    y2 = torch.empty_like(y)
+    lib.moe_combine(out, saved.slot_row, None, y2, wl.R)
+    torch.cuda.synchronize()
+    offsets = saved.offsets.cpu().numpy()
+    o_s = O.expert_ffn(bits(saved.x_perm), offsets, bits(inp["W1"]), bits(inp["W3"]),
+                       bits(inp["W2"]), row_scale=f64(w_row))[3]
+    ref = O.combine(o_s, saved.slot_row.cpu().numpy(), None, wl.T, wl.R)
+    assert_close(f64(y2), ref, "y (weights on the expert side)")

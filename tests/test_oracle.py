@@ -254,6 +254,33 @@ def test_expert_ffn_matches_torch_per_expert_with_rounding():
         assert np.mean(h[s] == th.numpy()) > 0.99 and np.mean(o[s] == to.numpy()) > 0.99
 
 
+def test_expert_ffn_row_scale():
+    # the scale multiplies the unrounded row before its bf16 rounding: 1 changes
+    # nothing, a power of two scales the rounded value exactly, and a general
+    # scale matches torch (fp64 product, then its bf16 conversion)
+    r = _rng(19)
+    E, d, f = 3, 16, 12
+    counts = [4, 0, 6]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    N = int(offsets[-1])
+    xb = _bf16_bits_of(r.standard_normal((N, d)))
+    W1 = _bf16_bits_of(r.standard_normal((E, f, d)) * 0.3)
+    W3 = _bf16_bits_of(r.standard_normal((E, f, d)) * 0.3)
+    W2 = _bf16_bits_of(r.standard_normal((E, d, f)) * 0.3)
+    o = O.expert_ffn(xb, offsets, W1, W3, W2)[3]
+    assert np.array_equal(O.expert_ffn(xb, offsets, W1, W3, W2, row_scale=np.ones(N))[3], o)
+    p2 = 2.0 ** r.integers(-6, 7, N)
+    assert np.array_equal(O.expert_ffn(xb, offsets, W1, W3, W2, row_scale=p2)[3], p2[:, None] * o)
+    sc = r.random(N) + 0.1
+    _, _, h, os_ = O.expert_ffn(xb, offsets, W1, W3, W2, row_scale=sc)
+    for e in (0, 2):
+        s = slice(offsets[e], offsets[e + 1])
+        p = torch.tensor(h[s]) @ torch.tensor(O.bf16_to_f64(W2[e])).T
+        want = (torch.tensor(sc[s])[:, None] * p).to(torch.bfloat16).to(torch.float64).numpy()
+        np.testing.assert_allclose(os_[s], want, rtol=2 ** -7, atol=0)
+        assert np.mean(os_[s] == want) > 0.95
+
+
 # ---------------------------------------------------------------- combine
 def test_identity_experts_roundtrip_is_exact():
     # combine(dispatch(x)) == x because the gate weights sum to 1
