@@ -66,6 +66,9 @@ def parse():
     p.add_argument("--shared-serial", action="store_true",
                    help="run the shared expert on the caller's stream after the routed path "
                         "(MOE_SHARED_SERIAL), for comparison")
+    p.add_argument("--flush-l2", action="store_true",
+                   help="write a 512 MB buffer (4x L2) between timed steps, outside the stage "
+                        "events, so small workloads read HBM; ms_per_step then includes it")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -325,7 +328,11 @@ def run_ours(args, rank, world, device):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
+    flush = (torch.empty(512 << 20, dtype=torch.uint8, device=device) if args.flush_l2
+             else None)
     for k in range(args.steps):
+        if flush is not None:
+            flush.fill_(k & 0xff)
         traces[k].arm()
         step()
     B.StageTrace.disarm()
@@ -502,7 +509,9 @@ def run_ours(args, rank, world, device):
                    + (" fp8-dispatch" if args.fp8 else ""),
                    "parallelism": f"replicas x{world} (no cross-GPU exchange)",
                    "global_batch_tokens": wl.T * world,
-                   "l2": "inputs larger than L2 every step (no flush)",
+                   "l2": ("512 MB written between steps (flushes L2; outside the stage events, "
+                          "inside ms_per_step)" if args.flush_l2 else
+                          "inputs larger than L2 every step (no flush)"),
                    "weights": weights_note,
                    "gemm_tiles": None if identity else
                    ("128-row, one CTA" if args.single_cta else "256-row, CTA pairs"),

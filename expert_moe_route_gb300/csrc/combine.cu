@@ -15,24 +15,30 @@ namespace moe {
 namespace {
 constexpr int CW = 8;   // warps per block
 
+// One warp per (token, column chunk of cv 16-byte vectors, a multiple of 32):
+// with few tokens (small batches, e.g. decode) each row is cut into `chunks`
+// pieces so that every SM gets several warps.
 __global__ void __launch_bounds__(CW * 32) combine_kernel(const uint16_t* __restrict__ o,
                                                           const int32_t* __restrict__ slot_row,
                                                           const float* __restrict__ w, int T,
-                                                          int d, int R, int N,
+                                                          int d, int R, int N, int chunks, int cv,
                                                           const uint16_t* __restrict__ add,
                                                           uint16_t* __restrict__ y) {
   __shared__ int rows_s[CW][32];
   __shared__ float w_s[CW][32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int nv = d / 8;
-  for (int t = blockIdx.x * CW + wid; t < T; t += gridDim.x * CW) {
+  const long long units = (long long)T * chunks;
+  for (long long u = (long long)blockIdx.x * CW + wid; u < units; u += (long long)gridDim.x * CW) {
+    const int t = (int)(u / chunks), c = (int)(u % chunks);
+    const int vend = min(nv, (c + 1) * cv);
     if (lane < R) {
       const int row = slot_row[(size_t)t * R + lane];
       rows_s[wid][lane] = ((unsigned)row < (unsigned)N) ? row : -1;
       w_s[wid][lane] = w ? w[(size_t)t * R + lane] : 1.f;
     }
     __syncwarp();
-    for (int v = lane; v < nv; v += 32) {
+    for (int v = c * cv + lane; v < vend; v += 32) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       if (add) unpack8(ldg_nc_v4(add + (size_t)t * d + (size_t)v * 8), acc);   // shared expert first
       for (int r0 = 0; r0 < R; r0 += 4) {
@@ -81,8 +87,20 @@ cudaError_t launch_selftest_wait(unsigned limit_us, int* err, cudaStream_t s) {
 cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const float* w, int T,
                            int d, int R, uint16_t* y, cudaStream_t s, const uint16_t* add) {
   if (T == 0) return cudaSuccess;
-  const int blocks = ceil_div(T, CW) < 152 * 8 ? ceil_div(T, CW) : 152 * 8;
-  combine_kernel<<<blocks, CW * 32, 0, s>>>(o, slot_row, w, T, d, R, T * R, add, y);
+  // few tokens: cut each row into column chunks so that ~16 warps per SM work
+  const int nv = d / 8;
+  const long long want = 152LL * 16;
+  int chunks = 1;
+  if (T < want) {
+    const long long c = (want + T - 1) / T;
+    const int cmax = nv / 32 > 1 ? nv / 32 : 1;
+    chunks = c < cmax ? (int)c : cmax;
+  }
+  const int cv = ceil_div(ceil_div(nv, chunks), 32) * 32;
+  chunks = ceil_div(nv, cv);
+  const long long units = (long long)T * chunks;
+  const int blocks = (int)((units + CW - 1) / CW < 152 * 8 ? (units + CW - 1) / CW : 152 * 8);
+  combine_kernel<<<blocks, CW * 32, 0, s>>>(o, slot_row, w, T, d, R, T * R, chunks, cv, add, y);
   count_launches(1);
   return cudaGetLastError();
 }

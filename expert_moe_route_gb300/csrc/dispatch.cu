@@ -176,30 +176,38 @@ __global__ void __launch_bounds__(256) slot_rank_kernel(const int32_t* __restric
 }
 
 // One warp per token; lanes move 16-byte vectors of x[t] to the token's R rows.
+// One warp per (token, column chunk): a token's row is cut into `chunks`
+// pieces of `cv` 16-byte vectors (a multiple of 128) when there are too few
+// tokens to give every SM several warps (small batches, e.g. decode).
 __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __restrict__ x, int T,
-                                                           int d, int R, int N,
+                                                           int d, int R, int N, int chunks,
+                                                           int cv,
                                                            const int32_t* __restrict__ slot_row,
                                                            uint16_t* __restrict__ x_perm) {
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x / 32;
   const int nv = d / 8;
-  for (int t = blockIdx.x * warps + threadIdx.x / 32; t < T; t += gridDim.x * warps) {
+  const long long units = (long long)T * chunks;
+  for (long long u = (long long)blockIdx.x * warps + threadIdx.x / 32; u < units;
+       u += (long long)gridDim.x * warps) {
+    const int t = (int)(u / chunks), c = (int)(u % chunks);
     int my_row = lane < R ? slot_row[(size_t)t * R + lane] : -1;
     if ((unsigned)my_row >= (unsigned)N) my_row = -1;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    for (int base = 0; base < nv; base += 32 * 4) {  // warp-uniform trip count
+    const int vend = min(nv, (c + 1) * cv);
+    for (int base = c * cv; base < vend; base += 32 * 4) {  // warp-uniform trip count
       const int v0 = base + lane;
       uint4 q[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (v0 + 32 * u < nv) q[u] = ldg_nc_v4(src + v0 + 32 * u);
+        if (v0 + 32 * u < vend) q[u] = ldg_nc_v4(src + v0 + 32 * u);
       for (int r = 0; r < R; ++r) {
         const int row = __shfl_sync(kFull, my_row, r);
         if (row < 0) continue;
         uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * d);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          if (v0 + 32 * u < nv) dst[v0 + 32 * u] = q[u];
+          if (v0 + 32 * u < vend) dst[v0 + 32 * u] = q[u];
       }
     }
   }
@@ -302,8 +310,20 @@ cudaError_t launch_dispatch(const uint16_t* x, const int32_t* idx, int T, int d,
   slot_rank_kernel<<<nblk, 256, rank_smem, s>>>(idx, T, E, R, nblk, blk_base, row_slot, slot_row);
   count_launches(3);
   if (x != nullptr && x_perm != nullptr) {
-    const int blocks = ceil_div(T, 8) < 152 * 8 ? ceil_div(T, 8) : 152 * 8;
-    permute_rows_kernel<<<blocks, 256, 0, s>>>(x, T, d, R, T * R, slot_row, x_perm);
+    // few tokens: cut each row into column chunks so that ~16 warps per SM copy
+    const int nv = d / 8;
+    const long long want = 152LL * 16;
+    int chunks = 1;
+    if (T < want) {
+      const long long c = (want + T - 1) / T;
+      const int cmax = nv / 128 > 1 ? nv / 128 : 1;
+      chunks = c < cmax ? (int)c : cmax;
+    }
+    const int cv = ceil_div(ceil_div(nv, chunks), 128) * 128;
+    chunks = ceil_div(nv, cv);
+    const long long units = (long long)T * chunks;
+    const int blocks = (int)((units + 7) / 8 < 152 * 8 ? (units + 7) / 8 : 152 * 8);
+    permute_rows_kernel<<<blocks, 256, 0, s>>>(x, T, d, R, T * R, chunks, cv, slot_row, x_perm);
     count_launches(1);
   }
   return cudaGetLastError();
