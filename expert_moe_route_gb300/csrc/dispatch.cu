@@ -15,6 +15,9 @@
 //      row = blk_base + earlier warps + earlier groups + rank (stable order).
 //   4. permute_rows: one warp per token reads x[t] once (16-byte vectors) and
 //      writes it to its R rows of x_perm.
+// With at most CHUNK tokens (one block of slots, e.g. a decode batch) one
+// kernel does 1-3 (dispatch_plan_one_block): the same per-warp counts and
+// ranks, with the per-expert totals scanned in shared memory.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -175,6 +178,103 @@ __global__ void __launch_bounds__(256) slot_rank_kernel(const int32_t* __restric
   }
 }
 
+// Steps 1-3 for T <= CHUNK in one block: validation, per-warp counts (pass 1 of
+// slot_rank), per-expert totals, their exclusive scan (offsets), warp bases,
+// and the rows (pass 2).  Same rows as the three-kernel path.
+__global__ void __launch_bounds__(256) dispatch_plan_one_block_kernel(
+    const int32_t* __restrict__ idx, int T, int E, int R, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ row_slot, int32_t* __restrict__ slot_row,
+    int* __restrict__ err) {
+  extern __shared__ int32_t sm[];
+  int32_t* wcnt = sm;                       // [DWARPS][E]
+  int32_t* keys = sm + DWARPS * E;          // [CHUNK*R]
+  int32_t* tot = keys + CHUNK * R;          // [E]
+  __shared__ int32_t warp_sums[DWARPS];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int ns = T * R;
+  bool bad = false;
+  for (int i = threadIdx.x; i < DWARPS * E; i += blockDim.x) wcnt[i] = 0;
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    const int e = idx[i];
+    const bool ok = (unsigned)e < (unsigned)E;
+    bad |= !ok;
+    keys[i] = ok ? e : -1;
+  }
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {  // repeated expert in a token
+    const int32_t* row = idx + (size_t)t * R;
+    for (int i = 1; i < R; ++i) {
+      const int ei = row[i];
+      for (int j = 0; j < i; ++j) bad |= (row[j] == ei);
+    }
+  }
+  if (bad) atomicOr(err, kErrBadRouting);
+  __syncthreads();
+  const int per_warp = ceil_div(ns, DWARPS * 32) * 32;
+  const int w0 = wid * per_warp;
+  const int w1 = min(ns, w0 + per_warp);
+  int32_t* my = wcnt + wid * E;
+  for (int g = w0; g < w1; g += 32) {  // per-warp counts
+    const int i = g + lane;
+    const int e = i < w1 ? keys[i] : -1;
+    const unsigned peers = __match_any_sync(kFull, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < DWARPS; ++w) c += wcnt[w * E + e];
+    tot[e] = c;
+  }
+  __syncthreads();
+  // exclusive scan of tot: each thread a contiguous range of experts
+  const int per = ceil_div(E, (int)blockDim.x);
+  const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+  int sum = 0;
+  for (int e = e0; e < e1; ++e) sum += tot[e];
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  int run = incl - sum;
+  for (int w = 0; w < wid; ++w) run += warp_sums[w];
+  for (int e = e0; e < e1; ++e) {   // offsets, counts and the warps' bases of expert e
+    const int c = tot[e];
+    offsets[e] = run;
+    counts[e] = c;
+    int wrun = run;
+#pragma unroll
+    for (int w = 0; w < DWARPS; ++w) {
+      const int cw = wcnt[w * E + e];
+      wcnt[w * E + e] = wrun;
+      wrun += cw;
+    }
+    run += c;
+  }
+  if (threadIdx.x == blockDim.x - 1) offsets[E] = run;   // rows of valid slots
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int g = w0; g < w1; g += 32) {  // rows
+    const int i = g + lane;
+    const int e = i < w1 ? keys[i] : -1;
+    const unsigned peers = __match_any_sync(kFull, e);
+    int row = -1;
+    if (e >= 0) row = my[e] + __popc(peers & lt);
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+    __syncwarp();
+    if (i < w1) {
+      slot_row[i] = row;
+      if (row >= 0) row_slot[row] = i;
+    }
+  }
+}
+
 // One warp per token; lanes move 16-byte vectors of x[t] to the token's R rows.
 // One warp per (token, column chunk): a token's row is cut into `chunks`
 // pieces of `cv` 16-byte vectors (a multiple of 128) when there are too few
@@ -304,11 +404,20 @@ cudaError_t launch_dispatch(const uint16_t* x, const int32_t* idx, int T, int d,
     if (e != cudaSuccess) return e;
     return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
   }
-  expert_hist_kernel<<<nblk, 256, E * sizeof(int32_t), s>>>(idx, T, E, R, nblk, blk_counts, err);
-  expert_scan_kernel<<<1, 1024, 0, s>>>(blk_counts, E, nblk, blk_base, counts, offsets);
-  const size_t rank_smem = sizeof(int32_t) * ((size_t)DWARPS * E + (size_t)CHUNK * R);
-  slot_rank_kernel<<<nblk, 256, rank_smem, s>>>(idx, T, E, R, nblk, blk_base, row_slot, slot_row);
-  count_launches(3);
+  if (nblk == 1) {   // one block of slots: the plan in one kernel
+    const size_t smem = sizeof(int32_t) * ((size_t)DWARPS * E + (size_t)CHUNK * R + E);
+    dispatch_plan_one_block_kernel<<<1, 256, smem, s>>>(idx, T, E, R, counts, offsets, row_slot,
+                                                        slot_row, err);
+    count_launches(1);
+  } else {
+    expert_hist_kernel<<<nblk, 256, E * sizeof(int32_t), s>>>(idx, T, E, R, nblk, blk_counts,
+                                                             err);
+    expert_scan_kernel<<<1, 1024, 0, s>>>(blk_counts, E, nblk, blk_base, counts, offsets);
+    const size_t rank_smem = sizeof(int32_t) * ((size_t)DWARPS * E + (size_t)CHUNK * R);
+    slot_rank_kernel<<<nblk, 256, rank_smem, s>>>(idx, T, E, R, nblk, blk_base, row_slot,
+                                                  slot_row);
+    count_launches(3);
+  }
   if (x != nullptr && x_perm != nullptr) {
     // few tokens: cut each row into column chunks so that ~16 warps per SM copy
     const int nv = d / 8;
@@ -355,8 +464,12 @@ cudaError_t launch_dequant_fp8(const uint8_t* xq, const float* xs, long long N, 
 
 cudaError_t dispatch_set_smem_limits() {
   const int max_rank_smem = sizeof(int32_t) * (DWARPS * 1024 + CHUNK * 32);
-  return cudaFuncSetAttribute(slot_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              max_rank_smem);
+  cudaError_t e = cudaFuncSetAttribute(slot_rank_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max_rank_smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(dispatch_plan_one_block_kernel,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              max_rank_smem + (int)sizeof(int32_t) * 1024);
 }
 
 }  // namespace moe
