@@ -18,14 +18,24 @@ from tests.helpers import LazyExperts, assert_close, bits, f64, near_tie_tokens
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_layer(B, wl, train):
+def _gpu_layer(B, wl, train, prepacked=False):
     inp = synth.layer_inputs(wl, device="cuda")          # as bench.py: weights drawn on the GPU
     layer = B.Layer(inp["w_gate"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], wl.R, wl.T)
+    packed_y = None
+    if prepacked:   # bench.py streams prepacked tiles in forward-only workloads: same bits
+        P = [torch.empty_like(inp[k]) for k in ("W1", "W3", "W2")]
+        B.moe_prepack_weights(inp["W1"], inp["W3"], inp["W2"], *P)
+        pl = B.Layer(inp["w_gate"], inp["bias"], *P, wl.R, wl.T)
+        packed_y = torch.empty_like(inp["x"])
+        B.moe_layer_fwd(pl, inp["x"], packed_y, B.Saved(pl, "cuda", train=False),
+                        B.workspace(B.layer_fwd_ws_bytes(pl)),
+                        flags=B.MOE_CHECK | B.MOE_WEIGHTS_PREPACKED)
+        del P, pl
     saved = B.Saved(layer, "cuda", train=train)
     y = torch.empty_like(inp["x"])
     B.moe_layer_fwd(layer, inp["x"], y, saved, B.workspace(B.layer_fwd_ws_bytes(layer)),
                     flags=B.MOE_CHECK)
-    out = {"inp": inp, "saved": saved, "y": y}
+    out = {"inp": inp, "saved": saved, "y": y, "packed_y": packed_y}
     if train:
         dx = torch.empty_like(inp["x"])
         dWg = torch.empty((wl.d, wl.E), dtype=torch.float32, device="cuda")
@@ -58,7 +68,9 @@ def _oracle_subset(inp, wl, toks, bias, train):
 @pytest.mark.parametrize("name", ["large", "large_hot", "train"])
 def test_forward_full_size_sampled_tokens(lib, name):
     wl = synth.workload(name)
-    run = _gpu_layer(lib, wl, train=False)
+    run = _gpu_layer(lib, wl, train=False, prepacked=name != "train")
+    if run["packed_y"] is not None:
+        assert torch.equal(run["packed_y"].view(torch.int16), run["y"].view(torch.int16))
     logits, idx, w, bias = _oracle_routing(run["inp"], wl)
     gidx = run["saved"].topk_idx.cpu().numpy()
     same = (gidx == idx).all(axis=1)
