@@ -27,7 +27,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 SYMBOLS = ("moe_status_string", "moe_version", "moe_last_cuda_error", "moe_trace_events",
            "moe_kernel_launches", "moe_selftest_wait_timeout",
            "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_dispatch_fp8",
-           "moe_dequant_fp8", "moe_prepack_weights", "moe_grouped_ffn",
+           "moe_dequant_fp8", "moe_prepack_weights", "moe_grouped_ffn", "moe_grouped_ffn_fp8",
            "moe_combine", "moe_layer_fwd", "moe_layer_bwd")
 
 # moe_stage_t
@@ -94,6 +94,9 @@ def _declare(lib):
     lib.moe_grouped_ffn.restype = _i
     lib.moe_grouped_ffn.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _vp, _vp, _szp, _u, _vp]
+    lib.moe_grouped_ffn_fp8.restype = _i
+    lib.moe_grouped_ffn_fp8.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
+                                        _vp, _vp, _vp, _vp, _szp, _u, _vp]
     lib.moe_combine.restype = _i
     lib.moe_combine.argtypes = [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]
     lib.moe_layer_fwd.restype = _i
@@ -252,6 +255,25 @@ def moe_grouped_ffn(x_perm, offsets, W1, W3, W2, h, out, ws, a_save=None, b_save
                                _p(row_scale), _p(a_save), _p(b_save), _p(h), _p(out), _p(ws),
                                ctypes.byref(n), flags, _stream(stream))
     _check(st, "moe_grouped_ffn")
+
+
+def moe_grouped_ffn_fp8(xq_perm, xscale_perm, offsets, W1, W3, W2, h, out, ws, a_save=None,
+                        b_save=None, flags=0, stream=None, row_scale=None):
+    """moe_grouped_ffn on block-scaled fp8 rows (uint8 codes [N, d], fp32 scales [N, d/128])."""
+    N, d = xq_perm.shape
+    E, f, _ = W1.shape
+    _dt(xq_perm, torch.uint8, "xq_perm")
+    _dt(xscale_perm, torch.float32, "xscale_perm")
+    for name, t in (("W1", W1), ("W3", W3), ("W2", W2), ("h", h), ("out", out),
+                    ("a_save", a_save), ("b_save", b_save)):
+        _dt(t, torch.bfloat16, name)
+    _dt(offsets, torch.int32, "offsets")
+    _dt(row_scale, torch.float32, "row_scale")
+    n = ctypes.c_size_t(ws.numel())
+    st = lib().moe_grouped_ffn_fp8(_p(xq_perm), _p(xscale_perm), _p(offsets), N, d, f, E, _p(W1),
+                                   _p(W3), _p(W2), _p(row_scale), _p(a_save), _p(b_save), _p(h),
+                                   _p(out), _p(ws), ctypes.byref(n), flags, _stream(stream))
+    _check(st, "moe_grouped_ffn_fp8")
 
 
 def moe_prepack_weights(W1, W3, W2, W1p, W3p, W2p, stream=None):

@@ -346,6 +346,41 @@ moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int
   return finish(e, err, flags, s);
 }
 
+moe_status_t moe_grouped_ffn_fp8(const uint8_t* xq_perm, const float* xscale_perm,
+                                 const int32_t* offsets, int N, int d, int f, int E,
+                                 const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                                 const float* row_scale, uint16_t* a_save, uint16_t* b_save,
+                                 uint16_t* h, uint16_t* out, void* ws, size_t* ws_bytes,
+                                 unsigned flags, moe_stream_t stream) {
+  if (N < 0 || d <= 0 || f <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 128 || f % 8 || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if ((flags & MOE_WEIGHTS_PREPACKED) && !prepack_supported(d, f)) return MOE_ERR_UNSUPPORTED;
+  if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t need = kErrBytes + tiles_ws_bytes(N, E);
+  if (!ws) {
+    *ws_bytes = need;
+    return MOE_OK;
+  }
+  if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
+  if (!offsets || !W1 || !W3 || !W2) return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!xq_perm || !xscale_perm || !h || !out)) return MOE_ERR_INVALID_ARG;
+  if ((a_save == nullptr) != (b_save == nullptr)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {xq_perm, W1, W3, W2, a_save, b_save, h, out};
+  for (const void* p : ps)
+    if (p && !al16(p)) return MOE_ERR_UNSUPPORTED;
+  if ((uintptr_t)xscale_perm & 3) return MOE_ERR_UNSUPPORTED;
+  if (!init_once()) return MOE_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  int* err = static_cast<int*>(ws);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  cudaError_t e = launch_ffn_fwd(nullptr, offsets, N, d, f, E, W1, W3, W2, a_save, b_save, h, out,
+                                 static_cast<uint8_t*>(ws) + kErrBytes, err,
+                                 (flags & MOE_WEIGHTS_PREPACKED) != 0,
+                                 !(flags & MOE_SINGLE_CTA_TILES), s, row_scale, xq_perm,
+                                 xscale_perm);
+  return finish(e, err, flags, s);
+}
+
 moe_status_t moe_prepack_weights(const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, int E,
                                  int d, int f, uint16_t* W1p, uint16_t* W3p, uint16_t* W2p,
                                  moe_stream_t stream) {

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,6 +45,25 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
 __device__ __forceinline__ uint4 pack8(const float* f) {
   return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
                     pack_bf16(f[6], f[7]));
+}
+
+// f[i] = (value of the E4M3 code in byte i of q) * scale, i = 0..7: the code's
+// value is exact in half precision and the fp32 product rounds once.  The fp8
+// dequantiser and the fp8-input gate-up GEMM both use this, so that they give
+// the same bits.
+__device__ __forceinline__ void e4m3x8_scaled(const uint2& q, float scale, float* f) {
+  const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[h] >> (16 * j)) & 0xffff);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+      const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      f[h * 4 + j * 2] = ff.x * scale;
+      f[h * 4 + j * 2 + 1] = ff.y * scale;
+    }
+  }
 }
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {

@@ -370,18 +370,7 @@ __global__ void __launch_bounds__(256) dequant_fp8_kernel(const uint8_t* __restr
     const float scale = xs[row * nb + c / 128];
     const uint2 q = *reinterpret_cast<const uint2*>(xq + row * d + c);
     float f[8];
-    const uint32_t w[2] = {q.x, q.y};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[h] >> (16 * j)) & 0xffff);
-        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-        const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-        f[h * 4 + j * 2] = ff.x * scale;
-        f[h * 4 + j * 2 + 1] = ff.y * scale;
-      }
-    }
+    e4m3x8_scaled(q, scale, f);
     *reinterpret_cast<uint4*>(out + row * d + c) = pack8(f);
   }
 }

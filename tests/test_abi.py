@@ -81,6 +81,15 @@ def test_host_argument_checks():
     # grouped ffn: f % 8
     assert lib.moe_grouped_ffn(None, None, 10, 64, 60, 4, None, None, None, None, None, None,
                                None, None, None, ctypes.byref(n), 0, None) == 2
+    # fp8 grouped ffn: d % 128 (scale blocks), then a size query
+    assert lib.moe_grouped_ffn_fp8(None, None, None, 10, 192, 64, 4, None, None, None, None, None,
+                                   None, None, None, None, ctypes.byref(n), 0, None) == 2
+    assert lib.moe_grouped_ffn_fp8(None, None, None, 10, 256, 64, 4, None, None, None, None, None,
+                                   None, None, None, None, ctypes.byref(n), 0, None) == 0
+    m = ctypes.c_size_t(0)
+    assert lib.moe_grouped_ffn(None, None, 10, 256, 64, 4, None, None, None, None, None, None,
+                               None, None, None, ctypes.byref(m), 0, None) == 0
+    assert n.value == m.value
 
 
 def test_layer_ws_query_and_bwd_shape_limits():
