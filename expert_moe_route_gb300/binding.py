@@ -257,6 +257,14 @@ def moe_grouped_ffn(x_perm, offsets, W1, W3, W2, h, out, ws, a_save=None, b_save
     _check(st, "moe_grouped_ffn")
 
 
+def grouped_ffn_fp8_ws_bytes(N, d, f, E) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_grouped_ffn_fp8(None, None, None, N, d, f, E, None, None, None, None, None,
+                                     None, None, None, None, ctypes.byref(n), 0, None),
+           "moe_grouped_ffn_fp8(ws query)")
+    return n.value
+
+
 def moe_grouped_ffn_fp8(xq_perm, xscale_perm, offsets, W1, W3, W2, h, out, ws, a_save=None,
                         b_save=None, flags=0, stream=None, row_scale=None):
     """moe_grouped_ffn on block-scaled fp8 rows (uint8 codes [N, d], fp32 scales [N, d/128])."""

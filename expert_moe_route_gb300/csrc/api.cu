@@ -356,7 +356,8 @@ moe_status_t moe_grouped_ffn_fp8(const uint8_t* xq_perm, const float* xscale_per
   if (d % 128 || f % 8 || E > 1024) return MOE_ERR_UNSUPPORTED;
   if ((flags & MOE_WEIGHTS_PREPACKED) && !prepack_supported(d, f)) return MOE_ERR_UNSUPPORTED;
   if (!ws_bytes) return MOE_ERR_INVALID_ARG;
-  const size_t need = kErrBytes + tiles_ws_bytes(N, E);
+  const size_t tws = tiles_ws_bytes(N, E);
+  const size_t need = kErrBytes + tws + align_up((size_t)N * d * 2, 256);
   if (!ws) {
     *ws_bytes = need;
     return MOE_OK;
@@ -373,11 +374,17 @@ moe_status_t moe_grouped_ffn_fp8(const uint8_t* xq_perm, const float* xscale_per
   cudaStream_t s = S(stream);
   int* err = static_cast<int*>(ws);
   MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
-  cudaError_t e = launch_ffn_fwd(nullptr, offsets, N, d, f, E, W1, W3, W2, a_save, b_save, h, out,
-                                 static_cast<uint8_t*>(ws) + kErrBytes, err,
-                                 (flags & MOE_WEIGHTS_PREPACKED) != 0,
-                                 !(flags & MOE_SINGLE_CTA_TILES), s, row_scale, xq_perm,
-                                 xscale_perm);
+  // Each element is converted once, into the workspace: a gate-up GEMM that
+  // converted its fp8 A tiles in shared memory would convert every element
+  // once per 128-column tile of W1 / W3, more than the SM's conversion rate
+  // can feed to the tensor cores.
+  uint16_t* x_perm = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + kErrBytes + tws);
+  cudaError_t e = N > 0 ? launch_dequant_fp8(xq_perm, xscale_perm, N, d, x_perm, s) : cudaSuccess;
+  if (e == cudaSuccess)
+    e = launch_ffn_fwd(x_perm, offsets, N, d, f, E, W1, W3, W2, a_save, b_save, h, out,
+                       static_cast<uint8_t*>(ws) + kErrBytes, err,
+                       (flags & MOE_WEIGHTS_PREPACKED) != 0, !(flags & MOE_SINGLE_CTA_TILES), s,
+                       row_scale);
   return finish(e, err, flags, s);
 }
 

@@ -48,9 +48,7 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 }
 
 // f[i] = (value of the E4M3 code in byte i of q) * scale, i = 0..7: the code's
-// value is exact in half precision and the fp32 product rounds once.  The fp8
-// dequantiser and the fp8-input gate-up GEMM both use this, so that they give
-// the same bits.
+// value is exact in half precision and the fp32 product rounds once.
 __device__ __forceinline__ void e4m3x8_scaled(const uint2& q, float scale, float* f) {
   const uint32_t w[2] = {q.x, q.y};
 #pragma unroll

@@ -31,7 +31,6 @@ namespace moe {
 namespace {
 constexpr int BM = 128, BK = 64, BN = 256, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
-constexpr int A8_BYTES = BM * BK;               // 8 KiB: a 128 x 64 tile of fp8 codes
 constexpr int B_BYTES = BN * BK * 2;            // 32 KiB
 constexpr int ATOM_BYTES = 64 * BK * 2;         // MN-major block: 64 elements x 64 k-rows
 constexpr int EPI_WARPS = 8;                      // two per TMEM lane quadrant
@@ -40,12 +39,10 @@ constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;  // per CTA (weight-gradie
 constexpr int CTL_BYTES = 256;
 
 constexpr int THREADS = 64 + 32 * EPI_WARPS;     // TMA warp, MMA warp, epilogue warps
-constexpr int CONV_WARPS = 4;                    // GATEUP8: fp8 -> bf16 converter warps
-constexpr int SMEM_LIMIT = 232448;               // opt-in shared memory per block
 constexpr uint32_t TMEM_COLS = 512;
 
 enum Mode : int { GATEUP = 0, DOWN = 1, DH = 2, DX = 3, WG2 = 4, WG13 = 5, GATE = 6,
-                  GATEUP2 = 7, DOWN2 = 8, GATEUP8 = 9 };
+                  GATEUP2 = 7, DOWN2 = 8 };
 
 template <int M, bool C2 = false> struct Traits {
   static constexpr bool a_mn = (M == WG2 || M == WG13);
@@ -65,37 +62,21 @@ template <int M, bool C2 = false> struct Traits {
   // regime (few rows per expert).  No second accumulator set, so the epilogue
   // does not overlap the next item's main loop.
   static constexpr bool pair = (M == GATEUP2 || M == DOWN2);
-  static constexpr bool is_gateup = (M == GATEUP || M == GATEUP2 || M == GATEUP8);
-  // GATEUP8: gate-up whose A rows are block-scaled fp8 (E4M3 codes, one fp32
-  // scale per row and 128 channels).  The TMA ring stages the 8 KB code tile
-  // (on the CTA's own barrier) and B; CONV_WARPS converter warps turn each
-  // code tile into the bf16 A tile, bf16(code * scale) in the 128-B swizzled
-  // layout a TMA box would have, in a separate ring of conv_bufs buffers that
-  // the MMAs read.  Both rings are freed by the MMAs' commits.
-  static constexpr bool f8a = (M == GATEUP8);
-  static constexpr int conv_bufs = f8a ? (C2 ? 3 : 2) : 0;
-  static constexpr int threads = THREADS + (f8a ? 32 * CONV_WARPS : 0);
+  static constexpr bool is_gateup = (M == GATEUP || M == GATEUP2);
   static constexpr bool is_down = (M == DOWN || M == DOWN2);
   static constexpr bool single_acc = partials || pair;
   // C2: the CTA pair computes 256-row tiles; each CTA stages 128 rows of A
   // and half of B (128 of the 256 columns), so a stage is 32 KB and six fit.
   static constexpr int tile_m = C2 ? 2 * BM : BM;
   static constexpr int stages = pair ? 3 : (C2 ? 6 : STAGES);
-  static constexpr int a_bytes = f8a ? A8_BYTES : (pair ? 2 * A_BYTES : A_BYTES);
+  static constexpr int a_bytes = pair ? 2 * A_BYTES : A_BYTES;
   static constexpr int b_bytes = C2 ? B_BYTES / 2 : B_BYTES;
   static constexpr int stage_bytes = a_bytes + b_bytes;
   // bytes the full barrier expects per stage (rank 0's barrier counts both CTAs' loads)
-  // (GATEUP8: B only; the code tiles signal each CTA's own barrier)
   static constexpr uint32_t stage_tx =
-      partials ? A_BYTES + 128 * BK * 2
-      : f8a    ? (uint32_t)(C2 ? 2 * b_bytes : b_bytes)
-               : (uint32_t)(C2 ? 2 * stage_bytes : stage_bytes);
-  // stages | converted A tiles | epilogue staging | control block, plus slack
-  // for 1024-B alignment
-  static constexpr int conv_off = stages * stage_bytes;
-  static constexpr int epi_off = conv_off + conv_bufs * A_BYTES;
-  static constexpr int smem_bytes = epi_off + epi_bytes + CTL_BYTES + 1024;
-  static_assert(smem_bytes <= SMEM_LIMIT, "shared memory");
+      partials ? A_BYTES + 128 * BK * 2 : (uint32_t)(C2 ? 2 * stage_bytes : stage_bytes);
+  // stages | epilogue staging | control block, plus slack for 1024-B alignment
+  static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + CTL_BYTES + 1024;
 };
 
 constexpr int MAX_STAGES = 6;
@@ -106,9 +87,6 @@ struct alignas(8) SharedCtl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
-  uint64_t afull[MAX_STAGES];   // GATEUP8: this CTA's code tile landed
-  uint64_t cfull[3];            // GATEUP8: converted A tile written (rank 0: both CTAs')
-  uint64_t cempty[3];           // GATEUP8: converted A tile consumed by the MMAs
   uint32_t tmem_base;
   int abort;
 };
@@ -168,7 +146,7 @@ __device__ __forceinline__ void store_bf16x16(uint16_t* dst, const float* v, int
 }
 
 template <int MODE, bool C2>
-__global__ void __launch_bounds__(Traits<MODE, C2>::threads, 1)
+__global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
                     const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ CUtensorMap tmC3,
@@ -180,7 +158,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tile_base = (raw_addr + 1023u) & ~1023u;       // 1024-B aligned stages
   uint8_t* tile_ptr = smem_raw + (tile_base - raw_addr);
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(tile_ptr + Tr::epi_off + Tr::epi_bytes);
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(tile_ptr + Tr::stages * Tr::stage_bytes + Tr::epi_bytes);
   static_assert(sizeof(SharedCtl) <= CTL_BYTES, "control block");
   volatile int* abort_flag = &ctl->abort;
 
@@ -202,13 +180,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       mbar_init(smem_u32(&ctl->tempty[a]), C2 ? 2 * EPI_WARPS : EPI_WARPS);
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
-    if (Tr::f8a) {
-      for (int s = 0; s < Tr::stages; ++s) mbar_init(smem_u32(&ctl->afull[s]), 1);
-      for (int c = 0; c < Tr::conv_bufs; ++c) {
-        mbar_init(smem_u32(&ctl->cfull[c]), C2 ? 2 * CONV_WARPS : CONV_WARPS);
-        mbar_init(smem_u32(&ctl->cempty[c]), 1);
-      }
-    }
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -268,13 +239,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const int kx = kb * BK;
           if (Tr::pair) tma_load_2d(sa + A_BYTES, &tmA, bar, kx, it.row0 + BM);   // rows 128-255
           if (Tr::is_gateup) {
-            if (Tr::f8a) {   // the code tile lands on this CTA's own barrier
-              const uint32_t abar = smem_u32(&ctl->afull[s]);
-              mbar_arrive_expect_tx(abar, A8_BYTES);
-              tma_load_2d(sa, &tmA, abar, kx, it.row0 + rrow);
-            } else {
-              ld2(sa, &tmA, bar, kx, it.row0 + rrow);
-            }
+            ld2(sa, &tmA, bar, kx, it.row0 + rrow);
             // B = [W1 rows; W3 rows] of the column tile (C2: rank 0 W1, rank 1 W3)
             if (g.prepacked) {   // one contiguous 16 KB tile per box
               const int rt = it.e * (g.f / 128) + it.nt;
@@ -342,9 +307,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           volatile int never = 0;
           mbar_wait_bounded(smem_u32(&ctl->full[c % Tr::stages]), (c / Tr::stages) & 1u, &never,
                             nullptr);
-          if (Tr::f8a)
-            mbar_wait_bounded(smem_u32(&ctl->afull[c % Tr::stages]), (c / Tr::stages) & 1u,
-                              &never, nullptr);
         }
       }
     }
@@ -371,18 +333,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int s = it_count % Tr::stages;
         const uint32_t ph = (it_count / Tr::stages) & 1u;
         ok = mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, g.err);
-        // GATEUP8: A is the converted tile (C2: both CTAs' converters arrive here)
-        const int cb = Tr::f8a ? (int)(it_count % Tr::conv_bufs) : 0;
-        if (Tr::f8a && ok) {
-          const uint32_t cph = (it_count / Tr::conv_bufs) & 1u;
-          ok = C2 ? mbar_wait_bounded_cluster(smem_u32(&ctl->cfull[cb]), cph, abort_flag, g.err)
-                  : mbar_wait_bounded(smem_u32(&ctl->cfull[cb]), cph, abort_flag, g.err);
-        }
         ok = __all_sync(kFull, ok);
         if (!ok) break;
-        const uint32_t sa = Tr::f8a ? tile_base + Tr::conv_off + cb * A_BYTES
-                                    : tile_base + s * Tr::stage_bytes;
-        const uint32_t sb = tile_base + s * Tr::stage_bytes + Tr::a_bytes;
+        const uint32_t sa = tile_base + s * Tr::stage_bytes;
+        const uint32_t sb = sa + Tr::a_bytes;
         int kk_end = BK / 16;
         if (Tr::wgrad) {
           // The expert's last K-block may hold rows of the next expert: issue
@@ -433,10 +387,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           // frees the stage (C2: in both CTAs) when these MMAs finish
           if (C2) tc_commit_pair(smem_u32(&ctl->empty[s]), 3);
           else tc_commit(smem_u32(&ctl->empty[s]));
-          if (Tr::f8a) {   // and the converted A tile
-            if (C2) tc_commit_pair(smem_u32(&ctl->cempty[cb]), 3);
-            else tc_commit(smem_u32(&ctl->cempty[cb]));
-          }
           issued_any = true;
         }
         __syncwarp();
@@ -462,7 +412,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       mbar_wait_bounded(smem_u32(&ctl->mma_done), 0, &never, nullptr);
     }
     __syncwarp();
-  } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
     const int r_local = q * 32 + lane;   // accumulator row owned by this thread
@@ -471,8 +421,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // This warp's staging box: 32 rows (its TMEM lanes) x 128 B, 128-B swizzled
     // (16-B chunk j of row r at r * 128 + (j ^ (r & 7)) * 16), written by the
     // warp and sent to global memory by one bulk tensor store.
-    const uint32_t sbox = tile_base + Tr::epi_off + (warp - 2) * EPI_WARP_BYTES;
-    uint8_t* sbox_row = tile_ptr + Tr::epi_off + (warp - 2) * EPI_WARP_BYTES +
+    const uint32_t sbox = tile_base + Tr::stages * Tr::stage_bytes + (warp - 2) * EPI_WARP_BYTES;
+    uint8_t* sbox_row = tile_ptr + Tr::stages * Tr::stage_bytes + (warp - 2) * EPI_WARP_BYTES +
                         lane * 128;
     auto stage_begin = [&]() {   // the box is free once its previous store has read it
       if (lane == 0) bulk_wait_read_0();
@@ -705,8 +655,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           map = &tmC2;
           mrow = m0 - g.f;
         }
-        const uint32_t box = tile_base + Tr::epi_off + (warp - 2) * EPI_WARP_BYTES;
-        uint8_t* box_ptr = tile_ptr + Tr::epi_off + (warp - 2) * EPI_WARP_BYTES;
+        const uint32_t box = tile_base + Tr::stages * Tr::stage_bytes + (warp - 2) * EPI_WARP_BYTES;
+        uint8_t* box_ptr = tile_ptr + Tr::stages * Tr::stage_bytes + (warp - 2) * EPI_WARP_BYTES;
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           float v[32];
           if (it.kblocks > 0) {
@@ -748,58 +698,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (MODE != GATE) {
       if (lane == 0) bulk_wait_all();   // stores done before the CTA's shared memory goes away
       __syncwarp();
-    }
-  } else if (Tr::f8a && warp >= 2 + EPI_WARPS) {
-    // ------------------------------------------------------------ fp8 -> bf16 converters
-    // Thread r converts row r of this CTA's 128 A rows: 64 codes of the stage's
-    // code tile (row r at r * 64) times the row's scale for the k-block's
-    // 128-channel block, into row r of a converted tile (16-B chunk j at
-    // r * 128 + (j ^ (r & 7)) * 16, the 128-B swizzle of a TMA box).  Rows at
-    // or past N were zero-filled by the TMA and get scale 0.
-    const int r = (int)threadIdx.x - 32 * (2 + EPI_WARPS);
-    const int rrow = (int)rank * BM;
-    const int nb = g.d / 128;
-    uint32_t it_count = 0;
-    bool ok = true;
-    for (int item = first_item; item < total && ok; item += item_step) {
-      Item it;
-      decode_item(g, MODE, item, it);
-      const int grow = it.row0 + rrow + r;
-      const bool live = grow < g.N;
-      const float* srow = g.a_scale + (size_t)(live ? grow : 0) * nb;
-      float sc = live ? __ldg(srow) : 0.f;
-      for (int kb = 0; kb < it.kblocks; ++kb, ++it_count) {
-        // the next k-block's scale, requested before the waits
-        const float sc_next =
-            (live && kb + 1 < it.kblocks) ? __ldg(srow + ((kb + 1) * BK) / 128) : 0.f;
-        const int s = it_count % Tr::stages;
-        const uint32_t ph = (it_count / Tr::stages) & 1u;
-        const int cb = it_count % Tr::conv_bufs;
-        const uint32_t cph = (it_count / Tr::conv_bufs) & 1u;
-        ok = mbar_wait_bounded(smem_u32(&ctl->afull[s]), ph, abort_flag, g.err);
-        if (ok) ok = mbar_wait_bounded(smem_u32(&ctl->cempty[cb]), cph ^ 1u, abort_flag, g.err);
-        ok = __all_sync(kFull, ok);
-        if (!ok) break;
-        const uint8_t* src = tile_ptr + s * Tr::stage_bytes + r * 64;
-        uint8_t* dst = tile_ptr + Tr::conv_off + cb * A_BYTES + r * 128;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 q = *reinterpret_cast<const uint4*>(src + 16 * i);
-          float f[8];
-          e4m3x8_scaled(make_uint2(q.x, q.y), sc, f);
-          *reinterpret_cast<uint4*>(dst + (((2 * i) ^ (r & 7)) * 16)) = pack8(f);
-          e4m3x8_scaled(make_uint2(q.z, q.w), sc, f);
-          *reinterpret_cast<uint4*>(dst + (((2 * i + 1) ^ (r & 7)) * 16)) = pack8(f);
-        }
-        fence_proxy_async_smem();   // visible to the tensor core (async proxy)
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t cf = smem_u32(&ctl->cfull[cb]);
-          if (C2 && !leader) mbar_arrive_cluster(mapa_shared(cf, 0));
-          else mbar_arrive(cf);
-        }
-        sc = sc_next;
-      }
     }
   }
 
@@ -931,19 +829,6 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// uint8 matrix [rows, cols], box {64 cols, box_rows}, no swizzle: fp8 codes.
-bool make_map_u8(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols};
-  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // fp32 [E, rows, cols] (dense), box {32 cols, 32 rows, 1}, 128-B swizzle: output
 // of the weight-gradient epilogue's bulk tensor stores.
 bool make_map_f32_3d(CUtensorMap* m, void* base, long long E, long long rows, long long cols) {
@@ -999,7 +884,7 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(Traits<MODE, C2>::threads);
+  cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
   if (C2) {
@@ -1102,16 +987,13 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
                            void* tiles_ws, int* err, bool prepacked, bool cta_pairs,
-                           cudaStream_t s, const float* row_scale, const uint8_t* xq,
-                           const float* xscale) {
+                           cudaStream_t s, const float* row_scale) {
   if (N == 0) return cudaSuccess;
-  // xq, xscale: A given as block-scaled fp8 rows (GATEUP8); x_perm is unused
-  const bool f8 = xq != nullptr;
   // cta_pairs: 256-row tiles on CTA pairs (tcgen05 .cta_group::2).  Otherwise
   // single-CTA tiles; with few rows per expert (on average at most two 128-row
   // tiles) the layer streams weights, so one CTA takes both 128-row halves of
   // a 256-row block to share each weight tile (GATEUP2 / DOWN2).
-  const bool pair = !cta_pairs && !f8 && (long long)N <= 2LL * BM * E;
+  const bool pair = !cta_pairs && (long long)N <= 2LL * BM * E;
   const int tile_rows = (pair || cta_pairs) ? 2 * BM : BM;
   // On pairs with few rows per expert (on average at most one 256-row tile),
   // an expert's last tile of at most 128 rows runs on one CTA after the pairs
@@ -1140,9 +1022,7 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   // gate-up: A = x_perm, B = W1 / W3 rows (128 per tile each)
   g.prepacked = prepacked ? 1 : 0;
 
-  if (f8 ? !make_map_u8(&ma, xq, N, d, BM) : !make_map(&ma, x_perm, N, d, BM))
-    return cudaErrorInvalidValue;
-  g.a_scale = xscale;
+  if (!make_map(&ma, x_perm, N, d, BM)) return cudaErrorInvalidValue;
   if (prepacked ? !(make_map_tiles(&mb, W1, (long long)E * f / 128, d / 64, 128) &&
                     make_map_tiles(&mb2, W3, (long long)E * f / 128, d / 64, 128))
                 : !(make_map(&mb, W1, (long long)E * f, d, 128) &&
@@ -1158,18 +1038,13 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
   if (a_save && !(make_map(&msa, a_save, N, f, 32) && make_map(&msb, b_save, N, f, 32)))
     return cudaErrorInvalidValue;
   const long long items = max_m_tiles * g.n_tiles_n;
-  if (f8)
-    e = cta_pairs ? launch_mode<GATEUP8, true>(ma, mb, mb2, mh, msa, msb, g, items, s)
-                  : launch_mode<GATEUP8>(ma, mb, mb2, mh, msa, msb, g, items, s);
-  else
-    e = cta_pairs ? launch_mode<GATEUP, true>(ma, mb, mb2, mh, msa, msb, g, items, s)
-        : pair    ? launch_mode<GATEUP2>(ma, mb, mb2, mh, msa, msb, g, items, s)
-                  : launch_mode<GATEUP>(ma, mb, mb2, mh, msa, msb, g, items, s);
+  e = cta_pairs ? launch_mode<GATEUP, true>(ma, mb, mb2, mh, msa, msb, g, items, s)
+      : pair    ? launch_mode<GATEUP2>(ma, mb, mb2, mh, msa, msb, g, items, s)
+                : launch_mode<GATEUP>(ma, mb, mb2, mh, msa, msb, g, items, s);
   if (e == cudaSuccess && split_tails) {
     // one CTA loads a whole 128-row W1 and W3 tile: the same maps as the pairs
     const long long n = tails(gt);
-    e = f8 ? launch_mode<GATEUP8>(ma, mb, mb2, mh, msa, msb, gt, n, s)
-           : launch_mode<GATEUP>(ma, mb, mb2, mh, msa, msb, gt, n, s);
+    e = launch_mode<GATEUP>(ma, mb, mb2, mh, msa, msb, gt, n, s);
   }
   trace_end(MOE_STAGE_GATEUP, s);
   if (e != cudaSuccess) return e;

@@ -32,7 +32,6 @@ struct GemmArgs {
   float* out_f32b;
   const float* bias;
   const float* row_scale;     // down epilogue: out[row] = bf16(row_scale[row] * acc), or null
-  const float* a_scale;       // GATEUP8: fp32 [N, d/128] scales of the fp8 A rows
   int* err;
 };
 
@@ -75,8 +74,7 @@ cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,
                            void* tiles_ws, int* err, bool prepacked, bool cta_pairs,
-                           cudaStream_t s, const float* row_scale = nullptr,
-                           const uint8_t* xq = nullptr, const float* xscale = nullptr);
+                           cudaStream_t s, const float* row_scale = nullptr);
 // Weight tiles for the forward GEMMs: W1p, W3p [E][f/128][d/64][128][64] and
 // W2p [E][d/256][f/64][256][64] (bf16), each tile one TMA box, contiguous.
 bool prepack_supported(int d, int f);

@@ -225,14 +225,14 @@ moe_status_t moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int
 /*
  * moe_grouped_ffn_fp8 -- moe_grouped_ffn on the block-scaled fp8 rows that
  * moe_dispatch_fp8 writes (section "Evaluation": tokens travel in
- * block-scaled fp8).  The gate-up GEMM reads the E4M3 codes and their fp32
- * scales and forms each bf16 input element as bf16(code value * scale) in
- * shared memory, the same arithmetic as moe_dequant_fp8, so every output
- * equals that of moe_dequant_fp8 followed by moe_grouped_ffn, bit for bit,
- * and the bf16 rows are never written to memory.
+ * block-scaled fp8).  The rows are dequantised once, as moe_dequant_fp8 does
+ * (bf16(code value * scale)), into the workspace, and the bf16 grouped FFN
+ * runs on them: every output equals that of moe_dequant_fp8 followed by
+ * moe_grouped_ffn, bit for bit, in one call.
  * xq_perm: uint8 [N, d], 16-byte aligned; xscale_perm: fp32 [N, d/128];
- * d must be a multiple of 128 (else MOE_ERR_UNSUPPORTED).  Every other
- * argument, the workspace and the flags as for moe_grouped_ffn.
+ * d must be a multiple of 128 (else MOE_ERR_UNSUPPORTED).  The workspace is
+ * that of moe_grouped_ffn plus N * d * 2 bytes (rounded up to 256).  Every
+ * other argument and the flags as for moe_grouped_ffn.
  */
 moe_status_t moe_grouped_ffn_fp8(const uint8_t* xq_perm, const float* xscale_perm,
                                  const int32_t* offsets, int N, int d, int f, int E,

@@ -1,9 +1,8 @@
 """GPU parity: the grouped SwiGLU FFN on block-scaled fp8 rows
-(moe_grouped_ffn_fp8).  Its gate-up GEMM forms each bf16 input element from
-the E4M3 code and the row's 128-channel scale in shared memory, so every
-output must equal, bit for bit, moe_dequant_fp8 followed by the bf16
-moe_grouped_ffn; and both must match the oracle's FFN on the oracle's
-dequantised rows within the layer's tolerance."""
+(moe_grouped_ffn_fp8, which dequantises the rows once into its workspace and
+runs the bf16 grouped FFN).  Every output must equal, bit for bit,
+moe_dequant_fp8 followed by moe_grouped_ffn with caller buffers, and match the
+oracle's FFN on the oracle's dequantised rows within the layer's tolerance."""
 import numpy as np
 import pytest
 import torch
@@ -37,7 +36,7 @@ def _both_paths(B, xq, xs, offsets, W1, W3, W2, flags, row_scale=None, save=True
     """(fp8 GEMM outputs, dequantise-then-bf16 GEMM outputs), each h, out, a, b."""
     N, d = xq.shape
     E, f, _ = W1.shape
-    ws = B.workspace(B.grouped_ffn_ws_bytes(N, d, f, E))
+    ws = B.workspace(B.grouped_ffn_fp8_ws_bytes(N, d, f, E))
 
     def bufs():
         a = torch.empty((N, f), dtype=torch.bfloat16, device="cuda") if save else None
@@ -109,7 +108,7 @@ def test_fp8_ffn_row_scale_prepacked_and_without_saves(lib):
     h = torch.empty_like(got["h"])
     out = torch.empty_like(got["out"])
     lib.moe_grouped_ffn_fp8(xq, xs, offs, W1p, W3p, W2p, h, out,
-                            lib.workspace(lib.grouped_ffn_ws_bytes(N, d, f, E)),
+                            lib.workspace(lib.grouped_ffn_fp8_ws_bytes(N, d, f, E)),
                             flags=lib.MOE_WEIGHTS_PREPACKED | lib.MOE_CHECK, row_scale=rs)
     torch.cuda.synchronize()
     assert _same(h, got["h"]) and _same(out, got["out"])
