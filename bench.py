@@ -52,8 +52,9 @@ def parse():
     p.add_argument("--cpu-tokens", type=int, default=None,
                    help="tokens in the CPU oracle sample (default per workload)")
     p.add_argument("--fp8", action="store_true",
-                   help="dispatch workloads: block-scaled fp8 dispatch (E4M3 + per-128 scales), "
-                        "dequantising identity experts, bf16 combine")
+                   help="block-scaled fp8 dispatch (E4M3 + per-128 scales), bf16 combine: "
+                        "dispatch workloads dequantise in identity experts; layer workloads "
+                        "pass MOE_FP8_DISPATCH (the GEMMs read the dequantised rows)")
     p.add_argument("--no-prepack", action="store_true",
                    help="forward-only workloads: stream the plain weight layout instead of the "
                         "tiles moe_prepack_weights writes once before timing")
@@ -149,11 +150,14 @@ def stage_work(wl, fp8=False, shared_fs=0):
     """
     T, d, E, R, f = wl.T, wl.d, wl.E, wl.R, wl.f
     N = T * R
+    q8 = N * d + 4.0 * N * d / 128          # fp8 codes and their scales
+    # fp8 in a layer: the codes and scales are written, read back and the bf16
+    # rows the GEMMs read are written, all inside the dispatch stage
+    disp = (2.0 * N * d if not fp8 else q8 if not f else 2.0 * q8 + 2.0 * N * d)
     w = {
         "gate": ("tflop3" if d % 64 == 0 else "alu", 2.0 * T * d * E),
         "topk": ("gb", 4.0 * T * E + 8.0 * N),
-        "dispatch": ("gb", 2.0 * T * d + (N * d + 4.0 * N * d / 128 if fp8 else 2.0 * N * d)
-                     + 4.0 * N * 3),
+        "dispatch": ("gb", 2.0 * T * d + disp + 4.0 * N * 3),
         "combine": ("gb", 2.0 * N * d + 8.0 * N + 2.0 * T * d),
     }
     if f:
@@ -253,7 +257,7 @@ def run_ours(args, rank, world, device):
         inp = synth.layer_inputs(wl, device=device, weight_device=device if big else "cpu")
         train = wl.train
         gemm_flags = B.MOE_SINGLE_CTA_TILES if args.single_cta else 0
-        fwd_flags = gemm_flags
+        fwd_flags = gemm_flags | (B.MOE_FP8_DISPATCH if args.fp8 else 0)
         weights_note = "plain [E, out, in]"
         if (not train and not args.no_prepack and wl.d % 256 == 0 and wl.f % 128 == 0):
             # inference: the weights are laid out once (like loading a model), outside the timing
@@ -282,7 +286,7 @@ def run_ours(args, rank, world, device):
         saved = B.Saved(layer, device, train=train)
         x = inp["x"]
         y = torch.empty_like(x)
-        fws = B.workspace(B.layer_fwd_ws_bytes(layer), device)
+        fws = B.workspace(B.layer_fwd_ws_bytes(layer, fwd_flags), device)
         if train:
             g = inp["g"]
             dx = torch.empty_like(x)

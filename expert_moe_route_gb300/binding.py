@@ -20,6 +20,7 @@ MOE_CHECK = 0x2
 MOE_WEIGHTS_PREPACKED = 0x4
 MOE_SINGLE_CTA_TILES = 0x8
 MOE_SHARED_SERIAL = 0x10
+MOE_FP8_DISPATCH = 0x20
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CUDA"}
 
@@ -355,10 +356,10 @@ class Saved:
         self.c = moe_saved_t(*[_p(getattr(self, n)) for n, _ in moe_saved_t._fields_])
 
 
-def layer_fwd_ws_bytes(layer: Layer) -> int:
+def layer_fwd_ws_bytes(layer: Layer, flags=0) -> int:
     n = ctypes.c_size_t(0)
-    _check(lib().moe_layer_fwd(ctypes.byref(layer.c), None, None, None, None, ctypes.byref(n), 0,
-                               None), "moe_layer_fwd(ws query)")
+    _check(lib().moe_layer_fwd(ctypes.byref(layer.c), None, None, None, None, ctypes.byref(n),
+                               flags, None), "moe_layer_fwd(ws query)")
     return n.value
 
 

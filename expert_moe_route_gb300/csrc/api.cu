@@ -442,10 +442,17 @@ static size_t shared_fwd_ws(const moe_layer_t* L) {
   return 256 + tiles_ws_bytes((int)T, 1) + align_up(T * d * 2, 256) + align_up(T * fs * 2, 256);
 }
 
-static size_t layer_fwd_ws(const moe_layer_t* L) {
+// fp8 dispatch (MOE_FP8_DISPATCH): the rows' E4M3 codes and their scales.
+static size_t fp8_rows_ws(const moe_layer_t* L) {
+  const size_t N = (size_t)L->T * L->R, d = L->d;
+  return align_up(N * d, 256) + align_up(N * (d / 128) * 4, 256);
+}
+
+static size_t layer_fwd_ws(const moe_layer_t* L, unsigned flags) {
   const int N = L->T * L->R;
   return kErrBytes + align_up(dispatch_ws_bytes(L->T, L->E), 256) + tiles_ws_bytes(N, L->E) +
-         align_up(gate_ws_bytes(L->d, L->E), 256) + shared_fwd_ws(L);
+         align_up(gate_ws_bytes(L->d, L->E), 256) + shared_fwd_ws(L) +
+         ((flags & MOE_FP8_DISPATCH) ? fp8_rows_ws(L) : 0);
 }
 
 moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
@@ -454,8 +461,10 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   moe_status_t st = check_layer(L);
   if (st != MOE_OK) return st;
   if ((flags & MOE_WEIGHTS_PREPACKED) && !prepack_supported(L->d, L->f)) return MOE_ERR_UNSUPPORTED;
+  const bool fp8 = (flags & MOE_FP8_DISPATCH) != 0;
+  if (fp8 && L->d % 128) return MOE_ERR_UNSUPPORTED;
   if (!ws_bytes) return MOE_ERR_INVALID_ARG;
-  const size_t need = layer_fwd_ws(L);
+  const size_t need = layer_fwd_ws(L, flags);
   if (!ws) {
     *ws_bytes = need;
     return MOE_OK;
@@ -486,6 +495,12 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   void* dws = c.take(dispatch_ws_bytes(T, E));
   void* tws = c.take(tiles_ws_bytes(N, E));
   void* gws = c.take(gate_ws_bytes(d, E));
+  uint8_t* xq = nullptr;
+  float* xs = nullptr;
+  if (fp8) {
+    xq = static_cast<uint8_t*>(c.take((size_t)N * d));
+    xs = static_cast<float*>(c.take((size_t)N * (d / 128) * 4));
+  }
   int32_t* s_off = nullptr;
   void* s_tws = nullptr;
   uint16_t *s_out = nullptr, *s_h = nullptr;
@@ -523,8 +538,14 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   }
   {
     Stage st_(s, MOE_STAGE_DISPATCH);
-    MOE_TRY(launch_dispatch(x, sv->topk_idx, T, d, E, R, sv->counts, sv->offsets, sv->row_slot,
-                            sv->slot_row, sv->x_perm, dws, err, s));
+    if (fp8) {   // the rows travel as fp8 codes and scales; the GEMMs read them dequantised
+      MOE_TRY(launch_dispatch_fp8(x, sv->topk_idx, T, d, E, R, sv->counts, sv->offsets,
+                                  sv->row_slot, sv->slot_row, xq, xs, dws, err, s));
+      MOE_TRY(launch_dequant_fp8(xq, xs, N, d, sv->x_perm, s));
+    } else {
+      MOE_TRY(launch_dispatch(x, sv->topk_idx, T, d, E, R, sv->counts, sv->offsets, sv->row_slot,
+                              sv->slot_row, sv->x_perm, dws, err, s));
+    }
   }
   MOE_TRY(launch_ffn_fwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
                          sv->h, sv->o, tws, err, (flags & MOE_WEIGHTS_PREPACKED) != 0, pairs, s));

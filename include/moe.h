@@ -74,6 +74,12 @@ typedef void* moe_stream_t;  /* cudaStream_t */
                                        caller's stream after the routed path instead of on the
                                        library's side stream beside it (same results, bit for
                                        bit; for comparison) */
+#define MOE_FP8_DISPATCH 0x20u      /* moe_layer_fwd: dispatch the tokens in block-scaled fp8
+                                       (as moe_dispatch_fp8) and give the grouped FFN their
+                                       dequantised rows (as moe_dequant_fp8), which saved->x_perm
+                                       keeps (a backward treats the quantisation as the
+                                       identity); needs d % 128 == 0 and a workspace queried
+                                       with this flag */
 
 /* Stages of moe_layer_fwd / moe_layer_bwd, for moe_trace_events. */
 typedef enum {

@@ -103,6 +103,16 @@ def test_layer_ws_query_and_bwd_shape_limits():
     L2 = B.moe_layer_t(256, 520, 8, 2, 1024, 8, 0, 16, 32, 48)   # d % 64 != 0: no backward
     assert lib.moe_layer_bwd(ctypes.byref(L2), None, None, None, None, None, None, None, None,
                              None, ctypes.byref(n), 0, None) == 2
+    # fp8 dispatch in the forward: its workspace adds the codes (N*d B) and
+    # scales (4*N*d/128 B) of N = 512 rows; d % 128 != 0 is refused
+    plain, fp8 = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.moe_layer_fwd(ctypes.byref(L), None, None, None, None, ctypes.byref(plain), 0,
+                             None) == 0
+    assert lib.moe_layer_fwd(ctypes.byref(L), None, None, None, None, ctypes.byref(fp8),
+                             B.MOE_FP8_DISPATCH, None) == 0
+    assert fp8.value - plain.value == 512 * 512 + 512 * 4 * 4
+    assert lib.moe_layer_fwd(ctypes.byref(L2), None, None, None, None, ctypes.byref(fp8),
+                             B.MOE_FP8_DISPATCH, None) == 2
 
 
 def test_no_cpu_fallback_without_gpu():

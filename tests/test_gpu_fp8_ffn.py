@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 import torch
 
+from expert_moe_route_gb300 import synth
 from oracle import moe_oracle as O
 from tests.helpers import assert_close, bits, f64, random_routing
 
@@ -154,3 +155,50 @@ def test_fp8_ffn_full_size_equals_dequantised_path(lib, T, d, E, R, f, skew):
     assert _same(got["h"], want["h"]) and _same(got["out"], want["out"])
     del W1, W3, W2
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,over", [("mid", dict(T=1024)), ("train", dict(T=512))])
+def test_layer_forward_with_fp8_dispatch(lib, name, over):
+    """MOE_FP8_DISPATCH: the layer's rows travel as fp8 and the GEMMs read them
+    dequantised -- the same bits as the separate calls on the layer's routing,
+    and the oracle's layer on fp8-quantised rows."""
+    wl = synth.workload(name, **over)
+    inp = synth.layer_inputs(wl)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    T, d, E, R, f = wl.T, wl.d, wl.E, wl.R, wl.f
+    N = T * R
+    layer = lib.Layer(dev["w_gate"], dev["bias"], dev["W1"], dev["W3"], dev["W2"], R, T)
+    saved = lib.Saved(layer, "cuda", train=False)
+    y = torch.empty_like(dev["x"])
+    flags = lib.MOE_FP8_DISPATCH
+    assert lib.layer_fwd_ws_bytes(layer, flags) > lib.layer_fwd_ws_bytes(layer)
+    lib.moe_layer_fwd(layer, dev["x"], y, saved, lib.workspace(lib.layer_fwd_ws_bytes(layer, flags)),
+                      flags=flags | lib.MOE_CHECK)
+    torch.cuda.synchronize()
+    # the separate calls on the layer's routing
+    i32 = dict(dtype=torch.int32, device="cuda")
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    row_slot, slot_row = torch.empty(N, **i32), torch.empty(N, **i32)
+    xq = torch.empty((N, d), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((N, d // 128), dtype=torch.float32, device="cuda")
+    lib.moe_dispatch_fp8(dev["x"], saved.topk_idx, E, counts, offsets, row_slot, slot_row, xq, xs,
+                         lib.workspace(lib.dispatch_ws_bytes(T, d, E, R)), flags=lib.MOE_CHECK)
+    xd = torch.empty((N, d), dtype=torch.bfloat16, device="cuda")
+    lib.moe_dequant_fp8(xq, xs, xd)
+    h = torch.empty((N, f), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty((N, d), dtype=torch.bfloat16, device="cuda")
+    lib.moe_grouped_ffn(xd, offsets, dev["W1"], dev["W3"], dev["W2"], h, o,
+                        lib.workspace(lib.grouped_ffn_ws_bytes(N, d, f, E)), flags=lib.MOE_CHECK)
+    y2 = torch.empty_like(y)
+    lib.moe_combine(o, slot_row, saved.topk_w, y2, R)
+    torch.cuda.synchronize()
+    assert _same(saved.x_perm, xd)
+    assert _same(y, y2)
+    # the oracle: the layer's routing, the oracle's quantiser, its FFN and combine
+    idx = saved.topk_idx.cpu().numpy()
+    _, offs, rs, sr = O.dispatch_plan(idx, E)
+    codes, scales = O.quantize_fp8_blocks(bits(inp["x"]))
+    xp = O.bf16_round(O.dequantize_fp8_blocks(codes, scales))[rs // R]
+    o_ref = O.expert_ffn(xp, offs, bits(inp["W1"]), bits(inp["W3"]), bits(inp["W2"]))[3]
+    y_ref = O.combine(o_ref, sr, saved.topk_w.cpu().numpy(), T, R)
+    assert_close(f64(y), y_ref, "y (fp8 dispatch)")
