@@ -87,6 +87,11 @@ struct alignas(8) SharedCtl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
+  // C2 weight-gradient modes, a k-block whose last 16-row group is partial:
+  // rank 1's loads land on its own lfull[s]; rank 1 zeroes its foreign rows
+  // and arrives on rank 0's pfix[s]
+  uint64_t lfull[MAX_STAGES];
+  uint64_t pfix[MAX_STAGES];
   uint32_t tmem_base;
   int abort;
 };
@@ -129,6 +134,26 @@ __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int ite
   it.krow0 = it.krows = 0;
   it.kblocks = g.kblocks;
   return true;
+}
+
+// Weight-gradient modes: k-block kb of an item ends inside a 16-row group
+// (rows past the expert's end share the group with its last rows), so those
+// rows must be zeroed in shared memory before that group's MMA.
+__device__ __forceinline__ bool needs_fix(const Item& it, int kb) {
+  const int rem = it.krows - kb * BK;
+  return rem < BK && (rem & 15) != 0;
+}
+
+// Zero rows rem .. (rem rounded up to 16) - 1 of each of the stage's `atoms`
+// 64-element blocks (rows of 128 B), lane-strided across the warp.
+__device__ __forceinline__ void zero_foreign_rows(uint8_t* stage, int atoms, int rem, int lane) {
+  const int z1 = (rem + 15) & ~15;
+  const int per_atom = (z1 - rem) * 8;   // 16-B chunks per block
+  uint8_t* base = stage + rem * 128;
+  for (int atom = 0; atom < atoms; ++atom)
+    for (int w = lane; w < per_atom; w += 32)
+      *reinterpret_cast<uint4*>(base + atom * ATOM_BYTES + (w >> 3) * 128 + (w & 7) * 16) =
+          make_uint4(0, 0, 0, 0);
 }
 
 __device__ __forceinline__ int total_items(const GemmArgs& g, int mode) {
@@ -180,6 +205,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       mbar_init(smem_u32(&ctl->tempty[a]), C2 ? 2 * EPI_WARPS : EPI_WARPS);
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
+    if (C2 && Tr::wgrad) {
+      for (int s = 0; s < Tr::stages; ++s) {
+        mbar_init(smem_u32(&ctl->lfull[s]), 1);
+        mbar_init(smem_u32(&ctl->pfix[s]), 1);
+      }
+    }
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -235,7 +266,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t bar = C2 ? mapa_shared(bar_local, 0) : bar_local;
           const uint32_t sa = tile_base + s * Tr::stage_bytes;
           const uint32_t sb = sa + Tr::a_bytes;
-          if (leader) mbar_arrive_expect_tx(bar_local, Tr::stage_tx);
+          // C2 k-block to fix: each CTA's loads land on its own barrier (rank 0's
+          // full barrier then counts rank 0's bytes only)
+          const bool fix = C2 && Tr::wgrad && needs_fix(it, kb);
+          if (leader) mbar_arrive_expect_tx(bar_local, fix ? (uint32_t)Tr::stage_bytes : Tr::stage_tx);
           const int kx = kb * BK;
           if (Tr::pair) tma_load_2d(sa + A_BYTES, &tmA, bar, kx, it.row0 + BM);   // rows 128-255
           if (Tr::is_gateup) {
@@ -282,6 +316,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
             for (int j = 0; j < Tr::b_bytes / ATOM_BYTES; ++j)
               ld2(sb + j * ATOM_BYTES, first ? &tmB : &tmB2, bar, it.nt * BN + rcol + j * 64, krow);
+          } else if (fix && !leader) {   // WG2 / WG13, rank 1: onto its own barrier
+            const int krow = it.krow0 + kx;
+            const uint32_t lbar = smem_u32(&ctl->lfull[s]);
+            mbar_arrive_expect_tx(lbar, Tr::stage_bytes);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d(sa + j * ATOM_BYTES, &tmA, lbar, it.mt * Tr::tile_m + rrow + j * 64, krow);
+#pragma unroll
+            for (int j = 0; j < Tr::b_bytes / ATOM_BYTES; ++j)
+              tma_load_2d(sb + j * ATOM_BYTES, &tmB, lbar, it.nt * BN + rcol + j * 64, krow);
           } else {  // WG2 / WG13: both operands MN-major, K = rows of expert e
             const int krow = it.krow0 + kx;
 #pragma unroll
@@ -314,6 +358,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_bf16(Tr::tile_m, Tr::bn, Tr::a_mn, Tr::b_mn);
     uint32_t it_count = 0;
+    uint32_t pfix_par = 0;   // C2 weight gradients: phase bits of pfix[]
     int j = 0;
     bool ok = true;
     bool issued_any = false;
@@ -338,42 +383,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t sa = tile_base + s * Tr::stage_bytes;
         const uint32_t sb = sa + Tr::a_bytes;
         int kk_end = BK / 16;
+        bool fix = false;
         if (Tr::wgrad) {
           // The expert's last K-block may hold rows of the next expert: issue
-          // MMAs only for the 16-row groups that contain real rows, and zero the
-          // foreign rows inside the last of those groups.
+          // MMAs only for the 16-row groups that contain real rows.  Rows past
+          // the expert's end inside the last of those groups are zeroed first:
+          // here, and on a pair by rank 1 in its own shared memory (it arrives
+          // on pfix[s]).
           const int rem = it.krows - kb * BK;
-          if (rem < BK) {
-            kk_end = ceil_div(rem, 16);
-            const int z1 = kk_end * 16;
-            if (rem < z1) {
-              // rows rem .. z1-1 of each of the stage's 64-element blocks (six;
-              // C2: four in each CTA of the pair): (z1 - rem) rows x 8 chunks of
-              // 16 B, lane-strided within a block
-              constexpr int atoms = Tr::stage_bytes / ATOM_BYTES;
-              const int per_atom = (z1 - rem) * 8;
-              const uint32_t base = tile_base + s * Tr::stage_bytes + rem * 128;
-              uint8_t* base_ptr = tile_ptr + s * Tr::stage_bytes + rem * 128;
-#pragma unroll
-              for (int atom = 0; atom < atoms; ++atom)
-                for (int w = lane; w < per_atom; w += 32) {
-                  const uint32_t off = atom * ATOM_BYTES + (w >> 3) * 128 + (w & 7) * 16;
-                  *reinterpret_cast<uint4*>(base_ptr + off) = make_uint4(0, 0, 0, 0);
-                  if (C2) st_shared_cluster_v4(mapa_shared(base + off, 1), make_uint4(0, 0, 0, 0));
-                }
-              fence_proxy_async_smem();
-              if (C2) fence_proxy_async_cluster();
-            }
-          }
-          __syncwarp();
+          if (rem < BK) kk_end = ceil_div(rem, 16);
+          fix = needs_fix(it, kb);
         }
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t d_tmem = Tr::partials ? tmem_base + (kb & 3) * 128 : d_base;
-          const bool first = Tr::partials ? kb < 4 : kb == 0;
+        const uint32_t d_tmem = Tr::partials ? tmem_base + (kb & 3) * 128 : d_base;
+        const bool first = Tr::partials ? kb < 4 : kb == 0;
+        auto issue = [&](int kk0, int kk1) {   // 16-deep K groups kk0 .. kk1-1 (one lane)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            if (kk >= kk_end) break;
+            if (kk < kk0) continue;
+            if (kk >= kk1) break;
             const uint64_t ad = Tr::a_mn ? smem_desc_sw128(sa + kk * 2048, ATOM_BYTES, 1024)
                                          : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, ATOM_BYTES, 1024)
@@ -384,11 +411,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               tc_mma_bf16(tmem_base + BN, smem_desc_sw128(sa + A_BYTES + kk * 32, 16, 1024), bd,
                           idesc, (!first || kk > 0) ? 1u : 0u);
           }
+        };
+        if (fix) {
+          zero_foreign_rows(tile_ptr + s * Tr::stage_bytes, Tr::stage_bytes / ATOM_BYTES,
+                            it.krows - kb * BK, lane);
+          fence_proxy_async_smem();   // the zeros, before the tensor core reads the group
+          if (C2) {
+            // rank 1's half of this k-block landed on its own barrier: its arrival
+            // here says the data is in and its foreign rows are zero
+            ok = mbar_wait_bounded_cluster(smem_u32(&ctl->pfix[s]), (pfix_par >> s) & 1u,
+                                           abort_flag, g.err);
+            pfix_par ^= 1u << s;
+            ok = __all_sync(kFull, ok);
+          }
+          __syncwarp();
+        }
+        if (ok && lane == 0) {
+          tc_fence_after();
+          issue(0, kk_end);
+          issued_any = true;
           // frees the stage (C2: in both CTAs) when these MMAs finish
           if (C2) tc_commit_pair(smem_u32(&ctl->empty[s]), 3);
           else tc_commit(smem_u32(&ctl->empty[s]));
-          issued_any = true;
         }
+        if (!ok) break;   // (warp-uniform)
         __syncwarp();
       }
       if (!ok) break;
@@ -412,6 +458,31 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       mbar_wait_bounded(smem_u32(&ctl->mma_done), 0, &never, nullptr);
     }
     __syncwarp();
+  } else if (C2 && Tr::wgrad && warp == 1) {
+    // ------------------------------------------------------------ rank 1: foreign rows
+    // For each item's last k-block that ends inside a 16-row group, this CTA's
+    // loads land on lfull[s]; zero the rows past the expert's end in this
+    // CTA's blocks and tell rank 0 (release at cluster scope, after the proxy
+    // fence, so its MMAs see the zeros).
+    uint32_t it_count = 0, par = 0;
+    for (int item = first_item; item < total; item += item_step) {
+      Item it;
+      decode_item(g, MODE, item, it);
+      const int kb = it.kblocks - 1;
+      if (kb >= 0 && needs_fix(it, kb)) {
+        const int s = (int)((it_count + kb) % Tr::stages);
+        bool ok = mbar_wait_bounded(smem_u32(&ctl->lfull[s]), (par >> s) & 1u, abort_flag, g.err);
+        par ^= 1u << s;
+        ok = __all_sync(kFull, ok);
+        if (!ok) break;
+        zero_foreign_rows(tile_ptr + s * Tr::stage_bytes, Tr::stage_bytes / ATOM_BYTES,
+                          it.krows - kb * BK, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->pfix[s]), 0));
+      }
+      it_count += it.kblocks;
+    }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
