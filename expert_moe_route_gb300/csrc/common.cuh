@@ -175,10 +175,6 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Wait until at most one committed bulk group still reads shared memory.
-__device__ __forceinline__ void bulk_wait_read_1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
 // Wait until no committed bulk group still reads shared memory.
 __device__ __forceinline__ void bulk_wait_read_0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -307,14 +303,6 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// 16 bytes into the shared memory of another CTA of the cluster.
-__device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
-               ::"r"(cluster_addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 // TMA tile loads into this CTA's shared memory that signal an mbarrier of
 // either CTA of the pair (`bar` is a cluster-window address).

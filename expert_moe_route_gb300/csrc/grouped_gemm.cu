@@ -11,14 +11,18 @@
 //   DX      dx_perm = bf16([da|db] [W1[e]; W3[e]])
 //   WG2     dW2[e] = do^T h                     (K = the expert's rows, ragged)
 //   WG13    [dW1[e]; dW3[e]] = [da|db]^T x_perm (K ragged)
-// Roles (320 threads): warp 0 issues TMA loads into a 4-stage shared-memory
-// ring, warp 1 owns TMEM and issues tcgen05.mma (128 x 256 x 16, bf16 in, fp32
-// accumulate), warps 2-9 drain the accumulator (tcgen05.ld; two warps per TMEM
-// lane quadrant, each taking half of the columns) and run the
-// epilogue.  Two 256-column TMEM accumulators let the epilogue of one tile
-// overlap the main loop of the next.  Every wait is bounded (kWaitLimitNs);
-// a timeout sets the error word and all roles return after their in-flight
-// copies and MMAs have drained.
+// Roles (320 threads): warp 0 issues TMA loads into a shared-memory ring,
+// warp 1 owns TMEM and issues tcgen05.mma (bf16 in, fp32 accumulate), warps
+// 2-9 drain the accumulator (tcgen05.ld; two warps per TMEM lane quadrant,
+// each taking half of the columns) and run the epilogue.  Two 256-column TMEM
+// accumulators let the epilogue of one tile overlap the main loop of the next.
+// By default a cluster of two CTAs computes 256 x 256 tiles with
+// tcgen05.mma.cta_group::2 (each CTA stages 128 rows of A and 128 columns of
+// B, six 32 KB stages; rank 0 issues the MMAs, rank 1's warp 1 zeroes its own
+// foreign rows in the weight-gradient modes); single-CTA kernels compute
+// 128 x 256 tiles from four 48 KB stages.  Every wait is bounded
+// (kWaitLimitNs); a timeout sets the error word and all roles return after
+// their in-flight copies and MMAs have drained.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
