@@ -24,18 +24,6 @@ static void trace_record(int slot, cudaStream_t s) {
 }
 void trace_begin(int stage, cudaStream_t s) { trace_record(2 * stage, s); }
 void trace_end(int stage, cudaStream_t s) { trace_record(2 * stage + 1, s); }
-}  // namespace moe
-
-using namespace moe;
-
-namespace {
-
-constexpr size_t kErrBytes = 256;   // device error word, at the start of every workspace
-
-inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
-
-inline cudaStream_t S(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 moe_status_t shape_check(int T, int d, int E, int R) {
   if (T < 0 || d <= 0 || E <= 0 || R <= 0) return MOE_ERR_INVALID_ARG;
@@ -45,20 +33,8 @@ moe_status_t shape_check(int T, int d, int E, int R) {
   return MOE_OK;
 }
 
-bool init_once() {
-  static int done[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (dev < 0 || dev >= 64) return false;
-  if (!done[dev]) {
-    if (dispatch_set_smem_limits() != cudaSuccess) return false;
-    done[dev] = 1;
-  }
-  return true;
-}
-
 // The CUDA error behind this thread's last MOE_ERR_CUDA (moe_last_cuda_error).
-thread_local int g_last_cuda = 0;
+static thread_local int g_last_cuda = 0;
 
 moe_status_t cuda_failed(cudaError_t e) {
   g_last_cuda = (int)e;
@@ -78,6 +54,30 @@ moe_status_t finish(cudaError_t launched, const int* err_dev, unsigned flags, cu
   if (h & kErrTimeout) return MOE_ERR_TIMEOUT;
   if (h & kErrBadRouting) return MOE_ERR_BAD_ROUTING;
   return MOE_OK;
+}
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kErrBytes = 256;   // device error word, at the start of every workspace
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+inline cudaStream_t S(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool init_once() {
+  static int done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev < 0 || dev >= 64) return false;
+  if (!done[dev]) {
+    if (dispatch_set_smem_limits() != cudaSuccess) return false;
+    done[dev] = 1;
+  }
+  return true;
 }
 
 struct Carve {

@@ -136,6 +136,21 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Tensor maps written on the device: the writer sets one outer extent with
+// tensormap.replace and releases it to the tensor-map proxy; a kernel that
+// loads through such a map acquires it first.
+__device__ __forceinline__ void tensormap_set_dim1(void* gmap, int extent) {
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;"
+               ::"l"(reinterpret_cast<uint64_t>(gmap)), "r"(extent) : "memory");
+}
+__device__ __forceinline__ void tensormap_release() {
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void tensormap_acquire(const void* gmap) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;"
+               ::"l"(reinterpret_cast<uint64_t>(gmap)) : "memory");
+}
+
 // 2-D tiled load of a box at (x = inner element index, y = row) into shared
 // memory; completion is signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int x,

@@ -8,7 +8,9 @@
 // synchronisation is not acceptable.  For them this variant of moe_dispatch
 // keeps its scratch (per-block expert histograms, their scan and the device
 // error word) in a file-scope device array of fixed size, which every GPU that
-// loads the library holds until the process exits.
+// loads the library holds until the process exits.  Its argument checks,
+// status codes, recorded CUDA errors and trace events are those of
+// moe_dispatch.
 #include <mutex>
 
 #include "common.cuh"
@@ -56,9 +58,8 @@ extern "C" moe_status_t moe_dispatch_noalloc(const uint16_t* x, const int32_t* t
                                              int32_t* offsets, int32_t* row_slot,
                                              int32_t* slot_row, uint16_t* x_perm, unsigned flags,
                                              moe_stream_t stream) {
-  if (T < 0 || d <= 0 || E <= 0 || R <= 0 || R > E) return MOE_ERR_INVALID_ARG;
-  if (R > 32 || E > 1024 || d % 8 != 0 || (long long)T * R >= (1LL << 31))
-    return MOE_ERR_UNSUPPORTED;
+  moe_status_t st = moe::shape_check(T, d, E, R);
+  if (st != MOE_OK) return st;
   // the static scratch must hold the error word and the histograms of this call
   if (kErrBytes + moe::dispatch_ws_bytes(T, E) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
   if (!counts || !offsets || (T > 0 && (!topk_idx || !row_slot || !slot_row)))
@@ -66,20 +67,16 @@ extern "C" moe_status_t moe_dispatch_noalloc(const uint16_t* x, const int32_t* t
   if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
   if (x && (!al16(x) || !al16(x_perm))) return MOE_ERR_UNSUPPORTED;
   void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) return moe::cuda_failed(e);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(scratch);
   // the array keeps the previous call's contents: the error word must start at zero
-  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t e = moe::launch_dispatch(x, topk_idx, T, d, E, R, counts, offsets, row_slot,
-                                       slot_row, x_perm, static_cast<uint8_t*>(scratch) + kErrBytes,
-                                       err, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (!(flags & MOE_CHECK)) return MOE_OK;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
-  int h = 0;
-  if (cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  if (h & moe::kErrTimeout) return MOE_ERR_TIMEOUT;
-  if (h & moe::kErrBadRouting) return MOE_ERR_BAD_ROUTING;
-  return MOE_OK;
+  e = cudaMemsetAsync(err, 0, sizeof(int), s);
+  if (e != cudaSuccess) return moe::cuda_failed(e);
+  moe::trace_begin(MOE_STAGE_DISPATCH, s);
+  e = moe::launch_dispatch(x, topk_idx, T, d, E, R, counts, offsets, row_slot, slot_row, x_perm,
+                           static_cast<uint8_t*>(scratch) + kErrBytes, err, s);
+  moe::trace_end(MOE_STAGE_DISPATCH, s);
+  return moe::finish(e, err, flags, s);
 }

@@ -18,9 +18,11 @@
 // accumulators let the epilogue of one tile overlap the main loop of the next.
 // By default a cluster of two CTAs computes 256 x 256 tiles with
 // tcgen05.mma.cta_group::2 (each CTA stages 128 rows of A and 128 columns of
-// B, six 32 KB stages; rank 0 issues the MMAs, rank 1's warp 1 zeroes its own
-// foreign rows in the weight-gradient modes); single-CTA kernels compute
-// 128 x 256 tiles from four 48 KB stages.  Every wait is bounded
+// B, six 32 KB stages; rank 0 issues the MMAs); single-CTA kernels compute
+// 128 x 256 tiles from four 48 KB stages.  The weight-gradient modes contract
+// over each expert's rows: an expert's last, partial k-block is loaded through
+// tensor maps whose row extent ends at the expert's last row, so the rows of
+// the next expert arrive as zeros.  Every wait is bounded
 // (kWaitLimitNs); a timeout sets the error word and all roles return after
 // their in-flight copies and MMAs have drained.
 #include <cudaTypedefs.h>
@@ -91,11 +93,6 @@ struct alignas(8) SharedCtl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
-  // C2 weight-gradient modes, a k-block whose last 16-row group is partial:
-  // rank 1's loads land on its own lfull[s]; rank 1 zeroes its foreign rows
-  // and arrives on rank 0's pfix[s]
-  uint64_t lfull[MAX_STAGES];
-  uint64_t pfix[MAX_STAGES];
   uint32_t tmem_base;
   int abort;
 };
@@ -138,26 +135,6 @@ __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int ite
   it.krow0 = it.krows = 0;
   it.kblocks = g.kblocks;
   return true;
-}
-
-// Weight-gradient modes: k-block kb of an item ends inside a 16-row group
-// (rows past the expert's end share the group with its last rows), so those
-// rows must be zeroed in shared memory before that group's MMA.
-__device__ __forceinline__ bool needs_fix(const Item& it, int kb) {
-  const int rem = it.krows - kb * BK;
-  return rem < BK && (rem & 15) != 0;
-}
-
-// Zero rows rem .. (rem rounded up to 16) - 1 of each of the stage's `atoms`
-// 64-element blocks (rows of 128 B), lane-strided across the warp.
-__device__ __forceinline__ void zero_foreign_rows(uint8_t* stage, int atoms, int rem, int lane) {
-  const int z1 = (rem + 15) & ~15;
-  const int per_atom = (z1 - rem) * 8;   // 16-B chunks per block
-  uint8_t* base = stage + rem * 128;
-  for (int atom = 0; atom < atoms; ++atom)
-    for (int w = lane; w < per_atom; w += 32)
-      *reinterpret_cast<uint4*>(base + atom * ATOM_BYTES + (w >> 3) * 128 + (w & 7) * 16) =
-          make_uint4(0, 0, 0, 0);
 }
 
 __device__ __forceinline__ int total_items(const GemmArgs& g, int mode) {
@@ -209,12 +186,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       mbar_init(smem_u32(&ctl->tempty[a]), C2 ? 2 * EPI_WARPS : EPI_WARPS);
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
-    if (C2 && Tr::wgrad) {
-      for (int s = 0; s < Tr::stages; ++s) {
-        mbar_init(smem_u32(&ctl->lfull[s]), 1);
-        mbar_init(smem_u32(&ctl->pfix[s]), 1);
-      }
-    }
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -256,9 +227,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       };
       const int rrow = (int)rank * BM;        // this CTA's rows of a 256-row tile
       const int rcol = (int)rank * (BN / 2);  // this CTA's half of the B columns
+      const CUtensorMap* emaps = static_cast<const CUtensorMap*>(g.emaps);
+      int acquired_e = -1;   // weight gradients: the expert whose maps this thread acquired
       for (int item = first_item; item < total && ok; item += item_step) {
         Item it;
         decode_item(g, MODE, item, it);
+        if (Tr::wgrad && (it.krows % BK) != 0 && it.e != acquired_e) {
+          // the expert's own maps (written by an earlier kernel), fetched ahead
+          // of the item's last k-block
+          tensormap_acquire(emaps + 2 * it.e);
+          tensormap_acquire(emaps + 2 * it.e + 1);
+          tma_prefetch_desc(emaps + 2 * it.e);
+          tma_prefetch_desc(emaps + 2 * it.e + 1);
+          acquired_e = it.e;
+        }
         for (int kb = 0; kb < it.kblocks; ++kb, ++it_count) {
           const int s = it_count % Tr::stages;
           const uint32_t ph = (it_count / Tr::stages) & 1u;
@@ -270,10 +252,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t bar = C2 ? mapa_shared(bar_local, 0) : bar_local;
           const uint32_t sa = tile_base + s * Tr::stage_bytes;
           const uint32_t sb = sa + Tr::a_bytes;
-          // C2 k-block to fix: each CTA's loads land on its own barrier (rank 0's
-          // full barrier then counts rank 0's bytes only)
-          const bool fix = C2 && Tr::wgrad && needs_fix(it, kb);
-          if (leader) mbar_arrive_expect_tx(bar_local, fix ? (uint32_t)Tr::stage_bytes : Tr::stage_tx);
+          if (leader) mbar_arrive_expect_tx(bar_local, Tr::stage_tx);
           const int kx = kb * BK;
           if (Tr::pair) tma_load_2d(sa + A_BYTES, &tmA, bar, kx, it.row0 + BM);   // rows 128-255
           if (Tr::is_gateup) {
@@ -320,24 +299,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
             for (int j = 0; j < Tr::b_bytes / ATOM_BYTES; ++j)
               ld2(sb + j * ATOM_BYTES, first ? &tmB : &tmB2, bar, it.nt * BN + rcol + j * 64, krow);
-          } else if (fix && !leader) {   // WG2 / WG13, rank 1: onto its own barrier
-            const int krow = it.krow0 + kx;
-            const uint32_t lbar = smem_u32(&ctl->lfull[s]);
-            mbar_arrive_expect_tx(lbar, Tr::stage_bytes);
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_2d(sa + j * ATOM_BYTES, &tmA, lbar, it.mt * Tr::tile_m + rrow + j * 64, krow);
-#pragma unroll
-            for (int j = 0; j < Tr::b_bytes / ATOM_BYTES; ++j)
-              tma_load_2d(sb + j * ATOM_BYTES, &tmB, lbar, it.nt * BN + rcol + j * 64, krow);
           } else {  // WG2 / WG13: both operands MN-major, K = rows of expert e
             const int krow = it.krow0 + kx;
+            // the last k-block of an expert whose rows end inside it: the
+            // expert's maps end at its last row, so the TMA fills the rest of
+            // the box with zeros (the full box's bytes still arrive)
+            const bool last = it.krows - kx < BK;
+            const CUtensorMap* mA = last ? emaps + 2 * it.e : &tmA;
+            const CUtensorMap* mB = last ? emaps + 2 * it.e + 1 : &tmB;
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-              ld2(sa + j * ATOM_BYTES, &tmA, bar, it.mt * Tr::tile_m + rrow + j * 64, krow);
+              ld2(sa + j * ATOM_BYTES, mA, bar, it.mt * Tr::tile_m + rrow + j * 64, krow);
 #pragma unroll
             for (int j = 0; j < Tr::b_bytes / ATOM_BYTES; ++j)
-              ld2(sb + j * ATOM_BYTES, &tmB, bar, it.nt * BN + rcol + j * 64, krow);
+              ld2(sb + j * ATOM_BYTES, mB, bar, it.nt * BN + rcol + j * 64, krow);
           }
         }
       }
@@ -362,7 +337,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_bf16(Tr::tile_m, Tr::bn, Tr::a_mn, Tr::b_mn);
     uint32_t it_count = 0;
-    uint32_t pfix_par = 0;   // C2 weight gradients: phase bits of pfix[]
     int j = 0;
     bool ok = true;
     bool issued_any = false;
@@ -387,16 +361,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t sa = tile_base + s * Tr::stage_bytes;
         const uint32_t sb = sa + Tr::a_bytes;
         int kk_end = BK / 16;
-        bool fix = false;
         if (Tr::wgrad) {
-          // The expert's last K-block may hold rows of the next expert: issue
-          // MMAs only for the 16-row groups that contain real rows.  Rows past
-          // the expert's end inside the last of those groups are zeroed first:
-          // here, and on a pair by rank 1 in its own shared memory (it arrives
-          // on pfix[s]).
+          // An expert's last K-block: MMAs only for the 16-row groups that
+          // hold its rows (the rows past its end were loaded as zeros).
           const int rem = it.krows - kb * BK;
           if (rem < BK) kk_end = ceil_div(rem, 16);
-          fix = needs_fix(it, kb);
         }
         const uint32_t d_tmem = Tr::partials ? tmem_base + (kb & 3) * 128 : d_base;
         const bool first = Tr::partials ? kb < 4 : kb == 0;
@@ -416,21 +385,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                           idesc, (!first || kk > 0) ? 1u : 0u);
           }
         };
-        if (fix) {
-          zero_foreign_rows(tile_ptr + s * Tr::stage_bytes, Tr::stage_bytes / ATOM_BYTES,
-                            it.krows - kb * BK, lane);
-          fence_proxy_async_smem();   // the zeros, before the tensor core reads the group
-          if (C2) {
-            // rank 1's half of this k-block landed on its own barrier: its arrival
-            // here says the data is in and its foreign rows are zero
-            ok = mbar_wait_bounded_cluster(smem_u32(&ctl->pfix[s]), (pfix_par >> s) & 1u,
-                                           abort_flag, g.err);
-            pfix_par ^= 1u << s;
-            ok = __all_sync(kFull, ok);
-          }
-          __syncwarp();
-        }
-        if (ok && lane == 0) {
+        if (lane == 0) {
           tc_fence_after();
           issue(0, kk_end);
           issued_any = true;
@@ -438,7 +393,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           if (C2) tc_commit_pair(smem_u32(&ctl->empty[s]), 3);
           else tc_commit(smem_u32(&ctl->empty[s]));
         }
-        if (!ok) break;   // (warp-uniform)
         __syncwarp();
       }
       if (!ok) break;
@@ -462,31 +416,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       mbar_wait_bounded(smem_u32(&ctl->mma_done), 0, &never, nullptr);
     }
     __syncwarp();
-  } else if (C2 && Tr::wgrad && warp == 1) {
-    // ------------------------------------------------------------ rank 1: foreign rows
-    // For each item's last k-block that ends inside a 16-row group, this CTA's
-    // loads land on lfull[s]; zero the rows past the expert's end in this
-    // CTA's blocks and tell rank 0 (release at cluster scope, after the proxy
-    // fence, so its MMAs see the zeros).
-    uint32_t it_count = 0, par = 0;
-    for (int item = first_item; item < total; item += item_step) {
-      Item it;
-      decode_item(g, MODE, item, it);
-      const int kb = it.kblocks - 1;
-      if (kb >= 0 && needs_fix(it, kb)) {
-        const int s = (int)((it_count + kb) % Tr::stages);
-        bool ok = mbar_wait_bounded(smem_u32(&ctl->lfull[s]), (par >> s) & 1u, abort_flag, g.err);
-        par ^= 1u << s;
-        ok = __all_sync(kFull, ok);
-        if (!ok) break;
-        zero_foreign_rows(tile_ptr + s * Tr::stage_bytes, Tr::stage_bytes / ATOM_BYTES,
-                          it.krows - kb * BK, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->pfix[s]), 0));
-      }
-      it_count += it.kblocks;
-    }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
@@ -806,6 +735,31 @@ __global__ void prepack_kernel(const uint16_t* __restrict__ W, long long rows, i
   }
 }
 
+// Per-expert operand maps of the weight-gradient GEMMs.  Thread i writes map
+// i % 4 of expert e = i / 4: a copy of tmpl.m[i % 4] whose row extent (outer
+// dimension) ends at the expert's last row offsets[e + 1], so that a box
+// reaching past that row reads zeros.  Maps 0, 1 (WG2's A and B) go to
+// out[2e], out[2e + 1]; maps 2, 3 (WG13's) to out[2E + 2e], out[2E + 2e + 1].
+struct MapTemplates {
+  CUtensorMap m[4];
+};
+
+__global__ void __launch_bounds__(256) expert_maps_kernel(const __grid_constant__ MapTemplates tmpl,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int E, CUtensorMap* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 4 * E) return;
+  const int e = i >> 2, m = i & 3;
+  CUtensorMap* dst = out + (m >> 1) * 2 * E + 2 * e + (m & 1);
+  const uint4* src = reinterpret_cast<const uint4*>(&tmpl.m[m]);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int k = 0; k < (int)(sizeof(CUtensorMap) / sizeof(uint4)); ++k) d4[k] = src[k];
+  const int end = offsets[e + 1];
+  tensormap_set_dim1(dst, end > 0 ? end : 1);   // (an empty leading expert's map is never used)
+  tensormap_release();
+}
+
 // Exclusive prefix sum of v over the block's 1024 threads; *total gets the sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -1027,9 +981,18 @@ cudaError_t launch_prepack(const uint16_t* W1, const uint16_t* W3, const uint16_
   return cudaGetLastError();
 }
 
-// Tile-list workspace: [tile count, tail count | E tail entries | tiles].
+// Tile-list workspace: [tile count, tail count | E tail entries | tiles], then
+// (128-B aligned) the weight-gradient GEMMs' per-expert maps, 4 per expert.
+static size_t tile_list_bytes(int N, int E) {
+  return align_up(16 + sizeof(int2) * ((size_t)E + ceil_div(N, BM) + E), 128);
+}
+
 size_t tiles_ws_bytes(int N, int E) {
-  return align_up(16 + sizeof(int2) * ((size_t)E + ceil_div(N, BM) + E), 256);
+  return align_up(tile_list_bytes(N, E) + 4 * sizeof(CUtensorMap) * (size_t)E, 256);
+}
+
+static CUtensorMap* expert_maps(void* ws, int N, int E) {
+  return reinterpret_cast<CUtensorMap*>(static_cast<uint8_t*>(ws) + tile_list_bytes(N, E));
 }
 
 struct TileLists {
@@ -1218,32 +1181,42 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
     trace_end(MOE_STAGE_BWD_DX, s);
     if (e != cudaSuccess) return e;
   }
-  // dW2[e] = do^T h: A = do [N, d] MN-major, B = h [N, f] MN-major
+  // dW2[e] = do^T h: A = do [N, d] MN-major, B = h [N, f] MN-major;
+  // [dW1[e]; dW3[e]] = [da | db]^T x_perm: A = dab [N, 2f], B = x_perm [N, d].
+  // Each expert also gets copies of the four operand maps whose rows end at its
+  // last row (its last k-block then reads zeros past it).
   const long long rows = N > 0 ? N : 1;
-  if (!make_map(&ma, dO, rows, d, 64) || !make_map(&mb, h, rows, f, 64)) return cudaErrorInvalidValue;
+  MapTemplates mt;
+  if (!make_map(&mt.m[0], dO, rows, d, 64) || !make_map(&mt.m[1], h, rows, f, 64) ||
+      !make_map(&mt.m[2], dab, rows, 2LL * f, 64) || !make_map(&mt.m[3], x_perm, rows, d, 64))
+    return cudaErrorInvalidValue;
+  CUtensorMap* emaps = expert_maps(tiles_ws, N, E);
+  trace_begin(MOE_STAGE_BWD_WG2, s);
+  expert_maps_kernel<<<ceil_div(4 * E, 256), 256, 0, s>>>(mt, offsets, E, emaps);
+  count_launches(1);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   g.n_tiles_m = ceil_div(d, tile_m);
   g.n_tiles_n = ceil_div(f, BN);
   g.out_f32 = dW2;
+  g.emaps = emaps;
   CUtensorMap mc, mc2;
   if (!make_map_f32_3d(&mc, dW2, E, d, f)) return cudaErrorInvalidValue;
-  trace_begin(MOE_STAGE_BWD_WG2, s);
   const long long wg2_items = (long long)E * g.n_tiles_m * g.n_tiles_n;
-  e = cta_pairs ? launch_mode<WG2, true>(ma, mb, mb, mc, mc, mc, g, wg2_items, s)
-                : launch_mode<WG2>(ma, mb, mb, mc, mc, mc, g, wg2_items, s);
+  e = cta_pairs ? launch_mode<WG2, true>(mt.m[0], mt.m[1], mt.m[1], mc, mc, mc, g, wg2_items, s)
+                : launch_mode<WG2>(mt.m[0], mt.m[1], mt.m[1], mc, mc, mc, g, wg2_items, s);
   trace_end(MOE_STAGE_BWD_WG2, s);
   if (e != cudaSuccess) return e;
-  // [dW1[e]; dW3[e]] = [da | db]^T x_perm: A = dab [N, 2f], B = x_perm [N, d]
-  if (!make_map(&ma, dab, rows, 2LL * f, 64) || !make_map(&mb, x_perm, rows, d, 64))
-    return cudaErrorInvalidValue;
   g.n_tiles_m = ceil_div(2 * f, tile_m);
   g.n_tiles_n = ceil_div(d, BN);
   g.out_f32 = dW1; g.out_f32b = dW3;
+  g.emaps = emaps + 2 * E;
   if (!make_map_f32_3d(&mc, dW1, E, f, d) || !make_map_f32_3d(&mc2, dW3, E, f, d))
     return cudaErrorInvalidValue;
   trace_begin(MOE_STAGE_BWD_WG13, s);
   const long long wg13_items = (long long)E * g.n_tiles_m * g.n_tiles_n;
-  e = cta_pairs ? launch_mode<WG13, true>(ma, mb, mb, mc, mc2, mc2, g, wg13_items, s)
-                : launch_mode<WG13>(ma, mb, mb, mc, mc2, mc2, g, wg13_items, s);
+  e = cta_pairs ? launch_mode<WG13, true>(mt.m[2], mt.m[3], mt.m[3], mc, mc2, mc2, g, wg13_items, s)
+                : launch_mode<WG13>(mt.m[2], mt.m[3], mt.m[3], mc, mc2, mc2, g, wg13_items, s);
   trace_end(MOE_STAGE_BWD_WG13, s);
   return e;
 }

@@ -5,7 +5,18 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
+
 namespace moe {
+
+// Host-side checks and status handling shared by the C ABI's entry points.
+// The shapes every routed entry point accepts (T tokens, hidden size d, E experts, top-R).
+moe_status_t shape_check(int T, int d, int E, int R);
+// Records e as this thread's last CUDA error (moe_last_cuda_error); returns MOE_ERR_CUDA.
+moe_status_t cuda_failed(cudaError_t e);
+// The status of a call whose work was enqueued with result `launched`; with
+// MOE_CHECK in `flags`, waits for `s` and translates the device error word.
+moe_status_t finish(cudaError_t launched, const int* err_dev, unsigned flags, cudaStream_t s);
 
 // Adds n to the process-wide count of kernels launched by the library.
 void count_launches(int n);
@@ -32,6 +43,9 @@ struct GemmArgs {
   float* out_f32b;
   const float* bias;
   const float* row_scale;     // down epilogue: out[row] = bf16(row_scale[row] * acc), or null
+  // weight-gradient modes: per expert e, tensor maps of A (entry 2e) and B
+  // (2e+1) whose row extent ends at the expert's last row (CUtensorMap, 64-B aligned)
+  const void* emaps;
   int* err;
 };
 

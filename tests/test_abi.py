@@ -134,3 +134,41 @@ def test_selftest_argument_checks():
     assert lib.moe_selftest_wait_timeout(2000000, ctypes.c_void_p(4096), None) == 1
     assert lib.moe_selftest_wait_timeout(100, None, None) == 1
     assert lib.moe_selftest_wait_timeout(100, ctypes.c_void_p(4096 + 8), None) == 3
+
+
+def test_noalloc_dispatch_argument_checks_match_moe_dispatch():
+    """moe_dispatch_noalloc rejects the shapes and arguments moe_dispatch rejects,
+    with the same status, before it touches a device."""
+    lib = B.lib()
+    code = {name: value for value, name in B.STATUS.items()}
+    n = ctypes.c_size_t(0)
+    P = 1 << 20                       # a 16-byte-aligned stand-in pointer; never dereferenced
+
+    def noalloc(T, d, E, R, x=None, idx=P, counts=P, offsets=P, row_slot=P, slot_row=P,
+                x_perm=None):
+        return lib.moe_dispatch_noalloc(x, idx, T, d, E, R, counts, offsets, row_slot, slot_row,
+                                        x_perm, 0, None)
+
+    def query(T, d, E, R):
+        return lib.moe_dispatch(None, None, T, d, E, R, None, None, None, None, None, None,
+                                ctypes.byref(n), 0, None)
+
+    for shape, want in [((100, 64, 8, 9), "MOE_ERR_INVALID_ARG"),      # R > E
+                        ((-1, 64, 8, 2), "MOE_ERR_INVALID_ARG"),       # T < 0
+                        ((100, 0, 8, 2), "MOE_ERR_INVALID_ARG"),       # d <= 0
+                        ((100, 60, 8, 2), "MOE_ERR_UNSUPPORTED"),      # d % 8 != 0
+                        ((100, 64, 2000, 2), "MOE_ERR_UNSUPPORTED"),   # E > 1024
+                        ((100, 64, 64, 33), "MOE_ERR_UNSUPPORTED"),    # R > 32
+                        ((1 << 28, 4096, 8, 1), "MOE_ERR_UNSUPPORTED")]:  # T*d >= 2^40
+        assert noalloc(*shape) == code[want], shape
+        assert query(*shape) == code[want], shape
+    # the static 4 MiB scratch: 1024 experts x 1025 blocks of 256 tokens do not fit
+    assert noalloc(1025 * 256, 64, 1024, 8) == code["MOE_ERR_WORKSPACE"]
+    shape = (64, 64, 8, 2)
+    assert noalloc(*shape, counts=None) == code["MOE_ERR_INVALID_ARG"]
+    assert noalloc(*shape, offsets=None) == code["MOE_ERR_INVALID_ARG"]
+    assert noalloc(*shape, idx=None) == code["MOE_ERR_INVALID_ARG"]
+    assert noalloc(*shape, row_slot=None) == code["MOE_ERR_INVALID_ARG"]
+    assert noalloc(*shape, x=P, x_perm=None) == code["MOE_ERR_INVALID_ARG"]  # x without x_perm
+    assert noalloc(*shape, x=P + 8, x_perm=P) == code["MOE_ERR_UNSUPPORTED"]  # x not 16-B aligned
+    assert noalloc(*shape, x=P, x_perm=P + 4) == code["MOE_ERR_UNSUPPORTED"]

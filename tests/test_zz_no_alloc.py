@@ -73,11 +73,12 @@ def test_noalloc_dispatch_clears_its_error_word_and_rejects_oversize(lib):
     x = torch.zeros((T, d), dtype=torch.bfloat16, device="cuda")
     idx = torch.tensor(np.tile([0, 1], (T, 1)), dtype=torch.int32, device="cuda")
     idx[3, 1] = E                                            # out of range
-    assert _noalloc(lib, x, idx, E, _buffers(T, d, E, R), lib.MOE_CHECK) == 4
+    code = {name: value for value, name in lib.STATUS.items()}
+    assert _noalloc(lib, x, idx, E, _buffers(T, d, E, R), lib.MOE_CHECK) == code["MOE_ERR_BAD_ROUTING"]
     idx[3, 1] = 1                                            # the next call starts clean
     assert _noalloc(lib, x, idx, E, _buffers(T, d, E, R), lib.MOE_CHECK) == lib.MOE_OK
     # 1024 experts x 1025 token blocks of histograms exceed the 4 MiB array
     big_T = 1025 * 256
     st = lib.lib().moe_dispatch_noalloc(None, None, big_T, 64, 1024, 8, None, None, None, None,
                                         None, 0, None)
-    assert st == 3          # MOE_ERR_WORKSPACE, before anything is enqueued
+    assert st == code["MOE_ERR_WORKSPACE"]          # before anything is enqueued
