@@ -1,11 +1,14 @@
 """Benchmark of the MoE layer hot path on GB300 (one JSON line on rank 0).
 
-Default workload: the MoE layer training step (forward + backward) with
+Headline workload: the MoE layer training step (forward + backward) with
 T=16384 tokens, d=4096, E=128 experts, top-8 routing, SwiGLU width f=1536 --
 one pass of every step of the path (route, dispatch, grouped SwiGLU FFN,
 combine, and their backward).  Other workloads: --workload large | large_hot |
 mid | tiny (forward only) and dispatch (dispatch + combine with identity
-experts, --tokens T).
+experts, --tokens T).  With the default headline the same run also times, each
+on its own clock and with its own stages and roofline, the forward of large,
+large_hot and mid and dispatch + combine at T=8192 and T=65536 (L2 flushed
+between steps), under the "workloads" key.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
@@ -14,13 +17,22 @@ value = tokens per second of the whole job (all ranks); each rank runs an
 independent replica of the workload (the path has no cross-GPU exchange), so
 scaling is weak.  The timed region is K back-to-back steps between CUDA events
 on the launching stream, after W warm-up steps, bracketed by a barrier and a
-device synchronisation; the max over ranks is reported.  Each step streams
-more than L2 (5 GB of expert weights for the default workload), so no flush
-is needed between steps.
+device synchronisation; the max over ranks is reported.  Each layer step
+streams more than L2 (5 GB of expert weights for the headline), so no flush is
+needed between its steps.
+
+Roofline: every stage is timed by CUDA events the library records around it.
+A stage's roofline time is max(FLOPs / tensor peak, bytes / HBM bandwidth),
+with the FLOPs of real rows only and the bytes it must move to or from HBM at
+least once; its fraction is that time over the measured one.  The tensor peak
+is the measured burst bf16 rate when the SM clock stayed within 5% of its
+maximum during the timed region, else the sustained (power-capped) rate; both
+fractions are printed.
 """
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -36,9 +48,23 @@ METRIC = "MoE layer tokens/s on 1 GB300; grouped-GEMM % BF16 TC peak; dispatch/c
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+BURST_CLOCK_FRACTION = 0.95
+
+# the other workloads the default run times after the headline:
+# (name, overrides, flush L2 between steps)
+EXTRA_WORKLOADS = (("large", {}, False), ("large_hot", {}, False), ("mid", {}, False),
+                   ("dispatch", {"T": 8192}, True), ("dispatch", {"T": 65536}, True))
+
+# two token counts of the oracle sample per workload (full-step estimate: a
+# straight line through the two timings).  The smaller one already routes to
+# (nearly) every expert; the larger one adds enough rows that the per-token
+# cost stands well above the timing noise of the per-expert part.
+CPU_SAMPLE_TOKENS = {"train": (256, 2048), "mid": (512, 2048), "large": (512, 1024),
+                     "large_hot": (512, 1024), "tiny": (128, 256), "dispatch": (2048, 8192),
+                     "dispatch_zipf": (2048, 8192)}
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
@@ -49,8 +75,8 @@ def parse():
                             "dispatch_zipf"])
     p.add_argument("--tokens", type=int, default=None, help="override T")
     p.add_argument("--experts", type=int, default=None, help="override E (smaller profiling cases)")
-    p.add_argument("--cpu-tokens", type=int, default=None,
-                   help="tokens in the CPU oracle sample (default per workload)")
+    p.add_argument("--cpu-tokens", type=int, nargs=2, default=None, metavar=("N1", "N2"),
+                   help="token counts of the two CPU oracle samples (default per workload)")
     p.add_argument("--fp8", action="store_true",
                    help="block-scaled fp8 dispatch (E4M3 + per-128 scales), bf16 combine: "
                         "dispatch workloads dequantise in identity experts; layer workloads "
@@ -70,9 +96,12 @@ def parse():
     p.add_argument("--flush-l2", action="store_true",
                    help="write a 512 MB buffer (4x L2) between timed steps, outside the stage "
                         "events, so small workloads read HBM; ms_per_step then includes it")
+    p.add_argument("--extra-workloads", default="auto", choices=["auto", "on", "off"],
+                   help="also time large, large_hot, mid and dispatch + combine (auto: only "
+                        "with the default headline workload)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def load_peaks():
@@ -82,6 +111,17 @@ def load_peaks():
         return pk, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def tensor_peak(pk, clk):
+    """(peak TFLOP/s, regime): the burst bf16 peak when the median SM clock under
+    load stayed within 5% of its maximum, else the sustained (power-capped) one."""
+    sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sust = pk.get("bf16_tflops_sustained", burst)
+    if sm and smax and sm < BURST_CLOCK_FRACTION * smax:
+        return sust, "sustained"
+    return burst, "burst"
 
 
 # ---------------------------------------------------------------- clocks
@@ -116,96 +156,197 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sms, maxs, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as fh:
-            for line in fh:
-                f = [c.strip() for c in line.split(",")]
-                if len(f) < 9:
-                    continue
-                try:
-                    sms.append(float(f[1]))
-                    maxs.append(float(f[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, f[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
+            out = parse_clock_samples(fh)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sms) if sms else None,
-                "sm_max_mhz": max(maxs) if maxs else None, "reasons": sorted(reasons),
-                "samples": len(sms)}
+        return out
+
+
+def parse_clock_samples(lines):
+    """Median SM clock, max clock and the throttle reasons seen in nvidia-smi CSV rows."""
+    sms, maxs, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        f = [c.strip() for c in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sms.append(float(f[1]))
+            maxs.append(float(f[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sms) if sms else None,
+            "sm_max_mhz": max(maxs) if maxs else None, "reasons": sorted(reasons),
+            "samples": len(sms)}
 
 
 # ---------------------------------------------------------------- work model
-def stage_work(wl, fp8=False, shared_fs=0):
-    """Algorithmic work of one launch of each traced stage: (kind, amount).
+def stage_work(wl, fp8=False, shared_fs=0, active_experts=None):
+    """Algorithmic work of one launch of each traced stage.
 
-    kind "tflop": FLOPs of real rows only (no padding); "side": the same for the
-    shared expert's GEMMs (overlapping other stages); "gb": bytes that must
-    move to or from HBM at least once (reads of inputs + writes of outputs);
-    "tflop3": the gate projection x W_g on the tensor cores as three bf16
-    products (W_g split into hi + mid + lo), so the pipe executes 3x the
-    algorithmic FLOPs counted here; "alu": the FP32 FMA gate (d % 64 != 0).
+    Returns {stage: {"kind": K, "flops": F, "bytes": B}}.  F counts the
+    FLOPs of real rows only (no padding); B the bytes the stage must move to or
+    from HBM at least once (inputs read, outputs written).  Kinds: "tensor" (a
+    grouped GEMM on the tensor cores), "tensor3" (the gate projection x W_g on
+    the tensor cores as three bf16 products, W_g split into hi + mid + lo, so
+    the pipe executes 3 F), "alu" (the FP32 FMA gate, d % 64 != 0), "hbm"
+    (data movement only) and "side" (the shared expert's GEMMs, overlapping
+    other stages).  ``active_experts``: experts with at least one row, whose
+    weights the forward and data-gradient GEMMs read (default: all E).
     """
     T, d, E, R, f = wl.T, wl.d, wl.E, wl.R, wl.f
+    Ea = E if active_experts is None else active_experts
     N = T * R
     q8 = N * d + 4.0 * N * d / 128          # fp8 codes and their scales
     # fp8 in a layer: the codes and scales are written, read back and the bf16
     # rows the GEMMs read are written, all inside the dispatch stage
     disp = (2.0 * N * d if not fp8 else q8 if not f else 2.0 * q8 + 2.0 * N * d)
+
+    def k(kind, flops=0.0, nbytes=0.0):
+        return {"kind": kind, "flops": float(flops), "bytes": float(nbytes)}
+
     w = {
-        "gate": ("tflop3" if d % 64 == 0 else "alu", 2.0 * T * d * E),
-        "topk": ("gb", 4.0 * T * E + 8.0 * N),
-        "dispatch": ("gb", 2.0 * T * d + disp + 4.0 * N * 3),
-        "combine": ("gb", 2.0 * N * d + 8.0 * N + 2.0 * T * d),
+        "gate": k("tensor3" if d % 64 == 0 else "alu", 2.0 * T * d * E,
+                  2.0 * T * d + 4.0 * d * E + 4.0 * T * E),
+        "topk": k("hbm", 0, 4.0 * T * E + 8.0 * N),
+        "dispatch": k("hbm", 0, 2.0 * T * d + disp + 4.0 * N * 3),
+        "combine": k("hbm", 0, 2.0 * N * d + 8.0 * N + 2.0 * T * d),
     }
     if f:
+        save_ab = 4.0 * N * f if wl.train else 0.0    # the saved a and b (training)
         w.update({
-            "gateup": ("tflop", 4.0 * N * d * f),
-            "down": ("tflop", 2.0 * N * d * f),
-            "bwd_route": ("gb", 2.0 * T * d + 2.0 * N * d + 2.0 * N * d + 12.0 * N),
-            "bwd_dh": ("tflop", 2.0 * N * d * f),
-            "bwd_dx": ("tflop", 4.0 * N * d * f),
-            "bwd_wg2": ("tflop", 2.0 * N * d * f),
-            "bwd_wg13": ("tflop", 4.0 * N * d * f),
+            "gateup": k("tensor", 4.0 * N * d * f, 2.0 * N * d + 4.0 * Ea * f * d + 2.0 * N * f
+                        + save_ab),
+            "down": k("tensor", 2.0 * N * d * f, 2.0 * N * f + 2.0 * Ea * d * f + 2.0 * N * d),
+            "bwd_route": k("hbm", 0, 2.0 * T * d + 2.0 * N * d + 2.0 * N * d + 12.0 * N),
+            # dh = do W2: reads do, W2, the saved a and b; writes [da | db]
+            "bwd_dh": k("tensor", 2.0 * N * d * f, 2.0 * N * d + 2.0 * Ea * d * f + 4.0 * N * f
+                        + 4.0 * N * f),
+            "bwd_dx": k("tensor", 4.0 * N * d * f, 4.0 * N * f + 4.0 * Ea * f * d + 2.0 * N * d),
+            # weight gradients: every expert's fp32 gradient is written
+            "bwd_wg2": k("tensor", 2.0 * N * d * f, 2.0 * N * d + 2.0 * N * f + 4.0 * E * d * f),
+            "bwd_wg13": k("tensor", 4.0 * N * d * f, 4.0 * N * f + 2.0 * N * d + 8.0 * E * f * d),
             # x once (its rows are gathered through row_slot, the R reads of a
             # row mostly from L2), row_slot and dsel per row, dW_g written
-            "bwd_dwg": ("gb", 2.0 * T * d + 8.0 * N + 4.0 * d * E),
-            "bwd_dxc": ("gb", 2.0 * N * d + 2.0 * T * d + 8.0 * E * d),
+            "bwd_dwg": k("hbm", 0, 2.0 * T * d + 8.0 * N + 4.0 * d * E),
+            "bwd_dxc": k("hbm", 0, 2.0 * N * d + 2.0 * T * d + 8.0 * E * d),
         })
     if f and shared_fs:
         # the shared expert on the side stream: reported, but its time overlaps
         # other stages, so it stays out of the GEMM summary and the dominant kernel
-        w.update({"shared_fwd": ("side", 6.0 * T * d * shared_fs),
-                  "shared_bwd": ("side", 12.0 * T * d * shared_fs)})
+        w.update({"shared_fwd": k("side", 6.0 * T * d * shared_fs),
+                  "shared_bwd": k("side", 12.0 * T * d * shared_fs)})
     return w
 
 
-def kernel_sources_digest():
-    """sha256 over the CUDA sources; ncu traffic is void once they change."""
+def stage_roofline(work, ms, tc_peak, pk, sm_mhz=None):
+    """One stage's figures: achieved rates, its roofline bound and fractions.
+
+    tc_peak: the tensor peak the fractions divide by (TFLOP/s); the burst and
+    sustained fractions are printed beside it for tensor stages.
+    """
+    kind, fl, nb = work["kind"], work["flops"], work["bytes"]
+    s = ms / 1e3
+    out = {"ms": round(ms, 4)}
+    hbm = pk["hbm_gbs"] * 1e9
+    if kind in ("tensor", "tensor3", "side"):
+        ex = 3.0 * fl if kind == "tensor3" else fl     # FLOPs the tensor pipe executes
+        out["tflops"] = round(fl / s / 1e12, 1)
+        if kind == "tensor3":
+            out["tensor_tflops"] = round(ex / s / 1e12, 1)
+        out["frac_burst"] = round(ex / s / 1e12 / pk.get("bf16_tflops", tc_peak), 4)
+        out["frac_sustained"] = round(
+            ex / s / 1e12 / pk.get("bf16_tflops_sustained", tc_peak), 4)
+        if kind == "side":
+            out["frac"] = round(ex / s / 1e12 / tc_peak, 4)
+            return out
+        t_tc = ex / (tc_peak * 1e12)
+        t_mem = nb / hbm
+        if nb:
+            out["gbs"] = round(nb / s / 1e9, 1)
+        out["bound"] = "tensor" if t_tc >= t_mem else "hbm"
+        out["roofline_ms"] = round(max(t_tc, t_mem) * 1e3, 4)
+        out["frac"] = round(max(t_tc, t_mem) / s, 4)
+    elif kind == "hbm":
+        out["gbs"] = round(nb / s / 1e9, 1)
+        out["bound"] = "hbm"
+        out["roofline_ms"] = round(nb / hbm * 1e3, 4)
+        out["frac"] = round(nb / hbm / s, 4)
+    else:   # FP32 FMA gate
+        peak = alu_peak_tflops(sm_mhz)
+        out["tflops"] = round(fl / s / 1e12, 2)
+        out["bound"] = "alu"
+        out["roofline_ms"] = round(fl / (peak * 1e12) * 1e3, 4)
+        out["frac"] = round(fl / (peak * 1e12) / s, 4)
+    return out
+
+
+def dominant_roofline(stages, work, dom, tc_peak, regime, pk, pk_src, traffic, sm_mhz=None):
+    """The roofline object of the bench line for the dominant stage ``dom``."""
+    st, w = stages[dom], work[dom]
+    r = {"kernel": dom, "traffic": traffic,
+         "algorithmic_bytes": w["bytes"] or None}
+    if st["bound"] == "tensor":
+        r.update(bound="tensor", unit="TFLOP/s",
+                 achieved=st.get("tensor_tflops", st["tflops"]), peak=tc_peak,
+                 frac=st["frac"], frac_burst=st["frac_burst"],
+                 frac_sustained=st["frac_sustained"],
+                 peak_source=f"{pk_src} bf16 {regime} (median SM clock "
+                             f"{'within' if regime == 'burst' else 'below'} 5% of max)")
+    elif st["bound"] == "hbm":
+        r.update(bound="hbm", unit="GB/s", achieved=st["gbs"], peak=pk["hbm_gbs"],
+                 frac=st["frac"], peak_source=f"{pk_src} HBM copy")
+        if "frac_burst" in st:   # a GEMM bound by its operand bytes
+            r.update(tensor_frac_burst=st["frac_burst"],
+                     tensor_frac_sustained=st["frac_sustained"])
+    else:
+        r.update(bound="alu", unit="TFLOP/s", achieved=st["tflops"],
+                 peak=round(alu_peak_tflops(sm_mhz), 1), frac=st["frac"],
+                 peak_source="FP32 FMA: 152 SMs x 128 lanes x 2 x median SM clock")
+    return r
+
+
+def kernel_sources_digest(files=None):
+    """sha256 over CUDA sources (all of them, or the named files of csrc/); an ncu
+    traffic figure is void once the sources of its kernel change."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "expert_moe_route_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files if files is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()
 
 
+def traffic_key(wl):
+    """The traffic table's key of a workload: its name, plus T when not the default one."""
+    from workloads import synth
+    default_T = synth.WORKLOADS[wl.name].T
+    return wl.name if wl.T == default_T else f"{wl.name}@T={wl.T}"
+
+
 def profiled_traffic(workload, stage):
-    """DRAM bytes per launch of a stage's kernel from the committed ncu summary, or None
-    when there is none for this workload or the kernels changed since it was taken."""
+    """DRAM bytes per launch of a stage's kernels from the committed ncu summary, or
+    None when there is none for this workload or the stage's kernel sources changed
+    since it was taken."""
     try:
         with open(PROFILE_TRAFFIC) as fh:
             table = json.load(fh)
     except (OSError, ValueError):
         return None
-    if table.get("kernel_sources_sha256") != kernel_sources_digest():
-        return None
     entry = table.get("workloads", {}).get(workload, {}).get(stage)
-    return entry.get("bytes_per_launch") if entry else None
+    if not entry:
+        return None
+    try:
+        if entry.get("sources_sha256") != kernel_sources_digest(entry.get("sources", [])):
+            return None
+    except OSError:
+        return None
+    return entry.get("bytes_per_launch")
 
 
 def alu_peak_tflops(sm_mhz):
@@ -214,13 +355,29 @@ def alu_peak_tflops(sm_mhz):
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, rank, world, device):
+class Opts:
+    """What one measured workload runs with."""
+
+    def __init__(self, args, name=None, over=None, flush_l2=None, e2e=None):
+        self.name = name or args.workload
+        self.over = overrides(args) if over is None else over
+        self.flush_l2 = args.flush_l2 if flush_l2 is None else flush_l2
+        self.e2e = (not args.no_e2e) if e2e is None else e2e
+        self.steps, self.warmup = args.steps, args.warmup
+        self.fp8 = args.fp8
+        self.single_cta = args.single_cta
+        self.no_prepack = args.no_prepack
+        self.shared_expert = args.shared_expert
+        self.shared_serial = args.shared_serial
+
+
+def run_ours(o, rank, world, device):
     import torch
 
     from expert_moe_route_gb300 import binding as B
-    from expert_moe_route_gb300 import synth
+    from workloads import synth
 
-    wl = synth.workload(args.workload, **overrides(args))
+    wl = synth.workload(o.name, **o.over)
     identity = wl.f == 0
     stream = torch.cuda.current_stream()
 
@@ -236,12 +393,12 @@ def run_ours(args, rank, world, device):
         x_perm = torch.empty((N, wl.d), dtype=torch.bfloat16, device=device)
         y = torch.empty_like(x)
         ws = B.workspace(B.dispatch_ws_bytes(wl.T, wl.d, wl.E, wl.R), device)
-        if args.fp8:
+        if o.fp8:
             xq = torch.empty((N, wl.d), dtype=torch.uint8, device=device)
             xs = torch.empty((N, wl.d // 128), dtype=torch.float32, device=device)
 
         def step(xin=None, yout=None):
-            if args.fp8:   # fp8 dispatch, identity experts dequantise to bf16, bf16 combine
+            if o.fp8:   # fp8 dispatch, identity experts dequantise to bf16, bf16 combine
                 B.moe_dispatch_fp8(x if xin is None else xin, idx, wl.E, counts, offsets,
                                    row_slot, slot_row, xq, xs, ws)
                 B.moe_dequant_fp8(xq, xs, x_perm)
@@ -256,21 +413,22 @@ def run_ours(args, rank, world, device):
         big = wl.E * wl.f * wl.d > (1 << 28)
         inp = synth.layer_inputs(wl, device=device, weight_device=device if big else "cpu")
         train = wl.train
-        gemm_flags = B.MOE_SINGLE_CTA_TILES if args.single_cta else 0
-        fwd_flags = gemm_flags | (B.MOE_FP8_DISPATCH if args.fp8 else 0)
+        gemm_flags = B.MOE_SINGLE_CTA_TILES if o.single_cta else 0
+        fwd_flags = gemm_flags | (B.MOE_FP8_DISPATCH if o.fp8 else 0)
         weights_note = "plain [E, out, in]"
-        if (not train and not args.no_prepack and wl.d % 256 == 0 and wl.f % 128 == 0):
+        if (not train and not o.no_prepack and wl.d % 256 == 0 and wl.f % 128 == 0):
             # inference: the weights are laid out once (like loading a model), outside the timing
             packed = [torch.empty_like(inp[k]) for k in ("W1", "W3", "W2")]
             B.moe_prepack_weights(inp["W1"], inp["W3"], inp["W2"], *packed)
             torch.cuda.synchronize()
             for k, t in zip(("W1", "W3", "W2"), packed):
                 inp[k] = t
+            del packed
             fwd_flags |= B.MOE_WEIGHTS_PREPACKED
             weights_note = "prepacked tiles (moe_prepack_weights once, before timing)"
         shared = None
-        if args.shared_expert:
-            fs = args.shared_expert
+        if o.shared_expert:
+            fs = o.shared_expert
             sw = {k: v.to(device) for k, v in synth.shared_expert_inputs(wl, fs).items()}
             sg = {}
             if train:
@@ -278,7 +436,7 @@ def run_ours(args, rank, world, device):
                           dW3=torch.empty((fs, wl.d), dtype=torch.float32, device=device),
                           dW2=torch.empty((wl.d, fs), dtype=torch.float32, device=device))
             shared = B.Shared(sw["W1"], sw["W3"], sw["W2"], **sg)
-            if args.shared_serial:
+            if o.shared_serial:
                 gemm_flags |= B.MOE_SHARED_SERIAL
                 fwd_flags |= B.MOE_SHARED_SERIAL
         layer = B.Layer(inp["w_gate"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], wl.R, wl.T,
@@ -311,18 +469,20 @@ def run_ours(args, rank, world, device):
     # ---- one checked step (device error word) before timing
     if identity:
         step()
+        active = wl.E
     else:
         B.moe_layer_fwd(layer, x, y, saved, fws, flags=B.MOE_CHECK | fwd_flags)
         if train:
             B.moe_layer_bwd(layer, x, saved, g, dx, dWg, dW1, dW3, dW2, bws,
                             flags=B.MOE_CHECK | gemm_flags)
+        active = int((saved.counts > 0).sum().item())   # experts whose weights are read
     torch.cuda.synchronize()
-    for _ in range(args.warmup):
+    for _ in range(o.warmup):
         step()
     torch.cuda.synchronize()
 
     # ---- timed region
-    traces = [B.StageTrace() for _ in range(args.steps)]
+    traces = [B.StageTrace() for _ in range(o.steps)]
     world_barrier(world)
     torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
@@ -331,10 +491,10 @@ def run_ours(args, rank, world, device):
     launches0 = B.kernel_launches()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    flush = (torch.empty(512 << 20, dtype=torch.uint8, device=device) if args.flush_l2
+    flush = (torch.empty(512 << 20, dtype=torch.uint8, device=device) if o.flush_l2
              else None)
-    for k in range(args.steps):
+    t0.record(stream)
+    for k in range(o.steps):
         if flush is not None:
             flush.fill_(k & 0xff)
         traces[k].arm()
@@ -347,17 +507,18 @@ def run_ours(args, rank, world, device):
     world_barrier(world)
     ms_total = t0.elapsed_time(t1)
     ms_total = world_max(ms_total, world, device)
-    ms_step = ms_total / args.steps
+    ms_step = ms_total / o.steps
     tokens_per_step = wl.T
-    value = job_tokens_per_s(tokens_per_step, world, args.steps, ms_total)
+    value = job_tokens_per_s(tokens_per_step, world, o.steps, ms_total)
 
     # ---- per-stage device time, averaged over the timed steps
     stage_ms = {}
     for tr in traces:
         for name, ms in tr.elapsed_ms().items():
-            stage_ms[name] = stage_ms.get(name, 0.0) + ms / args.steps
+            stage_ms[name] = stage_ms.get(name, 0.0) + ms / o.steps
     pk, pk_src = load_peaks()
-    work = stage_work(wl, fp8=args.fp8, shared_fs=args.shared_expert)
+    tc_peak, regime = tensor_peak(pk, clk)
+    work = stage_work(wl, fp8=o.fp8, shared_fs=o.shared_expert, active_experts=active)
     if identity:
         ran = ("dispatch", "combine")
     elif train:
@@ -368,55 +529,38 @@ def run_ours(args, rank, world, device):
     for name, ms in stage_ms.items():
         if name not in ran or name not in work or ms <= 0:
             continue
-        kind, amount = work[name]
-        if kind == "tflop":
-            ach = amount / (ms / 1e3) / 1e12
-            stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 1),
-                            "frac": round(ach / pk["bf16_tflops_sustained"], 4)}
-        elif kind == "gb":
-            ach = amount / (ms / 1e3) / 1e9
-            stages[name] = {"ms": round(ms, 4), "gbs": round(ach, 1),
-                            "frac": round(ach / pk["hbm_gbs"], 4)}
-        elif kind == "side":
-            ach = amount / (ms / 1e3) / 1e12
-            stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 1),
-                            "frac": round(ach / pk["bf16_tflops_sustained"], 4),
-                            "overlaps_other_stages": not args.shared_serial}
-        elif kind == "tflop3":
-            ach = amount / (ms / 1e3) / 1e12
-            stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 1),
-                            "tensor_tflops": round(3 * ach, 1),
-                            "frac": round(3 * ach / pk["bf16_tflops_sustained"], 4)}
-        else:
-            ach = amount / (ms / 1e3) / 1e12
-            stages[name] = {"ms": round(ms, 4), "tflops": round(ach, 2),
-                            "frac": round(ach / alu_peak_tflops(clk.get("sm_mhz")), 4)}
-    dom = max((n for n in stages if work[n][0] != "side"), key=lambda n: stages[n]["ms"])
-    kind, amount = work[dom]
-    traffic = profiled_traffic(wl.name, dom)
-    if kind in ("tflop", "tflop3"):
-        roof = {"bound": "tensor", "kernel": dom,
-                "achieved": stages[dom].get("tensor_tflops", stages[dom]["tflops"]),
-                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": stages[dom]["frac"], "traffic": traffic,
-                "peak_source": f"{pk_src} bf16 sustained (kernel timed inside a long step)"}
-    elif kind == "gb":
-        roof = {"bound": "hbm", "kernel": dom, "achieved": stages[dom]["gbs"],
-                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": stages[dom]["frac"],
-                "traffic": traffic, "peak_source": f"{pk_src} HBM copy"}
-    else:
-        roof = {"bound": "alu", "kernel": dom, "achieved": stages[dom]["tflops"],
-                "peak": round(alu_peak_tflops(clk.get("sm_mhz")), 1), "unit": "TFLOP/s",
-                "frac": stages[dom]["frac"], "traffic": traffic,
-                "peak_source": "FP32 FMA: 152 SMs x 128 lanes x 2 x median SM clock"}
-    gemm = [n for n in stages if work[n][0] == "tflop"]
+        stages[name] = stage_roofline(work[name], ms, tc_peak, pk, clk.get("sm_mhz"))
+    dom = max((n for n in stages if work[n]["kind"] != "side"), key=lambda n: stages[n]["ms"])
+    roof = dominant_roofline(stages, work, dom, tc_peak, regime, pk, pk_src,
+                             profiled_traffic(traffic_key(wl), dom), clk.get("sm_mhz"))
+    # the whole step: its FLOPs against the tensor peak, and the sum of the
+    # stages' roofline times against the measured step
+    step_fl = sum(3.0 * w["flops"] if w["kind"] == "tensor3" else w["flops"]
+                  for n, w in work.items() if n in ran and w["kind"] != "side")
+    step_roof_ms = sum(stages[n]["roofline_ms"] for n in stages if "roofline_ms" in stages[n])
+    summary = {"tensor_peak_regime": regime, "tensor_peak_tflops": tc_peak,
+               "active_experts": active}
+    if step_fl:
+        step_tf = step_fl / (ms_step / 1e3) / 1e12
+        summary["step_tflops"] = round(step_tf, 1)
+        roof["frac_step"] = round(step_tf / tc_peak, 4)
+    summary["step_roofline_ms"] = round(step_roof_ms, 4)
+    summary["step_frac_of_roofline"] = round(step_roof_ms / ms_step, 4)
+    roof["step_frac_of_roofline"] = summary["step_frac_of_roofline"]
+    gemm = [n for n in stages if work[n]["kind"] == "tensor"]
     gemm_ms = sum(stages[n]["ms"] for n in gemm)
-    gemm_fl = sum(work[n][1] for n in gemm)
-    summary = {}
     if gemm_ms > 0:
-        tf = gemm_fl / (gemm_ms / 1e3) / 1e12
+        fl = sum(work[n]["flops"] for n in gemm)
+        tf = fl / (gemm_ms / 1e3) / 1e12
         summary["grouped_gemm_tflops"] = round(tf, 1)
-        summary["grouped_gemm_frac_of_bf16_peak"] = round(tf / pk["bf16_tflops_sustained"], 4)
+        summary["grouped_gemm_frac_burst"] = round(tf / pk.get("bf16_tflops", tc_peak), 4)
+        summary["grouped_gemm_frac_sustained"] = round(
+            tf / pk.get("bf16_tflops_sustained", tc_peak), 4)
+        summary["grouped_gemm_frac_of_roofline"] = round(
+            sum(stages[n]["roofline_ms"] for n in gemm) / gemm_ms, 4)
+        summary["grouped_gemm_bound"] = (
+            "hbm" if sum(work[n]["bytes"] for n in gemm) / (pk["hbm_gbs"] * 1e9)
+            > fl / (tc_peak * 1e12) else "tensor")
     for n in ("dispatch", "combine"):
         if n in stages:
             summary[f"{n}_gbs"] = stages[n]["gbs"]
@@ -429,7 +573,7 @@ def run_ours(args, rank, world, device):
     # copies, so step k+1's inputs upload and step k's results download while
     # the layer computes.
     e2e = None
-    if not args.no_e2e:
+    if o.e2e:
         pin_in = {n: t.detach().cpu().pin_memory() for n, t in host_in}
         pin_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in host_out}
         dev_in = [{n: torch.empty_like(t) for n, t in host_in} for _ in range(2)]
@@ -487,49 +631,32 @@ def run_ours(args, rank, world, device):
             torch.cuda.synchronize()
             return t0.elapsed_time(t1)
 
-        run_e2e(max(1, args.warmup))
+        run_e2e(max(1, o.warmup))
         world_barrier(world)
-        ems = world_max(run_e2e(args.steps), world, device)
-        e2e = {"value": round(job_tokens_per_s(tokens_per_step, world, args.steps, ems), 1),
+        ems = world_max(run_e2e(o.steps), world, device)
+        e2e = {"value": round(job_tokens_per_s(tokens_per_step, world, o.steps, ems), 1),
                "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "ms_per_step": round(ems / args.steps, 4),
+               "ms_per_step": round(ems / o.steps, 4),
                "copies": "pinned host <-> device on two copy streams, double-buffered, "
                          "overlapping the layer's compute"}
 
-    result = {
-        "metric": METRIC,
-        "value": round(value, 1),
-        "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16 (fp32 accumulation)",
-        "data": "synthetic (seeded, shapes and distributions of the workload)",
-        "config": {"workload": synth.describe(wl) + (" fwd+bwd" if train else " fwd")
-                   + (" fp8-dispatch" if args.fp8 else ""),
-                   "parallelism": f"replicas x{world} (no cross-GPU exchange)",
-                   "global_batch_tokens": wl.T * world,
-                   "l2": ("512 MB written between steps (flushes L2; outside the stage events, "
-                          "inside ms_per_step)" if args.flush_l2 else
-                          "inputs larger than L2 every step (no flush)"),
-                   "weights": weights_note,
-                   "gemm_tiles": None if identity else
-                   ("128-row, one CTA" if args.single_cta else "256-row, CTA pairs"),
-                   "shared_expert": (None if not args.shared_expert else
-                                     {"fs": args.shared_expert,
-                                      "stream": "caller's, after the routed path"
-                                      if args.shared_serial else "side stream, overlapped"})},
-        "roofline": roof,
-        "summary": summary,
-        "stages": stages,
-        "clocks": clk,
-        "gpu_launches": launches,
-        "e2e": e2e,
-    }
+    config = {"workload": synth.describe(wl) + (" fwd+bwd" if train else " fwd")
+              + (" fp8-dispatch" if o.fp8 else ""),
+              "parallelism": f"replicas x{world} (no cross-GPU exchange)",
+              "global_batch_tokens": wl.T * world,
+              "l2": ("512 MB written between steps (flushes L2; outside the stage events, "
+                     "inside ms_per_step)" if o.flush_l2 else
+                     "inputs larger than L2 every step (no flush)"),
+              "weights": weights_note,
+              "gemm_tiles": None if identity else
+              ("128-row, one CTA" if o.single_cta else "256-row, CTA pairs"),
+              "shared_expert": (None if not o.shared_expert else
+                                {"fs": o.shared_expert,
+                                 "stream": "caller's, after the routed path"
+                                 if o.shared_serial else "side stream, overlapped"})}
+    result = {"value": round(value, 1), "ms_per_step": round(ms_step, 4), "config": config,
+              "roofline": roof, "summary": summary, "stages": stages, "clocks": clk,
+              "gpu_launches": launches, "e2e": e2e}
     return result, wl
 
 
@@ -543,20 +670,42 @@ class LazyExperts:
         return self.bits(self.t[e])
 
 
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(wl, device):
+    """The workload's seeded inputs for the oracle samples, drawn once per process."""
+    import torch
+
+    from workloads import synth
+    key = (repr(wl), device)
+    if key not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS.clear()
+        if wl.f == 0:
+            _ORACLE_INPUTS[key] = synth.drawn_routing(wl)
+        else:
+            big = wl.E * wl.f * wl.d > (1 << 28)
+            use_dev = device if (big and torch.cuda.is_available()) else "cpu"
+            _ORACLE_INPUTS[key] = synth.layer_inputs(wl, device=use_dev)
+    return _ORACLE_INPUTS[key]
+
+
 def cpu_oracle_sample(wl, device, n_tokens, steps=1, shared_fs=0):
-    """Times the CPU oracle (fwd, and bwd for training) on the first n_tokens tokens."""
+    """Times the CPU oracle (fwd, and bwd for training) on the first n_tokens tokens.
+
+    Returns (tokens/s of the sample, seconds, tokens, experts the sample routes to)."""
     import numpy as np
     import torch
 
-    from expert_moe_route_gb300 import synth
     from oracle import moe_oracle as O
+    from workloads import synth
 
     def bits(t):
         return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
     n = min(n_tokens, wl.T)
     if wl.f == 0:
-        r = synth.drawn_routing(wl)
+        r = _oracle_inputs(wl, device)
         x = bits(r["x"])[:n]
         idx = r["topk_idx"].numpy()[:n]
         w = r["topk_w"].numpy()[:n]
@@ -566,10 +715,9 @@ def cpu_oracle_sample(wl, device, n_tokens, steps=1, shared_fs=0):
             xp = O.permute_rows(x, row_slot, wl.R)
             O.combine(O.bf16_to_f64(xp), slot_row, w, n, wl.R)
         dt = time.perf_counter() - t0
+        touched = len(np.unique(idx))
     else:
-        big = wl.E * wl.f * wl.d > (1 << 28)
-        use_dev = device if (big and torch.cuda.is_available()) else "cpu"
-        inp = synth.layer_inputs(wl, device=use_dev)
+        inp = _oracle_inputs(wl, device)
         x = bits(inp["x"])[:n]
         # expert weights stay where they were drawn; the oracle reads one expert at a time
         W1, W3, W2 = (LazyExperts(inp[k], bits) for k in ("W1", "W3", "W2"))
@@ -586,7 +734,57 @@ def cpu_oracle_sample(wl, device, n_tokens, steps=1, shared_fs=0):
             if wl.train:
                 O.layer_bwd(fw, x, wg, W1, W3, W2, g, wl.R, shared=shared)
         dt = time.perf_counter() - t0
-    return n * steps / dt, dt, n
+        touched = int((fw["counts"] > 0).sum())
+        del fw, W1, W3, W2
+        gc.collect()
+    return n * steps / dt, dt, n, touched
+
+
+def full_step_estimate(wl, samples):
+    """The oracle's time for the whole workload from timed samples.
+
+    samples: [(tokens, seconds, experts routed to)] at two or more token counts.
+    The oracle's cost has a part that grows with the tokens (routing, dispatch,
+    the FFN rows, combine) and a part per expert the sample routes to (decoding
+    that expert's weights, and in training writing its dense weight gradients);
+    the samples are sized so that they route to (nearly) every expert, so a
+    straight line through (tokens, mean seconds) separates the two: the slope is
+    the per-token cost, the intercept the per-expert part.  Returns a dict with
+    the line and the extrapolated time for wl.T tokens.
+    """
+    by_n = {}
+    for n, s, touched in samples:
+        by_n.setdefault(n, []).append((s, touched))
+    ns = sorted(by_n)
+    if len(ns) < 2:
+        n = ns[0]
+        sec = statistics.mean(s for s, _ in by_n[n])
+        return {"per_token_s": sec / n, "fixed_s": 0.0, "full_step_s": sec / n * wl.T,
+                "tokens": ns, "experts_routed": [min(t for _, t in by_n[n])],
+                "method": "one sample size: proportional"}
+    xs = [float(n) for n in ns]
+    ys = [statistics.mean(s for s, _ in by_n[n]) for n in ns]
+    mx, my = statistics.mean(xs), statistics.mean(ys)
+    slope = sum((a - mx) * (b - my) for a, b in zip(xs, ys)) / sum((a - mx) ** 2 for a in xs)
+    slope = max(slope, 1e-12)
+    fixed = max(0.0, my - slope * mx)
+    return {"per_token_s": slope, "fixed_s": fixed, "full_step_s": fixed + slope * wl.T,
+            "tokens": ns, "experts_routed": [min(t for _, t in by_n[n]) for n in ns],
+            "mean_s": [round(y, 3) for y in ys],
+            "method": "straight line through (tokens, seconds), extrapolated to T"}
+
+
+def cpu_baseline_line(wl, est, cores, runs):
+    """The cpu_baseline object: the oracle's extrapolated full-step throughput."""
+    value = wl.T / est["full_step_s"]
+    return {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "full_step_s": round(est["full_step_s"], 1),
+            "sample": (f"the oracle ({'fwd+bwd' if wl.train else 'fwd'}, full d, E, R, f and "
+                       f"weights) timed on the first {est['tokens']} tokens of the workload "
+                       f"({runs}; they route to {est['experts_routed']} of {wl.E} experts); "
+                       f"per-token cost {est['per_token_s'] * 1e3:.2f} ms and fixed per-expert "
+                       f"cost {est['fixed_s']:.2f} s from a straight line through the timings, "
+                       f"extrapolated to all {wl.T} tokens: {est['full_step_s']:.1f} s per step")}
 
 
 def overrides(args):
@@ -621,10 +819,58 @@ def job_tokens_per_s(tokens_per_step, world, steps, ms_total):
     return tokens_per_step * world * steps / (ms_total / 1e3)
 
 
-def default_cpu_tokens(wl):
-    if wl.f == 0:
-        return 4096
-    return {"train": 192, "large": 16, "large_hot": 16, "mid": 512, "tiny": 256}.get(wl.name, 128)
+def cpu_sample_tokens(wl, args):
+    if args.cpu_tokens:
+        return tuple(args.cpu_tokens)
+    return CPU_SAMPLE_TOKENS.get(wl.name, (64, 128))
+
+
+def want_extras(args):
+    if args.extra_workloads == "on":
+        return True
+    if args.extra_workloads == "off":
+        return False
+    return (args.workload == "train" and not overrides(args) and not args.fp8
+            and not args.single_cta and not args.shared_expert and not args.flush_l2)
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    from workloads import synth
+    wl = synth.workload(args.workload, **overrides(args))
+    n1, n2 = cpu_sample_tokens(wl, args)
+    device = "cuda:0"
+    try:
+        import torch
+        if not torch.cuda.is_available():
+            device = "cpu"
+    except ImportError:
+        device = "cpu"
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, device, n1, shared_fs=args.shared_expert)
+    samples, t_all = [], 0.0
+    for k in range(args.steps):        # steps alternate between the two sample sizes
+        n = n1 if k % 2 == 0 else n2
+        _, dt, n, touched = cpu_oracle_sample(wl, device, n, shared_fs=args.shared_expert)
+        samples.append((n, dt, touched))
+        t_all += dt
+    est = full_step_estimate(wl, samples)
+    cb = cpu_baseline_line(wl, est, os.cpu_count(),
+                           f"{args.steps} timed samples alternating between the two sizes")
+    value = cb["value"]
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t_all / args.steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (bf16 storage points)",
+            "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": synth.describe(wl) + (" fwd+bwd" if wl.train else " fwd"),
+                       "parallelism": "host cores"},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "note": "value is the oracle's full-workload throughput extrapolated from the "
+                    "timed samples; ms_per_step is the mean time of one sample"}
+    print(json.dumps(line))
 
 
 def main():
@@ -635,41 +881,8 @@ def main():
     os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
 
     if args.impl == "reference":
-        if rank != 0:
-            return
-        from expert_moe_route_gb300 import synth
-        wl = synth.workload(args.workload, **overrides(args))
-        n = args.cpu_tokens or (8 if wl.f else 1024)
-        device = "cuda:0"
-        try:
-            import torch
-            if not torch.cuda.is_available():
-                device = "cpu"
-        except ImportError:
-            device = "cpu"
-        for _ in range(args.warmup):
-            cpu_oracle_sample(wl, device, n, shared_fs=args.shared_expert)
-        rates = []
-        t_all = 0.0
-        for _ in range(args.steps):
-            rate, dt, _ = cpu_oracle_sample(wl, device, n, shared_fs=args.shared_expert)
-            rates.append(rate)
-            t_all += dt
-        value = n * args.steps / t_all
-        line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": round(1e3 * t_all / args.steps, 2), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64 (bf16 storage points)",
-                "data": "synthetic (seeded)", "impl": "reference",
-                "config": {"workload": synth.describe(wl) + (" fwd+bwd" if wl.train else " fwd"),
-                           "parallelism": "host cores"},
-                "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
-                                 "cores": os.cpu_count(), "kind": "oracle",
-                                 "sample": f"each step: the oracle on the first {n} of {wl.T} tokens "
-                                           f"of the workload (full d, E, R, f and weights)"},
-                "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        if rank == 0:
+            run_reference(args)
         return
 
     import torch
@@ -680,14 +893,39 @@ def main():
     else:
         torch.cuda.set_device(0)
     device = f"cuda:{torch.cuda.current_device()}"
-    result, wl = run_ours(args, rank, world, device)
+    res, wl = run_ours(Opts(args), rank, world, device)
+    result = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
+              "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+              "dtype": "bf16 (fp32 accumulation)",
+              "data": "synthetic (seeded, shapes and distributions of the workload)"}
+    result.update({k: res[k] for k in ("config", "roofline", "summary", "stages", "clocks",
+                                       "gpu_launches", "e2e")})
+    del res
+    gc.collect()
+    torch.cuda.empty_cache()
+    if want_extras(args):
+        extras = []
+        for name, over, flush in EXTRA_WORKLOADS:
+            r, _ = run_ours(Opts(args, name, over, flush, e2e=False), rank, world, device)
+            extras.append({"workload": r["config"]["workload"], "value": r["value"],
+                           "unit": "tokens/s", "ms_per_step": r["ms_per_step"],
+                           "l2": r["config"]["l2"], "weights": r["config"]["weights"],
+                           "roofline": r["roofline"], "summary": r["summary"],
+                           "stages": r["stages"], "clocks": r["clocks"],
+                           "gpu_launches": r["gpu_launches"]})
+            del r
+            gc.collect()
+            torch.cuda.empty_cache()
+        result["workloads"] = extras
     if rank == 0 and not args.no_cpu_baseline:
-        n = args.cpu_tokens or default_cpu_tokens(wl)
-        rate, dt, n = cpu_oracle_sample(wl, device, n, shared_fs=args.shared_expert)
-        result["cpu_baseline"] = {
-            "value": round(rate, 2), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"the oracle ({'fwd+bwd' if wl.train else 'fwd'}) on the first {n} of "
-                      f"{wl.T} tokens (full d, E, R, f and weights), {dt:.1f} s"}
+        n1, n2 = cpu_sample_tokens(wl, args)
+        samples = []
+        for n in (n1, n2):
+            _, dt, n, touched = cpu_oracle_sample(wl, device, n, shared_fs=args.shared_expert)
+            samples.append((n, dt, touched))
+        result["cpu_baseline"] = cpu_baseline_line(wl, full_step_estimate(wl, samples),
+                                                   os.cpu_count(), "one timed sample of each")
     if rank == 0:
         print(json.dumps(result))
     if world > 1:

@@ -15,7 +15,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 sys.path.insert(0, ROOT)
 
-from expert_moe_route_gb300 import synth  # noqa: E402
+from workloads import synth  # noqa: E402
 from oracle import moe_oracle as O  # noqa: E402
 
 TARGET_SHARE = 0.25

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from expert_moe_route_gb300 import synth
+from workloads import synth
 from oracle import moe_oracle as O
 from tests.helpers import assert_close, bits, f64
 

@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 import torch
 
-from expert_moe_route_gb300 import synth
+from workloads import synth
 
 pytestmark = pytest.mark.gpu
 

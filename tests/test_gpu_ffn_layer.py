@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 import torch
 
-from expert_moe_route_gb300 import synth
+from workloads import synth
 from oracle import moe_oracle as O
 from tests.helpers import assert_close, bits, f64, near_tie_tokens, random_routing
 
@@ -97,6 +97,12 @@ def test_layer_forward(lib, name, T):
     tie = near_tie_tokens(ref["logits"], wl.R)
     same = (saved.topk_idx.cpu().numpy() == ref["idx"]).all(axis=1)
     assert (same | tie).all(), "routing differs on a token without a near tie"
+    # a row's h and o depend only on its token and expert: compare every row of
+    # every token routed alike, wherever the two layouts put it
+    gsr = saved.slot_row.cpu().numpy().reshape(wl.T, wl.R)[same].reshape(-1)
+    rsr = np.asarray(ref["slot_row"]).reshape(wl.T, wl.R)[same].reshape(-1)
+    assert_close(f64(saved.h)[gsr], ref["h"][rsr], "h (rows of tokens routed alike)")
+    assert_close(f64(saved.o)[gsr], ref["o"][rsr], "o (rows of tokens routed alike)")
     if same.all():
         assert np.array_equal(saved.offsets.cpu().numpy(), ref["offsets"])
         assert np.array_equal(saved.slot_row.cpu().numpy(), ref["slot_row"])
@@ -107,7 +113,7 @@ def test_layer_forward(lib, name, T):
 
 
 @pytest.mark.parametrize("name,T,E,f", [("tiny", None, None, None), ("train", 512, None, None),
-                                        ("mid", 1024, None, 448)])
+                                        ("mid", 1024, None, 448), ("mid", None, None, None)])
 def test_layer_backward(lib, name, T, E, f):
     over = {}
     if T is not None:

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from expert_moe_route_gb300 import synth
+from workloads import synth
 from oracle import moe_oracle as O
 from tests.helpers import LazyExperts, assert_close, bits, f64, near_tie_tokens
 
@@ -65,6 +65,27 @@ def _oracle_subset(inp, wl, toks, bias, train):
     return fw, bw
 
 
+def _tokens_covering_every_expert(gidx, same, E, seed):
+    """Tokens routed alike on both sides such that every expert with rows has at
+    least one of them (greedy: for each expert not yet covered, a random token
+    routed to it), plus a few random ones."""
+    rng = np.random.default_rng(seed)
+    covered = np.zeros(E, dtype=bool)
+    toks = set(rng.choice(np.nonzero(same)[0], 8, replace=False).tolist())
+    for t in toks:
+        covered[gidx[t]] = True
+    for e in np.unique(gidx):
+        if covered[e]:
+            continue
+        cand = np.nonzero(same & (gidx == e).any(axis=1))[0]
+        if cand.size == 0:
+            continue                                  # every row of e has a near tie
+        t = int(rng.choice(cand))
+        toks.add(t)
+        covered[gidx[t]] = True
+    return np.array(sorted(toks)), covered
+
+
 @pytest.mark.parametrize("name", ["large", "large_hot", "train"])
 def test_forward_full_size_sampled_tokens(lib, name):
     wl = synth.workload(name)
@@ -75,14 +96,25 @@ def test_forward_full_size_sampled_tokens(lib, name):
     gidx = run["saved"].topk_idx.cpu().numpy()
     same = (gidx == idx).all(axis=1)
     assert (same | near_tie_tokens(logits, wl.R)).all()
-    toks = np.sort(np.random.default_rng(1).choice(np.nonzero(same)[0], 8, replace=False))
+    toks, covered = _tokens_covering_every_expert(gidx, same, wl.E, seed=1)
+    counts = run["saved"].counts.cpu().numpy()
+    assert covered[counts > 0].mean() > 0.99           # (only an all-tie expert may be missed)
     fw, _ = _oracle_subset(run["inp"], wl, toks, bias, train=False)
     assert np.array_equal(fw["idx"], gidx[toks])
     assert_close(f64(run["y"][torch.from_numpy(toks).cuda()]), fw["y"], "y (sampled tokens)")
     rows = run["saved"].slot_row.cpu().numpy().reshape(wl.T, wl.R)[toks].reshape(-1)
     ref_rows = fw["slot_row"]                       # oracle's rows for the subset, same slot order
-    assert_close(f64(run["saved"].h[torch.from_numpy(rows).long().cuda()]),
-                 fw["h"][ref_rows], "h (sampled rows)")
+    sel = torch.from_numpy(rows).long().cuda()
+    # every expert with rows contributes at least one row to each comparison,
+    # and each expert's rows are checked on their own as well
+    assert_close(f64(run["saved"].h[sel]), fw["h"][ref_rows], "h (sampled rows)")
+    assert_close(f64(run["saved"].o[sel]), fw["o"][ref_rows], "o (sampled rows)")
+    ex = gidx[toks].reshape(-1)
+    gh, go = f64(run["saved"].h[sel]), f64(run["saved"].o[sel])
+    for e in np.unique(ex):
+        m = ex == e
+        assert_close(gh[m], fw["h"][ref_rows][m], f"h rows of expert {e}")
+        assert_close(go[m], fw["o"][ref_rows][m], f"o rows of expert {e}")
 
 
 def test_train_backward_full_size_sampled(lib):

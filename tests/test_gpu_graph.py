@@ -6,7 +6,7 @@ bit for bit."""
 import pytest
 import torch
 
-from expert_moe_route_gb300 import synth
+from workloads import synth
 
 pytestmark = pytest.mark.gpu
 

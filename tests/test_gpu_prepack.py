@@ -2,7 +2,7 @@
 import pytest
 import torch
 
-from expert_moe_route_gb300 import synth
+from workloads import synth
 
 pytestmark = pytest.mark.gpu
 

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from expert_moe_route_gb300 import synth
+from workloads import synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
