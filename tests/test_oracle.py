@@ -395,6 +395,36 @@ def test_backward_rounding_points_applied():
         assert np.array_equal(bw[key], O.bf16_round(bw[key]))
 
 
+def test_backward_rounding_points_hand_worked_case():
+    """A hand-derived one-token case (tests/golden/bwd_rounding_points.json) fixes
+    where the backward rounds: each expected value differs from what the same
+    arithmetic gives with that one rounding point skipped."""
+    with open(os.path.join(GOLD, "bwd_rounding_points.json")) as fh:
+        case = json.load(fh)
+    inp, want = case["inputs"], case["expected"]
+
+    def b16(v):
+        arr = np.asarray(v, np.float64)
+        assert np.array_equal(O.bf16_round(arr), arr)          # inputs are bf16 values
+        return O.f64_to_bf16_bits(arr)
+
+    wg = np.asarray(inp["w_gate"], np.float32)
+    W = [b16(inp[k]) for k in ("W1", "W3", "W2")]
+    fw = O.layer_fwd(b16(inp["x"]), wg, None, *W, 1)
+    bw = O.layer_bwd(fw, b16(inp["x"]), wg, *W, b16(inp["dy"]), 1)
+    for k in ("a", "b", "h", "o", "y"):
+        assert np.array_equal(fw[k], np.asarray(want[k], np.float64)), k
+    for k in ("do", "da", "db", "dx_perm", "dx", "dW1", "dW3", "dW2", "dW_gate"):
+        assert np.array_equal(bw[k], np.asarray(want[k], np.float64)), k
+    # without any rounding the same inputs give other values at every such point
+    fw0 = O.layer_fwd(b16(inp["x"]), wg, None, *W, 1, rounding=False)
+    bw0 = O.layer_bwd(fw0, b16(inp["x"]), wg, *W, b16(inp["dy"]), 1, rounding=False)
+    for k in ("h", "o"):
+        assert not np.array_equal(fw0[k], fw[k]), k
+    for k in ("da", "db", "dx_perm", "dW1", "dW3", "dW2"):
+        assert not np.array_equal(bw0[k], bw[k]), k
+
+
 # ---------------------------------------------------------------- shared expert
 def _shared_weights(seed, d, fs):
     r = _rng(seed)
