@@ -846,8 +846,8 @@ def run_reference(args):
             device = "cpu"
     except ImportError:
         device = "cpu"
-    for _ in range(args.warmup):
-        cpu_oracle_sample(wl, device, n1, shared_fs=args.shared_expert)
+    for _ in range(args.warmup):       # warm-up: a few tokens (the oracle's code paths, cached inputs)
+        cpu_oracle_sample(wl, device, min(8, n1), shared_fs=args.shared_expert)
     samples, t_all = [], 0.0
     for k in range(args.steps):        # steps alternate between the two sample sizes
         n = n1 if k % 2 == 0 else n2
