@@ -304,6 +304,99 @@ def dequantize_fp8_blocks(codes, scales):
 
 
 # ----------------------------------------------------------------------------
+# Microscaled fp8 for the expert GEMMs ("Enabling trillion-parameter models on
+# AWS EFA", section "Evaluation": the tokens travel as block-scaled fp8).
+# Reading for GEMMs that consume fp8 directly (the tensor cores' block-scaled
+# fp8 multiply takes one power-of-two scale per 32 consecutive elements along
+# the contraction): E4M3 codes, one UE8M0 scale (a power of two, stored as its
+# exponent + 127) per 32 consecutive elements of a row along K.  The scale of a
+# block is the smallest power of two 2^k with 448 * 2^k >= amax (so no code
+# saturates), k clamped to [-127, 127]; codes are the E4M3 values nearest to
+# x / 2^k, ties to even.  An all-zero block gets k = -127 (code 0) and zero
+# codes.  Weights are quantised the same way along their K (d for W1 and W3,
+# f for W2); the expert FFN quantises h = silu(a) * b the same way along f
+# before the down projection.
+# ----------------------------------------------------------------------------
+MX_BLOCK = 32
+MX_BIAS = 127
+
+
+def mx_scale_exponents(amax):
+    """Per block: the smallest integer k with 448 * 2^k >= amax, clamped to
+    [-127, 127] (k = -127 for amax = 0).  Exact: with amax = m * 2^e,
+    0.5 <= m < 1 and 448 = 0.875 * 2^9, k = e - 9 when m <= 0.875, else e - 8."""
+    a = np.asarray(amax, dtype=np.float64)
+    m, e = np.frexp(a)
+    k = np.where(m <= 0.875, e - 9, e - 8)
+    k = np.where(a == 0, -MX_BIAS, k)
+    return np.clip(k, -MX_BIAS, MX_BIAS).astype(np.int64)
+
+
+def quantize_mx(x):
+    """x: [rows, K] (bf16 bits or values), K % 32 == 0.  Returns E4M3 codes
+    uint8 [rows, K] and scale codes uint8 [rows, K/32] (k + 127)."""
+    xv = values(x)
+    rows, K = xv.shape
+    assert K % MX_BLOCK == 0
+    blocks = xv.reshape(rows, K // MX_BLOCK, MX_BLOCK)
+    k = mx_scale_exponents(np.abs(blocks).max(axis=2))
+    q = e4m3_round(blocks / np.ldexp(1.0, k)[:, :, None])      # exact division by 2^k
+    return e4m3_encode(q).reshape(rows, K), (k + MX_BIAS).astype(np.uint8)
+
+
+def dequantize_mx(codes, scales):
+    """codes uint8 [rows, K], scale codes uint8 [rows, K/32] -> float64 values."""
+    c = e4m3_decode(codes)
+    rows, K = c.shape
+    k = np.asarray(scales, dtype=np.int64)[:, : K // MX_BLOCK] - MX_BIAS
+    return (c.reshape(rows, K // MX_BLOCK, MX_BLOCK) * np.ldexp(1.0, k)[:, :, None]).reshape(rows, K)
+
+
+def expert_ffn_mx(xq, xs, offsets, W1q, W1s, W3q, W3s, W2q, W2s, quantize_h=True, row_scale=None):
+    """The expert FFN on microscaled fp8 operands.  Per expert e over its rows:
+
+        x = dequant(xq, xs);  w1, w3, w2 = dequant(W*q[e], W*s[e])
+        a = x w1^T, b = x w3^T,  hv = silu(a) * b          (float64)
+        hq, hs = quantize_mx(hv) along f;  h = dequant(hq, hs)   (hv itself
+                                                    when quantize_h is False)
+        o = bf16(s * (h w2^T))                              s = row_scale[row] or 1
+
+    W1q, W3q: uint8 [E, f, d] with scales [E, f, d/32]; W2q: uint8 [E, d, f]
+    with scales [E, d, f/32].  Returns a, b, hv, hq, hs, h, o.
+    """
+    E = len(offsets) - 1
+    N = int(offsets[-1])
+    f, d = W1q.shape[1], W1q.shape[2]
+    a = np.zeros((N, f))
+    b = np.zeros((N, f))
+    hv = np.zeros((N, f))
+    h = np.zeros((N, f))
+    hq = np.zeros((N, f), dtype=np.uint8)
+    hs = np.zeros((N, f // MX_BLOCK), dtype=np.uint8)
+    o = np.zeros((N, d))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r0 == r1:
+            continue
+        x = dequantize_mx(xq[r0:r1], xs[r0:r1])
+        ae = x @ dequantize_mx(W1q[e], W1s[e]).T
+        be = x @ dequantize_mx(W3q[e], W3s[e]).T
+        ve = silu(ae) * be
+        if quantize_h:
+            qe, se = quantize_mx(ve)
+            he = dequantize_mx(qe, se)
+            hq[r0:r1], hs[r0:r1] = qe, se
+        else:
+            he = ve
+        pe = he @ dequantize_mx(W2q[e], W2s[e]).T
+        if row_scale is not None:
+            pe = np.asarray(row_scale, dtype=np.float64)[r0:r1, None] * pe
+        a[r0:r1], b[r0:r1], hv[r0:r1], h[r0:r1] = ae, be, ve, he
+        o[r0:r1] = bf16_round(pe)
+    return a, b, hv, hq, hs, h, o
+
+
+# ----------------------------------------------------------------------------
 # Whole layer.
 # ----------------------------------------------------------------------------
 def shared_expert_fwd(x, Ws1, Ws3, Ws2, rounding=True):

@@ -566,3 +566,78 @@ def test_fp8_block_quantization_properties():
     z = np.zeros((1, 256), np.uint16)
     c0, s0 = O.quantize_fp8_blocks(z)
     assert not c0.any() and not s0.any()
+
+
+# ---------------------------------------------------------------- microscaled fp8 (MX) GEMM operands
+def test_mx_scale_exponents_hand_cases_and_brute_force():
+    # hand cases: 448 * 2^k is the first power-of-two multiple of 448 at or above amax
+    cases = {448.0: 0, 449.0: 1, 1.0: -8, 224.0: -1, 224.5: 0, 0.0: -127, 2.0 ** -140: -127,
+             3e38: 120, 1.75 * 2.0 ** -8: -16, 2.0 ** 127: 119}
+    got = O.mx_scale_exponents(np.array(list(cases)))
+    assert list(got) == list(cases.values())
+    # brute force over every k in [-127, 127]
+    r = _rng(30)
+    amax = np.concatenate([np.abs(r.standard_normal(2000)) * np.exp(r.uniform(-40, 40, 2000)),
+                           448.0 * np.ldexp(1.0, r.integers(-60, 60, 200))])
+    ks = np.arange(-127, 128)
+    for a, k in zip(amax, O.mx_scale_exponents(amax)):
+        ok = ks[448.0 * np.ldexp(1.0, ks) >= a]
+        assert k == (ok.min() if ok.size else 127)
+
+
+def test_mx_quantization_matches_torch_e4m3_and_round_trips():
+    r = _rng(31)
+    x = _bf16_bits_of(r.standard_normal((9, 256)) * np.exp(r.uniform(-8, 8, (9, 1))))
+    x[3, 32:64] = 0                                      # an all-zero block
+    codes, scales = O.quantize_mx(x)
+    assert codes.shape == (9, 256) and scales.shape == (9, 8) and scales.dtype == np.uint8
+    xv = O.bf16_to_f64(x)
+    blocks = xv.reshape(9, 8, 32)
+    k = scales.astype(np.int64) - 127
+    # the codes are torch's round-to-nearest-even E4M3 of the exactly scaled values
+    scaled = (blocks / np.ldexp(1.0, k)[:, :, None]).astype(np.float32)
+    want = torch.tensor(scaled).to(torch.float8_e4m3fn).view(torch.uint8).numpy().reshape(9, 256)
+    assert np.array_equal(codes, want)
+    # the block maximum lands in (224, 448] (no code saturates), except all-zero blocks
+    amax = np.abs(blocks).max(axis=2)
+    nz = amax > 0
+    top = amax[nz] / np.ldexp(1.0, k[nz])
+    assert ((top > 224) & (top <= 448)).all()
+    assert k[3, 1] == -127 and not codes[3, 32:64].any()
+    # round trip within half an E4M3 step
+    back = O.dequantize_mx(codes, scales).reshape(9, 8, 32)
+    step = np.maximum(np.abs(blocks) * 2.0 ** -4, np.ldexp(1.0, k)[:, :, None] * 2.0 ** -10)
+    assert (np.abs(back - blocks) <= step * (1 + 1e-12)).all()
+
+
+def test_expert_ffn_mx_textbook_loop():
+    """One expert, tiny sizes: a plain triple loop over the dequantised operands."""
+    r = _rng(32)
+    d, f, n = 64, 64, 3
+    x = _bf16_bits_of(r.standard_normal((n, d)))
+    W1 = _bf16_bits_of(r.standard_normal((1, f, d)) * 0.1)
+    W3 = _bf16_bits_of(r.standard_normal((1, f, d)) * 0.1)
+    W2 = _bf16_bits_of(r.standard_normal((1, d, f)) * 0.1)
+    xq, xs = O.quantize_mx(x)
+    q = [O.quantize_mx(w[0]) for w in (W1, W3, W2)]
+    wq = [(c[None], s[None]) for c, s in q]
+    offsets = np.array([0, n])
+    a, b, hv, hq, hs, h, o = O.expert_ffn_mx(xq, xs, offsets, *wq[0], *wq[1], *wq[2])
+    xd = O.dequantize_mx(xq, xs)
+    w1, w3, w2 = (O.dequantize_mx(c, s) for c, s in q)
+    for i in range(n):
+        for j in range(f):
+            aa = sum(xd[i, k] * w1[j, k] for k in range(d))
+            bb = sum(xd[i, k] * w3[j, k] for k in range(d))
+            assert abs(a[i, j] - aa) <= 1e-12 * (1 + abs(aa))
+            assert abs(b[i, j] - bb) <= 1e-12 * (1 + abs(bb))
+            assert abs(hv[i, j] - aa / (1 + math.exp(-aa)) * bb) <= 1e-12 * (1 + abs(hv[i, j]))
+    # h goes through the (separately pinned) MX quantisation along f
+    assert np.array_equal(hq, O.quantize_mx(hv)[0]) and np.array_equal(hs, O.quantize_mx(hv)[1])
+    for i in range(n):
+        for c in range(d):
+            oo = sum(h[i, j] * w2[c, j] for j in range(f))
+            assert o[i, c] == O.bf16_round(np.array([oo]))[0]
+    # without the h quantisation, h is hv
+    _, _, hv2, _, _, h2, _ = O.expert_ffn_mx(xq, xs, offsets, *wq[0], *wq[1], *wq[2], quantize_h=False)
+    assert np.array_equal(h2, hv2)
