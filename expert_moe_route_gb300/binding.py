@@ -21,6 +21,7 @@ MOE_WEIGHTS_PREPACKED = 0x4
 MOE_SINGLE_CTA_TILES = 0x8
 MOE_SHARED_SERIAL = 0x10
 MOE_FP8_DISPATCH = 0x20
+MOE_FP8_MX = 0x40
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CUDA"}
 
@@ -28,7 +29,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 SYMBOLS = ("moe_status_string", "moe_version", "moe_last_cuda_error", "moe_trace_events",
            "moe_kernel_launches", "moe_selftest_wait_timeout",
            "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_dispatch_fp8",
-           "moe_dequant_fp8", "moe_prepack_weights", "moe_grouped_ffn", "moe_grouped_ffn_fp8",
+           "moe_dequant_fp8", "moe_quantize_mx", "moe_dispatch_mx", "moe_grouped_ffn_mx",
+           "moe_prepack_weights", "moe_grouped_ffn", "moe_grouped_ffn_fp8",
            "moe_combine", "moe_layer_fwd", "moe_layer_bwd")
 
 # moe_stage_t
@@ -55,10 +57,15 @@ class moe_shared_t(ctypes.Structure):
                 ("dW2", _vp)]
 
 
+class moe_mx_weights_t(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("W1q", "W1s", "W3q", "W3s", "W2q", "W2s")]
+
+
 class moe_layer_t(ctypes.Structure):
     _fields_ = [("T", _i), ("d", _i), ("E", _i), ("R", _i), ("f", _i), ("w_gate", _vp),
                 ("bias", _vp), ("W1", _vp), ("W3", _vp), ("W2", _vp),
-                ("shared", ctypes.POINTER(moe_shared_t))]
+                ("shared", ctypes.POINTER(moe_shared_t)),
+                ("mx", ctypes.POINTER(moe_mx_weights_t))]
 
 
 class moe_saved_t(ctypes.Structure):
@@ -90,6 +97,15 @@ def _declare(lib):
                                      _szp, _u, _vp]
     lib.moe_dequant_fp8.restype = _i
     lib.moe_dequant_fp8.argtypes = [_vp, _vp, _i, _i, _vp, _vp]
+    _ll = ctypes.c_longlong
+    lib.moe_quantize_mx.restype = _i
+    lib.moe_quantize_mx.argtypes = [_vp, _ll, _i, _vp, _vp, _vp]
+    lib.moe_dispatch_mx.restype = _i
+    lib.moe_dispatch_mx.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _szp, _u, _vp]
+    lib.moe_grouped_ffn_mx.restype = _i
+    lib.moe_grouped_ffn_mx.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
+                                       _vp, _vp, _vp, _vp, _vp, _szp, _u, _vp]
     lib.moe_prepack_weights.restype = _i
     lib.moe_prepack_weights.argtypes = [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]
     lib.moe_grouped_ffn.restype = _i
@@ -285,6 +301,65 @@ def moe_grouped_ffn_fp8(xq_perm, xscale_perm, offsets, W1, W3, W2, h, out, ws, a
     _check(st, "moe_grouped_ffn_fp8")
 
 
+def mx_scale_row_bytes(K: int) -> int:
+    """Bytes per row of microscaled fp8 scales: K/32, rounded up to a multiple of 16."""
+    return -(-K // 512) * 16
+
+
+def moe_quantize_mx(W, codes, scales, stream=None):
+    """Microscaled fp8 codes (uint8 [rows, K]) and scales (uint8 [rows, sk]) of a bf16
+    matrix [..., K] along its last dimension."""
+    K = W.shape[-1]
+    rows = W.numel() // K
+    _dt(W, torch.bfloat16, "W"); _dt(codes, torch.uint8, "codes"); _dt(scales, torch.uint8, "scales")
+    _check(lib().moe_quantize_mx(_p(W), rows, K, _p(codes), _p(scales), _stream(stream)),
+           "moe_quantize_mx")
+
+
+def moe_dispatch_mx(x, topk_idx, E, counts, offsets, row_slot, slot_row, xq_perm, xscale_perm, ws,
+                    flags=0, stream=None):
+    """Dispatch with rows in microscaled fp8: codes uint8 [N, d], scales uint8 [N, sk(d)]."""
+    T, R = topk_idx.shape
+    d = x.shape[1]
+    _dt(x, torch.bfloat16, "x"); _dt(xq_perm, torch.uint8, "xq_perm")
+    _dt(xscale_perm, torch.uint8, "xscale_perm")
+    for name, t in (("topk_idx", topk_idx), ("counts", counts), ("offsets", offsets),
+                    ("row_slot", row_slot), ("slot_row", slot_row)):
+        _dt(t, torch.int32, name)
+    n = ctypes.c_size_t(ws.numel())
+    st = lib().moe_dispatch_mx(_p(x), _p(topk_idx), T, d, E, R, _p(counts), _p(offsets),
+                               _p(row_slot), _p(slot_row), _p(xq_perm), _p(xscale_perm), _p(ws),
+                               ctypes.byref(n), flags, _stream(stream))
+    _check(st, "moe_dispatch_mx")
+
+
+def grouped_ffn_mx_ws_bytes(N, d, f, E) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_grouped_ffn_mx(None, None, None, N, d, f, E, None, None, None, None, None,
+                                    None, None, None, None, None, None, ctypes.byref(n), 0, None),
+           "moe_grouped_ffn_mx(ws query)")
+    return n.value
+
+
+def moe_grouped_ffn_mx(xq, xs, offsets, W1q, W1s, W3q, W3s, W2q, W2s, out, ws, hq=None, hs=None,
+                       row_scale=None, flags=0, stream=None):
+    """The grouped SwiGLU FFN on microscaled fp8 operands (see include/moe.h).
+    W1q, W3q: uint8 [E, f, d] (scales [E, f, sk(d)]); W2q: uint8 [E, d, f] (scales [E, d, sk(f)])."""
+    N, d = xq.shape
+    E, f, _ = W1q.shape
+    for name, t in (("xq", xq), ("xs", xs), ("W1q", W1q), ("W1s", W1s), ("W3q", W3q),
+                    ("W3s", W3s), ("W2q", W2q), ("W2s", W2s), ("hq", hq), ("hs", hs)):
+        _dt(t, torch.uint8, name)
+    _dt(out, torch.bfloat16, "out")
+    _dt(offsets, torch.int32, "offsets")
+    _dt(row_scale, torch.float32, "row_scale")
+    n = ctypes.c_size_t(ws.numel())
+    st = lib().moe_grouped_ffn_mx(_p(xq), _p(xs), _p(offsets), N, d, f, E, _p(W1q), _p(W1s),
+                                  _p(W3q), _p(W3s), _p(W2q), _p(W2s), _p(row_scale), _p(hq),
+                                  _p(hs), _p(out), _p(ws), ctypes.byref(n), flags, _stream(stream))
+    _check(st, "moe_grouped_ffn_mx")
+
+
 def moe_prepack_weights(W1, W3, W2, W1p, W3p, W2p, stream=None):
     """Forward weight tiles (see include/moe.h); returns nothing, fills W1p, W3p, W2p."""
     E, f, d = W1.shape
@@ -315,19 +390,39 @@ class Shared:
         self.c = moe_shared_t(self.fs, _p(W1), _p(W3), _p(W2), _p(dW1), _p(dW3), _p(dW2))
 
 
+class MxWeights:
+    """The expert weights in microscaled fp8 (moe_mx_weights_t), quantised on the device
+    from bf16 W1, W3 [E, f, d] and W2 [E, d, f] with moe_quantize_mx."""
+
+    def __init__(self, W1, W3, W2, stream=None):
+        def q(W):
+            K = W.shape[-1]
+            codes = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+            scales = torch.empty(W.shape[:-1] + (mx_scale_row_bytes(K),), dtype=torch.uint8,
+                                 device=W.device)
+            moe_quantize_mx(W, codes, scales, stream)
+            return codes, scales
+        (self.W1q, self.W1s), (self.W3q, self.W3s), (self.W2q, self.W2s) = q(W1), q(W3), q(W2)
+        self.c = moe_mx_weights_t(*[_p(getattr(self, n)) for n, _ in moe_mx_weights_t._fields_])
+
+
 class Layer:
     """Parameters of one MoE layer (device tensors) and their C struct."""
 
-    def __init__(self, w_gate, bias, W1, W3, W2, R, T, shared: Shared = None):
+    def __init__(self, w_gate, bias, W1, W3, W2, R, T, shared: Shared = None,
+                 mx: MxWeights = None):
         self.w_gate, self.bias, self.W1, self.W3, self.W2 = w_gate, bias, W1, W3, W2
         self.E, self.f, self.d = W1.shape
         self.R, self.T = R, T
         self.shared = shared
+        self.mx = mx
         self.c = moe_layer_t(T, self.d, self.E, R, self.f, _p(w_gate), _p(bias), _p(W1), _p(W3),
-                             _p(W2), ctypes.pointer(shared.c) if shared is not None else None)
+                             _p(W2), ctypes.pointer(shared.c) if shared is not None else None,
+                             ctypes.pointer(mx.c) if mx is not None else None)
 
     def with_tokens(self, T):
-        return Layer(self.w_gate, self.bias, self.W1, self.W3, self.W2, self.R, T, self.shared)
+        return Layer(self.w_gate, self.bias, self.W1, self.W3, self.W2, self.R, T, self.shared,
+                     self.mx)
 
 
 class Saved:

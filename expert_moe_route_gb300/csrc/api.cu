@@ -388,6 +388,79 @@ moe_status_t moe_grouped_ffn_fp8(const uint8_t* xq_perm, const float* xscale_per
   return finish(e, err, flags, s);
 }
 
+moe_status_t moe_quantize_mx(const uint16_t* W, long long rows, int K, uint8_t* codes,
+                             uint8_t* scales, moe_stream_t stream) {
+  if (rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 32) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  if (!W || !codes || !scales) return MOE_ERR_INVALID_ARG;
+  if (!al16(W) || !al16(codes) || !al16(scales)) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = S(stream);
+  return finish(launch_quantize_mx(W, rows, K, codes, scales, s), nullptr, 0, s);
+}
+
+moe_status_t moe_dispatch_mx(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int R,
+                             int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                             int32_t* slot_row, uint8_t* xq_perm, uint8_t* xscale_perm, void* ws,
+                             size_t* ws_bytes, unsigned flags, moe_stream_t stream) {
+  moe_status_t st = shape_check(T, d, E, R);
+  if (st != MOE_OK) return st;
+  if (d % 128) return MOE_ERR_UNSUPPORTED;
+  if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t need = kErrBytes + dispatch_ws_bytes(T, E);
+  if (!ws) {
+    *ws_bytes = need;
+    return MOE_OK;
+  }
+  if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
+  if (!counts || !offsets || (T > 0 && (!x || !topk_idx || !row_slot || !slot_row || !xq_perm ||
+                                        !xscale_perm)))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!al16(x) || !al16(xq_perm) || !al16(xscale_perm))) return MOE_ERR_UNSUPPORTED;
+  if (!init_once()) return MOE_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  int* err = static_cast<int*>(ws);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  cudaError_t e;
+  {
+    Stage st_(s, MOE_STAGE_DISPATCH);
+    e = launch_dispatch_mx(x, topk_idx, T, d, E, R, counts, offsets, row_slot, slot_row, xq_perm,
+                           xscale_perm, static_cast<uint8_t*>(ws) + kErrBytes, err, s);
+  }
+  return finish(e, err, flags, s);
+}
+
+moe_status_t moe_grouped_ffn_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets,
+                                int N, int d, int f, int E, const uint8_t* W1q,
+                                const uint8_t* W1s, const uint8_t* W3q, const uint8_t* W3s,
+                                const uint8_t* W2q, const uint8_t* W2s, const float* row_scale,
+                                uint8_t* hq, uint8_t* hs, uint16_t* out, void* ws,
+                                size_t* ws_bytes, unsigned flags, moe_stream_t stream) {
+  if (N < 0 || d <= 0 || f <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (!ffn_mx_supported(d, f) || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (!ws_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t need = kErrBytes + ffn_mx_ws_bytes(N, d, f, E);
+  if (!ws) {
+    *ws_bytes = need;
+    return MOE_OK;
+  }
+  if (*ws_bytes < need || !al256(ws)) return MOE_ERR_WORKSPACE;
+  if (!offsets || !W1q || !W1s || !W3q || !W3s || !W2q || !W2s) return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!xq || !xs || !out)) return MOE_ERR_INVALID_ARG;
+  if ((hq == nullptr) != (hs == nullptr)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {xq, xs, W1q, W1s, W3q, W3s, W2q, W2s, hq, hs, out};
+  for (const void* p : ps)
+    if (p && !al16(p)) return MOE_ERR_UNSUPPORTED;
+  if (!init_once()) return MOE_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  int* err = static_cast<int*>(ws);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(int), s));
+  cudaError_t e = launch_ffn_mx(xq, xs, offsets, N, d, f, E, W1q, W1s, W3q, W3s, W2q, W2s,
+                                row_scale, hq, hs, out, static_cast<uint8_t*>(ws) + kErrBytes, err,
+                                s);
+  return finish(e, err, flags, s);
+}
+
 moe_status_t moe_prepack_weights(const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, int E,
                                  int d, int f, uint16_t* W1p, uint16_t* W3p, uint16_t* W2p,
                                  moe_stream_t stream) {
@@ -448,11 +521,19 @@ static size_t fp8_rows_ws(const moe_layer_t* L) {
   return align_up(N * d, 256) + align_up(N * (d / 128) * 4, 256);
 }
 
+// microscaled fp8 (MOE_FP8_MX): the rows' codes and scales, then the grouped FFN's own workspace
+static size_t mx_rows_ws(const moe_layer_t* L) {
+  const size_t N = (size_t)L->T * L->R, d = L->d;
+  return align_up(N * d, 256) + align_up(N * mx_scale_row_bytes(L->d), 256) +
+         ffn_mx_ws_bytes((int)N, L->d, L->f, L->E);
+}
+
 static size_t layer_fwd_ws(const moe_layer_t* L, unsigned flags) {
   const int N = L->T * L->R;
   return kErrBytes + align_up(dispatch_ws_bytes(L->T, L->E), 256) + tiles_ws_bytes(N, L->E) +
          align_up(gate_ws_bytes(L->d, L->E), 256) + shared_fwd_ws(L) +
-         ((flags & MOE_FP8_DISPATCH) ? fp8_rows_ws(L) : 0);
+         ((flags & MOE_FP8_DISPATCH) ? fp8_rows_ws(L) : 0) +
+         ((flags & MOE_FP8_MX) ? mx_rows_ws(L) : 0);
 }
 
 moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
@@ -463,6 +544,9 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   if ((flags & MOE_WEIGHTS_PREPACKED) && !prepack_supported(L->d, L->f)) return MOE_ERR_UNSUPPORTED;
   const bool fp8 = (flags & MOE_FP8_DISPATCH) != 0;
   if (fp8 && L->d % 128) return MOE_ERR_UNSUPPORTED;
+  const bool mx = (flags & MOE_FP8_MX) != 0;
+  if (mx && (fp8 || (flags & MOE_WEIGHTS_PREPACKED) || !ffn_mx_supported(L->d, L->f)))
+    return MOE_ERR_UNSUPPORTED;
   if (!ws_bytes) return MOE_ERR_INVALID_ARG;
   const size_t need = layer_fwd_ws(L, flags);
   if (!ws) {
@@ -473,8 +557,16 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   if (L->T == 0) return MOE_OK;   // nothing to route: no buffer is touched
   if (!sv || !x || !y) return MOE_ERR_INVALID_ARG;
   if (!sv->logits || !sv->topk_idx || !sv->topk_w || !sv->counts || !sv->offsets ||
-      !sv->row_slot || !sv->slot_row || !sv->x_perm || !sv->h || !sv->o)
+      !sv->row_slot || !sv->slot_row || !sv->o || (!mx && (!sv->x_perm || !sv->h)))
     return MOE_ERR_INVALID_ARG;
+  const moe_mx_weights_t* MX = L->mx;
+  if (mx && (!MX || !MX->W1q || !MX->W1s || !MX->W3q || !MX->W3s || !MX->W2q || !MX->W2s))
+    return MOE_ERR_INVALID_ARG;
+  if (mx) {
+    const void* qs[] = {MX->W1q, MX->W1s, MX->W3q, MX->W3s, MX->W2q, MX->W2s};
+    for (const void* p : qs)
+      if (!al16(p)) return MOE_ERR_UNSUPPORTED;
+  }
   if ((sv->a == nullptr) != (sv->b == nullptr)) return MOE_ERR_INVALID_ARG;
   const moe_shared_t* SH = L->shared;
   if (SH && ((sv->sa == nullptr) != (sv->sb == nullptr) || (sv->sa && !sv->sh)))
@@ -500,6 +592,13 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   if (fp8) {
     xq = static_cast<uint8_t*>(c.take((size_t)N * d));
     xs = static_cast<float*>(c.take((size_t)N * (d / 128) * 4));
+  }
+  uint8_t *mq = nullptr, *ms = nullptr;
+  void* mws = nullptr;
+  if (mx) {
+    mq = static_cast<uint8_t*>(c.take((size_t)N * d));
+    ms = static_cast<uint8_t*>(c.take((size_t)N * mx_scale_row_bytes(d)));
+    mws = c.take(ffn_mx_ws_bytes(N, d, f, E));
   }
   int32_t* s_off = nullptr;
   void* s_tws = nullptr;
@@ -542,13 +641,21 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
       MOE_TRY(launch_dispatch_fp8(x, sv->topk_idx, T, d, E, R, sv->counts, sv->offsets,
                                   sv->row_slot, sv->slot_row, xq, xs, dws, err, s));
       MOE_TRY(launch_dequant_fp8(xq, xs, N, d, sv->x_perm, s));
+    } else if (mx) {   // microscaled fp8 rows, multiplied as they are by the fp8 tensor cores
+      MOE_TRY(launch_dispatch_mx(x, sv->topk_idx, T, d, E, R, sv->counts, sv->offsets,
+                                 sv->row_slot, sv->slot_row, mq, ms, dws, err, s));
     } else {
       MOE_TRY(launch_dispatch(x, sv->topk_idx, T, d, E, R, sv->counts, sv->offsets, sv->row_slot,
                               sv->slot_row, sv->x_perm, dws, err, s));
     }
   }
-  MOE_TRY(launch_ffn_fwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
-                         sv->h, sv->o, tws, err, (flags & MOE_WEIGHTS_PREPACKED) != 0, pairs, s));
+  if (mx)
+    MOE_TRY(launch_ffn_mx(mq, ms, sv->offsets, N, d, f, E, MX->W1q, MX->W1s, MX->W3q, MX->W3s,
+                          MX->W2q, MX->W2s, nullptr, nullptr, nullptr, sv->o, mws, err, s));
+  else
+    MOE_TRY(launch_ffn_fwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a,
+                           sv->b, sv->h, sv->o, tws, err, (flags & MOE_WEIGHTS_PREPACKED) != 0,
+                           pairs, s));
   if (SH && !side) MOE_TRY(shared_fwd());
   if (side) MOE_TRY(join.now());
   cudaError_t e;

@@ -64,6 +64,29 @@ __device__ __forceinline__ void e4m3x8_scaled(const uint2& q, float scale, float
   }
 }
 
+// Microscaled fp8 (MX): E4M3 codes with one power-of-two scale per 32
+// consecutive elements along K, stored as the exponent k + 127 (UE8M0).  k is
+// the smallest integer with 448 * 2^k >= the block's amax, clamped to
+// [-127, 127] (amax = 0, or below 2^-126, gives -127), so no code saturates.
+// With amax = 1.m * 2^(ef - 127) (fp32 fields) and 448 = 1.75 * 2^8:
+// k = ef - 135 when 1.m <= 1.75, else ef - 134.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = (int)((b >> 23) & 0xffu);
+  if (ef == 0) return -127;
+  const int k = ((b & 0x7fffffu) <= 0x600000u) ? ef - 135 : ef - 134;
+  return k < -127 ? -127 : (k > 127 ? 127 : k);
+}
+
+// Four E4M3 codes (bytes, low first) of v[0..3] * 2^-k, rounded to nearest even.
+__device__ __forceinline__ uint32_t mx_codes4(const float* v, int k) {
+  const __nv_fp8x2_storage_t p0 = __nv_cvt_float2_to_fp8x2(
+      make_float2(ldexpf(v[0], -k), ldexpf(v[1], -k)), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t p1 = __nv_cvt_float2_to_fp8x2(
+      make_float2(ldexpf(v[2], -k), ldexpf(v[3], -k)), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)p0 | ((uint32_t)p1 << 16);
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -388,6 +411,46 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;
+}
+
+// D[tmem] (+)= (A * 2^sa) (B * 2^sb)^T with E4M3 A and B (one 32-deep K step)
+// and one UE8M0 scale per row of A and per column of B read from tensor memory
+// (kind::mxf8f6f4, scale_vec::1X).  Measured layout on the GB300 for M = 128:
+// row m of A reads its scale from lane m, column sfa + m / 32; column n of B
+// reads lane (n % 32) of the row's lane quadrant, column sfb + n / 32; the
+// instruction descriptor's scale ids pick the byte of the 32-bit cell.
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4: E4M3 A and B, K-major, UE8M0 scales.
+//   bits 4-5 B scale id, 7-9 A format (0 = E4M3), 10-12 B format, bits 17-22
+//   N >> 3, bit 23 scale format (1 = UE8M0), bits 27-28 M >> 7, bits 29-30 A scale id.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id_a, int sf_id_b) {
+  return ((uint32_t)sf_id_b << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 7) << 27) | ((uint32_t)sf_id_a << 29);
+}
+
+// This warp's 32 lanes (its lane quadrant), `n` consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+        "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.

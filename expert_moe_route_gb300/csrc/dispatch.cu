@@ -357,6 +357,49 @@ __global__ void __launch_bounds__(256) permute_rows_fp8_kernel(
   }
 }
 
+// Microscaled fp8 rows (mx_exponent, mx_codes4).  One warp per source row
+// (token t of x, or row t of a weight matrix): each
+// lane takes 8 channels, four lanes one 32-channel block (amax by shuffles
+// within the four), codes = E4M3(v * 2^-k) rounded to nearest even (exact
+// scaling), and writes the 8-byte code groups and the block's scale byte to
+// the row's R destination rows (slot_row), or to row t itself when slot_row is
+// null.  Scale rows are sk bytes apart (K/32 rounded up to 16).
+__global__ void __launch_bounds__(256) quantize_mx_rows_kernel(
+    const uint16_t* __restrict__ x, long long rows, int K, int R, int N,
+    const int32_t* __restrict__ slot_row, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+    int sk) {
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x / 32;
+  for (long long t = blockIdx.x * (long long)warps + threadIdx.x / 32; t < rows;
+       t += (long long)gridDim.x * warps) {
+    int my_row = -1;                               // (unused when slot_row is null)
+    if (slot_row != nullptr) {
+      my_row = lane < R ? slot_row[(size_t)t * R + lane] : -1;
+      if ((unsigned)my_row >= (unsigned)N) my_row = -1;
+    }
+    const int nr = slot_row == nullptr ? 1 : R;
+    for (int base = 0; base < K; base += 256) {    // eight blocks per pass, warp-uniform
+      const int c = base + lane * 8;
+      const bool valid = c < K;
+      float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (valid) unpack8(ldg_nc_v4(x + (size_t)t * K + c), v);
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      const int k = mx_exponent(amax);
+      const uint32_t w[2] = {mx_codes4(v, k), mx_codes4(v + 4, k)};
+      for (int r = 0; r < nr; ++r) {
+        const long long row = slot_row == nullptr ? t : (long long)__shfl_sync(kFull, my_row, r);
+        if (row < 0 || !valid) continue;
+        *reinterpret_cast<uint2*>(xq + (size_t)row * K + c) = make_uint2(w[0], w[1]);
+        if ((lane & 3) == 0) xs[(size_t)row * sk + c / 32] = (uint8_t)(k + 127);
+      }
+    }
+  }
+}
+
 // Identity expert for fp8-dispatched rows: out = bf16(code * scale).
 __global__ void __launch_bounds__(256) dequant_fp8_kernel(const uint8_t* __restrict__ xq,
                                                           const float* __restrict__ xs, long long N,
@@ -436,6 +479,33 @@ cudaError_t launch_dispatch_fp8(const uint16_t* x, const int32_t* idx, int T, in
   if (e != cudaSuccess || T == 0) return e;
   const int blocks = ceil_div(T, 8) < 152 * 8 ? ceil_div(T, 8) : 152 * 8;
   permute_rows_fp8_kernel<<<blocks, 256, 0, s>>>(x, T, d, R, T * R, slot_row, xq, xs);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+int mx_scale_row_bytes(int K) { return ceil_div(K / 32, 16) * 16; }
+
+cudaError_t launch_quantize_mx(const uint16_t* x, long long rows, int K, uint8_t* xq,
+                               uint8_t* xs, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const long long want = (rows + 7) / 8;
+  const int blocks = want < 152 * 8 ? (int)want : 152 * 8;
+  quantize_mx_rows_kernel<<<blocks, 256, 0, s>>>(x, rows, K, 1, 0, nullptr, xq, xs,
+                                                 mx_scale_row_bytes(K));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_mx(const uint16_t* x, const int32_t* idx, int T, int d, int E, int R,
+                               int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                               int32_t* slot_row, uint8_t* xq, uint8_t* xs, void* ws, int* err,
+                               cudaStream_t s) {
+  cudaError_t e = launch_dispatch(nullptr, idx, T, d, E, R, counts, offsets, row_slot, slot_row,
+                                  nullptr, ws, err, s);
+  if (e != cudaSuccess || T == 0) return e;
+  const int blocks = ceil_div(T, 8) < 152 * 8 ? ceil_div(T, 8) : 152 * 8;
+  quantize_mx_rows_kernel<<<blocks, 256, 0, s>>>(x, T, d, R, T * R, slot_row, xq, xs,
+                                                 mx_scale_row_bytes(d));
   count_launches(1);
   return cudaGetLastError();
 }

@@ -887,6 +887,24 @@ bool make_map_tiles(CUtensorMap* m, const void* base, long long tiles, long long
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool encode_map_2d(void* map, int dtype, const void* base, unsigned long long inner,
+                   unsigned long long outer, unsigned long long row_bytes, unsigned box_inner,
+                   unsigned box_outer, bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(static_cast<CUtensorMap*>(map), static_cast<CUtensorMapDataType>(dtype), 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 int sm_count() {
   static int n[64] = {0};
   int dev = 0;
@@ -995,13 +1013,6 @@ static CUtensorMap* expert_maps(void* ws, int N, int E) {
   return reinterpret_cast<CUtensorMap*>(static_cast<uint8_t*>(ws) + tile_list_bytes(N, E));
 }
 
-struct TileLists {
-  const int32_t* count;
-  const int2* tiles;
-  const int32_t* tail_count;
-  const int2* tails;
-};
-
 TileLists tile_lists(void* ws, int E) {
   uint8_t* b = static_cast<uint8_t*>(ws);
   return {reinterpret_cast<const int32_t*>(b), reinterpret_cast<const int2*>(b + 16 + 8 * (size_t)E),
@@ -1009,7 +1020,7 @@ TileLists tile_lists(void* ws, int E) {
 }
 
 cudaError_t launch_build_tiles(const int32_t* offsets, int E, void* ws, cudaStream_t s,
-                               int tile_rows = BM, int tail_rows = 0) {
+                               int tile_rows, int tail_rows) {
   uint8_t* b = static_cast<uint8_t*>(ws);
   build_tiles_kernel<<<1, 1024, 0, s>>>(offsets, E, tile_rows, tail_rows,
                                         reinterpret_cast<int2*>(b + 16 + 8 * (size_t)E),

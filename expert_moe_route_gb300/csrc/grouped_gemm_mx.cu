@@ -1,0 +1,455 @@
+// Grouped per-expert SwiGLU FFN on microscaled fp8 operands, on the 5th-generation
+// tensor cores (tcgen05.mma kind::mxf8f6f4 with UE8M0 block scales).
+// ("Enabling trillion-parameter models on AWS EFA", section "Evaluation": the
+// tokens travel as block-scaled fp8; here the expert GEMMs consume them as they
+// are, with weights quantised the same way.)
+//
+// Operands: E4M3 codes, K contiguous, one power-of-two scale per 32 elements
+// along K (scale rows padded to 16 bytes).  Two modes of one kernel:
+//   GATEUP  [a | b] = x W1[e]^T | x W3[e]^T;  epilogue h = silu(a) b (fp32),
+//           written as microscaled fp8 along f (codes + scales)
+//   DOWN    o = bf16(s_row * (h W2[e]^T))
+// One CTA per SM, 128-row tiles of an expert's rows (ragged, from the tile
+// list), 256 output columns (GATEUP: 128 of W1 and the same 128 of W3).  Roles
+// (448 threads): warp 0 issues TMA loads of 128-deep k-blocks (A 16 KB, B 32 KB)
+// into four stages, and with the first k-block of every four also the scales
+// of those four (16 bytes per row of A and of B); warp 1 issues the MMAs
+// (four 32-deep steps per k-block) into one 256-column TMEM accumulator;
+// warps 10-13 move each group's scales from shared to tensor memory
+// (tcgen05.st) into one of two buffers; warps 2-9 drain the accumulator and
+// write the outputs.  Every wait is bounded.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+constexpr int BM = 128, BK = 128, BN = 256, STAGES = 4;
+constexpr int A_BYTES = BM * BK;              // 16 KB of codes
+constexpr int B_BYTES = BN * BK;              // 32 KB
+constexpr int SFA_BYTES = BM * 16;            // scales of 4 k-blocks: 16 bytes per row
+constexpr int SFB_BYTES = BN * 16;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int EPI_WARPS = 8, SF_WARPS = 4;
+constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS);
+constexpr int SF_WARP0 = 2 + EPI_WARPS;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+// tensor-memory columns: accumulator 0-255; per scale buffer b (two), k-block j of
+// its group of four: A scales at 256 + 16b + 4j (+ m/32), B scales at 288 + 32b + 8j
+constexpr uint32_t SFA_COL = 256, SFB_COL = 288;
+
+enum Mode : int { GATEUP = 0, DOWN = 1 };
+
+struct alignas(8) Ctl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t sf_full[2];
+  uint64_t sf_empty[2];
+  uint64_t tfull, tempty, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Ctl) <= 256, "control block");
+
+struct MxArgs {
+  int E, N, d, f;
+  const int32_t* offsets;
+  const int2* tiles;           // 128-row tiles {first row, expert}
+  const int32_t* tile_count;
+  int n_tiles_n;               // 256-column output tiles (GATEUP: 128-column h tiles)
+  int kblocks;                 // 128-deep k-blocks
+  uint8_t* hq;                 // GATEUP: h codes [N, f] and scales [N, hs_stride]
+  uint8_t* hs;
+  int hs_stride;
+  uint16_t* out;               // DOWN: o [N, d]
+  const float* row_scale;      // DOWN: per-row output scale, or null
+  int* err;
+};
+
+__device__ __forceinline__ float silu_mx(float a) { return a / (1.f + expf(-a)); }
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmSA,
+                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+                       const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ CUtensorMap tmSB2,
+                       const __grid_constant__ MxArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t tile_base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* tile_ptr = smem_raw + (tile_base - raw_addr);
+  Ctl* ctl = reinterpret_cast<Ctl*>(tile_ptr + STAGES * STAGE_BYTES);
+  volatile int* abort_flag = &ctl->abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl->sf_full[b]), SF_WARPS);
+      mbar_init(smem_u32(&ctl->sf_empty[b]), 1);
+    }
+    mbar_init(smem_u32(&ctl->tfull), 1);
+    mbar_init(smem_u32(&ctl->tempty), EPI_WARPS);
+    mbar_init(smem_u32(&ctl->mma_done), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmSA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmSB);
+    if (MODE == GATEUP) {
+      tma_prefetch_desc(&tmB2);
+      tma_prefetch_desc(&tmSB2);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+  const int total = (*g.tile_count) * g.n_tiles_n;
+  const int nkb = g.kblocks;
+
+  auto decode = [&](int item, int& row0, int& e, int& row_end, int& nt) {
+    const int2 tl = g.tiles[item / g.n_tiles_n];
+    nt = item % g.n_tiles_n;
+    row0 = tl.x;
+    e = tl.y;
+    row_end = g.offsets[e + 1];
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it_count = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        int row0, e, row_end, nt;
+        decode(item, row0, e, row_end, nt);
+        const int brow = MODE == GATEUP ? e * g.f + nt * 128 : e * g.d + nt * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it_count) {
+          const int s = it_count % STAGES;
+          const uint32_t ph = (it_count / STAGES) & 1u;
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, g.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&ctl->full[s]);
+          const uint32_t sa = tile_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const uint32_t ssa = sb + B_BYTES;
+          const uint32_t ssb = ssa + SFA_BYTES;
+          const bool with_sf = (kb & 3) == 0;   // the scales of k-blocks kb .. kb+3
+          mbar_arrive_expect_tx(bar, A_BYTES + B_BYTES + (with_sf ? SFA_BYTES + SFB_BYTES : 0));
+          tma_load_2d(sa, &tmA, bar, kb * BK, row0);
+          if (MODE == GATEUP) {
+            tma_load_2d(sb, &tmB, bar, kb * BK, brow);
+            tma_load_2d(sb + B_BYTES / 2, &tmB2, bar, kb * BK, brow);
+          } else {
+            tma_load_2d(sb, &tmB, bar, kb * BK, brow);
+          }
+          if (with_sf) {
+            tma_load_2d(ssa, &tmSA, bar, (kb >> 2) * 16, row0);
+            if (MODE == GATEUP) {
+              tma_load_2d(ssb, &tmSB, bar, (kb >> 2) * 16, brow);
+              tma_load_2d(ssb + SFB_BYTES / 2, &tmSB2, bar, (kb >> 2) * 16, brow);
+            } else {
+              tma_load_2d(ssb, &tmSB, bar, (kb >> 2) * 16, brow);
+            }
+          }
+        }
+      }
+      if (!ok) {   // the loads still in flight land before the CTA exits
+        const uint32_t n = it_count < (uint32_t)STAGES ? it_count : (uint32_t)STAGES;
+        for (uint32_t q = 0; q < n; ++q) {
+          const uint32_t c = it_count - 1 - q;
+          volatile int never = 0;
+          mbar_wait_bounded(smem_u32(&ctl->full[c % STAGES]), (c / STAGES) & 1u, &never, nullptr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t it_count = 0, grp = 0;
+    bool ok = true, issued_any = false;
+    int j = 0;
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++j) {
+      ok = mbar_wait_bounded(smem_u32(&ctl->tempty), (j & 1u) ^ 1u, abort_flag, g.err);
+      ok = __all_sync(kFull, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t gcur = 0;
+      for (int kb = 0; kb < nkb; ++kb, ++it_count) {
+        const int s = it_count % STAGES;
+        const uint32_t ph = (it_count / STAGES) & 1u;
+        ok = mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, g.err);
+        if (ok && (kb & 3) == 0) {   // this group's scales are in tensor memory
+          gcur = grp++;
+          ok = mbar_wait_bounded(smem_u32(&ctl->sf_full[gcur & 1]), (gcur >> 1) & 1u, abort_flag,
+                                 g.err);
+        }
+        ok = __all_sync(kFull, ok);
+        if (!ok) break;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sa = tile_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const uint32_t buf = gcur & 1, jj = kb & 3;
+          const uint32_t sfa = tmem_base + SFA_COL + 16 * buf + 4 * jj;
+          const uint32_t sfb = tmem_base + SFB_COL + 32 * buf + 8 * jj;
+#pragma unroll
+          for (int ks = 0; ks < BK / 32; ++ks)
+            tc_mma_mxf8(tmem_base, smem_desc_sw128(sa + ks * 32, 16, 1024),
+                        smem_desc_sw128(sb + ks * 32, 16, 1024), idesc_mxf8(BM, BN, ks, ks), sfa,
+                        sfb, (kb > 0 || ks > 0) ? 1u : 0u);
+          issued_any = true;
+          tc_commit(smem_u32(&ctl->empty[s]));
+          if (jj == 3 || kb == nkb - 1) tc_commit(smem_u32(&ctl->sf_empty[buf]));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(smem_u32(&ctl->tfull));
+      __syncwarp();
+    }
+    if (lane == 0 && issued_any) {
+      tc_commit(smem_u32(&ctl->mma_done));
+      volatile int never = 0;
+      mbar_wait_bounded(smem_u32(&ctl->mma_done), 0, &never, nullptr);
+    }
+    __syncwarp();
+  } else if (warp >= SF_WARP0) {
+    // ------------------------------------------------------------ scales -> tensor memory
+    // This warp's lanes are TMEM lanes 32q .. 32q+31: A row m = 32q + lane, and
+    // (a copy of) the B scales that lane quadrant reads.
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+    uint32_t it_count = 0, grp = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      for (int kb0 = 0; kb0 < nkb; kb0 += 4, ++grp) {
+        const uint32_t c = it_count + kb0;
+        const int s = c % STAGES;
+        const uint32_t buf = grp & 1;
+        ok = mbar_wait_bounded(smem_u32(&ctl->full[s]), (c / STAGES) & 1u, abort_flag, g.err);
+        // the MMAs of the group that used this buffer two groups ago are done
+        ok = ok && mbar_wait_bounded(smem_u32(&ctl->sf_empty[buf]), ((grp >> 1) & 1u) ^ 1u,
+                                     abort_flag, g.err);
+        ok = __all_sync(kFull, ok);
+        if (!ok) break;
+        const uint8_t* ssa = tile_ptr + s * STAGE_BYTES + A_BYTES + B_BYTES;
+        const uint8_t* ssb = ssa + SFA_BYTES;
+        // A: row m's four k-blocks, each word copied to the four columns of its k-block
+        const uint4 wa = *reinterpret_cast<const uint4*>(ssa + m * 16);
+        const uint32_t av[4] = {wa.x, wa.y, wa.z, wa.w};
+        uint32_t r[16];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) r[jj * 4 + cc] = av[jj];
+        tmem_st16(lane_base + SFA_COL + 16 * buf, r);
+        // B: column 8 jj + t of k-block jj holds B row 32 t + lane
+        uint32_t bv[8][4];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const uint4 w = *reinterpret_cast<const uint4*>(ssb + (32 * t + lane) * 16);
+          bv[t][0] = w.x; bv[t][1] = w.y; bv[t][2] = w.z; bv[t][3] = w.w;
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+            for (int t = 0; t < 8; ++t) r[jj * 8 + t] = bv[t][half * 2 + jj];
+          tmem_st16(lane_base + SFB_COL + 32 * buf + 16 * half, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->sf_full[buf]));
+      }
+      it_count += nkb;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2-9)
+    const int q = warp & 3;                 // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;       // which half of the columns
+    int j = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
+      int row0, e, row_end, nt;
+      decode(item, row0, e, row_end, nt);
+      bool ok = mbar_wait_bounded(smem_u32(&ctl->tfull), j & 1u, abort_flag, g.err);
+      ok = __all_sync(kFull, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16);
+      const int row = row0 + q * 32 + lane;
+      const bool valid = row < row_end;
+      if (MODE == GATEUP) {
+        // 64 columns of h (two 32-element scale blocks): a at c, b at 128 + c
+        for (int blk = 0; blk < 2; ++blk) {
+          const int c = half * 64 + blk * 32;
+          float a[32], b[32];
+          tmem_ld16(t_row + c, a);
+          tmem_ld16(t_row + c + 16, a + 16);
+          tmem_ld16(t_row + 128 + c, b);
+          tmem_ld16(t_row + 128 + c + 16, b + 16);
+          tmem_ld_wait();
+          float amax = 0.f;
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            a[u] = silu_mx(a[u]) * b[u];
+            amax = fmaxf(amax, fabsf(a[u]));
+          }
+          const int k = mx_exponent(amax);
+          uint32_t w[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) w[u] = mx_codes4(a + 4 * u, k);
+          if (valid) {
+            const int col = nt * 128 + c;
+            uint4* dst = reinterpret_cast<uint4*>(g.hq + (size_t)row * g.f + col);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            g.hs[(size_t)row * g.hs_stride + col / 32] = (uint8_t)(k + 127);
+          }
+        }
+      } else {
+        const float sc = (valid && g.row_scale) ? g.row_scale[row] : 1.f;
+        for (int c = half * 128; c < half * 128 + 128; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_ld_wait();
+          const int col = nt * BN + c;
+          if (valid && col < g.d) {
+            if (g.row_scale) {
+#pragma unroll
+              for (int u = 0; u < 16; ++u) v[u] *= sc;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(g.out + (size_t)row * g.d + col);
+            dst[0] = pack8(v);
+            dst[1] = pack8(v + 8);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+constexpr int kU8 = (int)CU_TENSOR_MAP_DATA_TYPE_UINT8;
+
+int sms() {
+  static int n[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (n[dev] == 0) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
+  return n[dev] > 0 ? n[dev] : 148;
+}
+
+template <int MODE>
+cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& sa, const CUtensorMap& b,
+                      const CUtensorMap& b2, const CUtensorMap& sb, const CUtensorMap& sb2,
+                      const MxArgs& g, long long max_items, cudaStream_t s) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mx_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  if (max_items <= 0) return cudaSuccess;
+  const int grid = (int)(max_items < sms() ? max_items : sms());
+  grouped_gemm_mx_kernel<MODE><<<grid, THREADS, SMEM_BYTES, s>>>(a, sa, b, b2, sb, sb2, g);
+  count_launches(1);
+  return cudaGetLastError();
+}
+}  // namespace
+
+bool ffn_mx_supported(int d, int f) { return d % 128 == 0 && f % 128 == 0; }
+
+size_t ffn_mx_ws_bytes(int N, int d, int f, int E) {
+  (void)d;
+  return tiles_ws_bytes(N, E) + align_up((size_t)N * f, 256) +
+         align_up((size_t)N * mx_scale_row_bytes(f), 256);
+}
+
+cudaError_t launch_ffn_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets, int N,
+                          int d, int f, int E, const uint8_t* W1q, const uint8_t* W1s,
+                          const uint8_t* W3q, const uint8_t* W3s, const uint8_t* W2q,
+                          const uint8_t* W2s, const float* row_scale, uint8_t* hq, uint8_t* hs,
+                          uint16_t* out, void* ws, int* err, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* tws = w;
+  w += tiles_ws_bytes(N, E);
+  const int skd = mx_scale_row_bytes(d), skf = mx_scale_row_bytes(f);
+  if (!hq) hq = w;
+  w += align_up((size_t)N * f, 256);
+  if (!hs) hs = w;
+  trace_begin(MOE_STAGE_GATEUP, s);
+  cudaError_t e = launch_build_tiles(offsets, E, tws, s, BM, 0);
+  if (e != cudaSuccess) return e;
+  const TileLists tl = tile_lists(tws, E);
+  MxArgs g{};
+  g.E = E; g.N = N; g.d = d; g.f = f;
+  g.offsets = offsets;
+  g.tiles = tl.tiles;
+  g.tile_count = tl.count;
+  g.err = err;
+  g.hq = hq; g.hs = hs; g.hs_stride = skf;
+  g.out = out;
+  g.row_scale = row_scale;
+  const long long m_tiles = ceil_div(N, BM) + E;
+  CUtensorMap ma, msa, mb, mb2, msb, msb2;
+  // gate-up: A = x codes [N, d], B = W1 / W3 codes [E f, d] (128 rows each per tile)
+  if (!encode_map_2d(&ma, kU8, xq, d, N, d, BK, BM, true) ||
+      !encode_map_2d(&msa, kU8, xs, skd, N, skd, 16, BM, false) ||
+      !encode_map_2d(&mb, kU8, W1q, d, (unsigned long long)E * f, d, BK, 128, true) ||
+      !encode_map_2d(&mb2, kU8, W3q, d, (unsigned long long)E * f, d, BK, 128, true) ||
+      !encode_map_2d(&msb, kU8, W1s, skd, (unsigned long long)E * f, skd, 16, 128, false) ||
+      !encode_map_2d(&msb2, kU8, W3s, skd, (unsigned long long)E * f, skd, 16, 128, false))
+    return cudaErrorInvalidValue;
+  g.n_tiles_n = f / 128;
+  g.kblocks = d / BK;
+  e = launch_mx<GATEUP>(ma, msa, mb, mb2, msb, msb2, g, m_tiles * g.n_tiles_n, s);
+  trace_end(MOE_STAGE_GATEUP, s);
+  if (e != cudaSuccess) return e;
+  // down: A = h codes [N, f], B = W2 codes [E d, f] (256 rows per tile)
+  trace_begin(MOE_STAGE_DOWN, s);
+  if (!encode_map_2d(&ma, kU8, hq, f, N, f, BK, BM, true) ||
+      !encode_map_2d(&msa, kU8, hs, skf, N, skf, 16, BM, false) ||
+      !encode_map_2d(&mb, kU8, W2q, f, (unsigned long long)E * d, f, BK, BN, true) ||
+      !encode_map_2d(&msb, kU8, W2s, skf, (unsigned long long)E * d, skf, 16, BN, false))
+    return cudaErrorInvalidValue;
+  g.n_tiles_n = ceil_div(d, BN);
+  g.kblocks = f / BK;
+  e = launch_mx<DOWN>(ma, msa, mb, mb, msb, msb, g, m_tiles * g.n_tiles_n, s);
+  trace_end(MOE_STAGE_DOWN, s);
+  return e;
+}
+
+}  // namespace moe

@@ -75,6 +75,24 @@ cudaError_t launch_dispatch_fp8(const uint16_t* x, const int32_t* idx, int T, in
                                 cudaStream_t s);
 cudaError_t launch_dequant_fp8(const uint8_t* xq, const float* xs, long long N, int d,
                                uint16_t* out, cudaStream_t s);
+// Microscaled fp8 (E4M3 codes, one UE8M0 scale per 32 elements along K; scale
+// rows K/32 bytes rounded up to a multiple of 16).
+int mx_scale_row_bytes(int K);
+cudaError_t launch_quantize_mx(const uint16_t* x, long long rows, int K, uint8_t* xq,
+                               uint8_t* xs, cudaStream_t s);
+cudaError_t launch_dispatch_mx(const uint16_t* x, const int32_t* idx, int T, int d, int E, int R,
+                               int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                               int32_t* slot_row, uint8_t* xq, uint8_t* xs, void* ws, int* err,
+                               cudaStream_t s);
+// Grouped SwiGLU FFN on microscaled fp8 rows and weights (d % 128 == 0, f % 128 == 0):
+// h is quantised along f into hq / hs (or the workspace when null).
+bool ffn_mx_supported(int d, int f);
+size_t ffn_mx_ws_bytes(int N, int d, int f, int E);
+cudaError_t launch_ffn_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets, int N,
+                          int d, int f, int E, const uint8_t* W1q, const uint8_t* W1s,
+                          const uint8_t* W3q, const uint8_t* W3s, const uint8_t* W2q,
+                          const uint8_t* W2s, const float* row_scale, uint8_t* hq, uint8_t* hs,
+                          uint16_t* out, void* ws, int* err, cudaStream_t s);
 
 // y = bf16(add + sum_r w o); add (bf16 [T,d], the shared expert's output) may be null.
 cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const float* w, int T,
@@ -84,6 +102,23 @@ cudaError_t launch_combine(const uint16_t* o, const int32_t* slot_row, const flo
 cudaError_t launch_one_expert_offsets(int32_t* offsets, int T, cudaStream_t s);
 
 size_t tiles_ws_bytes(int N, int E);
+// The ragged tile lists in a tile workspace: {first row, expert} per tile_rows-row
+// tile (and, with tail_rows > 0, experts' last tiles of at most tail_rows rows
+// in a second list), their counts on the device.
+struct TileLists {
+  const int32_t* count;
+  const int2* tiles;
+  const int32_t* tail_count;
+  const int2* tails;
+};
+TileLists tile_lists(void* ws, int E);
+cudaError_t launch_build_tiles(const int32_t* offsets, int E, void* ws, cudaStream_t s,
+                               int tile_rows = 128, int tail_rows = 0);
+// A 2-D tensor map (CUtensorMap at `map`) of `outer` rows of `inner` elements of
+// CUtensorMapDataType `dtype`, rows `row_bytes` apart, box {box_inner, box_outer}.
+bool encode_map_2d(void* map, int dtype, const void* base, unsigned long long inner,
+                   unsigned long long outer, unsigned long long row_bytes, unsigned box_inner,
+                   unsigned box_outer, bool swizzle128);
 cudaError_t launch_ffn_fwd(const uint16_t* x_perm, const int32_t* offsets, int N, int d, int f,
                            int E, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                            uint16_t* a_save, uint16_t* b_save, uint16_t* h, uint16_t* out,

@@ -80,6 +80,13 @@ typedef void* moe_stream_t;  /* cudaStream_t */
                                        keeps (a backward treats the quantisation as the
                                        identity); needs d % 128 == 0 and a workspace queried
                                        with this flag */
+#define MOE_FP8_MX 0x40u            /* moe_layer_fwd: run the expert FFN on the fp8 tensor cores
+                                       in the microscaled fp8 format (moe_dispatch_mx, then
+                                       moe_grouped_ffn_mx on layer->mx's weights); saved->o gets
+                                       the expert outputs, saved->x_perm, h, a and b are not
+                                       written (may be NULL) and moe_layer_bwd does not apply;
+                                       needs d, f multiples of 128 and a workspace queried with
+                                       this flag */
 
 /* Stages of moe_layer_fwd / moe_layer_bwd, for moe_trace_events. */
 typedef enum {
@@ -248,6 +255,61 @@ moe_status_t moe_grouped_ffn_fp8(const uint8_t* xq_perm, const float* xscale_per
                                  unsigned flags, moe_stream_t stream);
 
 /*
+ * Microscaled fp8 ("MX") operands for expert GEMMs that take fp8 directly
+ * (section "Evaluation": the tokens travel as block-scaled fp8; here the
+ * tensor cores multiply the fp8 codes themselves).  A matrix [rows, K] becomes
+ * E4M3 codes uint8 [rows, K] and one UE8M0 scale byte per 32 consecutive
+ * elements of a row along K, stored in rows of sk = 16 * ceil(K / 512) bytes
+ * (K/32 bytes, padded to a multiple of 16), uint8 [rows, sk].  A block's scale
+ * is 2^k with k the smallest integer such that 448 * 2^k >= the block's
+ * largest magnitude (clamped to [-127, 127]; an all-zero block gets k = -127),
+ * stored as k + 127; codes are the E4M3 values nearest x / 2^k, ties to even
+ * (no code saturates).  value = E4M3(code) * 2^(scale - 127).
+ */
+
+/*
+ * moe_quantize_mx -- codes and scales of a bf16 matrix W [rows, K] along K (K a
+ * multiple of 32): codes uint8 [rows, K], scales uint8 [rows, sk].  Used once for
+ * the expert weights (W1, W3 as [E*f, d]; W2 as [E*d, f]) before
+ * moe_grouped_ffn_mx.  All pointers 16-byte aligned.  No workspace.
+ */
+moe_status_t moe_quantize_mx(const uint16_t* W, long long rows, int K, uint8_t* codes,
+                             uint8_t* scales, moe_stream_t stream);
+
+/*
+ * moe_dispatch_mx -- moe_dispatch whose rows are written in the microscaled
+ * fp8 format above (codes xq_perm uint8 [T*R, d], scales xscale_perm uint8
+ * [T*R, sk(d)]) instead of bf16: the same plan (counts, offsets, row_slot,
+ * slot_row), each token's row quantised once and copied to its R rows.
+ * d must be a multiple of 128.  Workspace as for moe_dispatch.
+ */
+moe_status_t moe_dispatch_mx(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int R,
+                             int32_t* counts, int32_t* offsets, int32_t* row_slot,
+                             int32_t* slot_row, uint8_t* xq_perm, uint8_t* xscale_perm, void* ws,
+                             size_t* ws_bytes, unsigned flags, moe_stream_t stream);
+
+/*
+ * moe_grouped_ffn_mx -- the grouped SwiGLU FFN with fp8 tensor-core GEMMs on
+ * microscaled operands (tcgen05 block-scaled fp8 multiply, fp32 accumulation).
+ * For every expert e and row i in [offsets[e], offsets[e+1]), with every
+ * operand taken at its dequantised value:
+ *   a = x_i W1[e]^T,  b = x_i W3[e]^T,  h_i = silu(a) * b           (fp32)
+ *   (hq_i, hs_i) = the microscaled fp8 form of h_i along f
+ *   out_i = bf16(s_i * (h~_i W2[e]^T))   h~ = dequantised h, s_i = row_scale[i] or 1
+ * xq, xs: the rows (moe_dispatch_mx); W1q/W1s, W3q/W3s: [E*f, d] codes and
+ * scales, W2q/W2s: [E*d, f] (moe_quantize_mx); hq uint8 [N, f] and hs uint8
+ * [N, sk(f)] receive h (or NULL: kept in the workspace); out bf16 [N, d].
+ * d and f must be multiples of 128 (else MOE_ERR_UNSUPPORTED).  Needs a
+ * workspace (error word, tile list, and h when hq/hs are NULL).
+ */
+moe_status_t moe_grouped_ffn_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets,
+                                int N, int d, int f, int E, const uint8_t* W1q,
+                                const uint8_t* W1s, const uint8_t* W3q, const uint8_t* W3s,
+                                const uint8_t* W2q, const uint8_t* W2s, const float* row_scale,
+                                uint8_t* hq, uint8_t* hs, uint16_t* out, void* ws,
+                                size_t* ws_bytes, unsigned flags, moe_stream_t stream);
+
+/*
  * moe_prepack_weights -- copy the expert weights into the tile layout the
  * forward grouped GEMMs stream (a performance layout for forward-only use, e.g.
  * inference; the page's grouped GEMMs take the weights as they are):
@@ -322,6 +384,18 @@ typedef struct {
   float* dW2;
 } moe_shared_t;
 
+/* The expert weights in the microscaled fp8 format (moe_quantize_mx along each
+ * matrix's K): W1q, W3q uint8 [E*f, d] with scales uint8 [E*f, sk(d)]; W2q
+ * uint8 [E*d, f] with scales uint8 [E*d, sk(f)]. */
+typedef struct {
+  const uint8_t* W1q;
+  const uint8_t* W1s;
+  const uint8_t* W3q;
+  const uint8_t* W3s;
+  const uint8_t* W2q;
+  const uint8_t* W2s;
+} moe_mx_weights_t;
+
 typedef struct {
   int T, d, E, R, f;
   const float* w_gate;  /* fp32 [d,E] */
@@ -330,6 +404,7 @@ typedef struct {
   const uint16_t* W3;   /* bf16 [E,f,d] */
   const uint16_t* W2;   /* bf16 [E,d,f] */
   const moe_shared_t* shared;   /* NULL: no shared expert */
+  const moe_mx_weights_t* mx;   /* microscaled fp8 expert weights for MOE_FP8_MX, or NULL */
 } moe_layer_t;
 
 /* Forward intermediates (caller-owned device buffers, written by the forward,

@@ -269,12 +269,18 @@ def e4m3_round(v):
 
 
 def e4m3_encode(vals):
-    """E4M3-representable float64 values -> their uint8 codes."""
+    """E4M3-representable float64 values -> their uint8 codes (-0 -> 0x80), by
+    lookup in the sorted table of the 254 finite code values."""
     table = e4m3_decode(np.arange(256, dtype=np.uint8))
-    lookup = {float(table[c]): c for c in range(256) if np.isfinite(table[c]) and c != 0x80}
-    flat = [lookup[float(x)] if x != 0 or not np.signbit(x) else 0x80
-            for x in np.asarray(vals, np.float64).ravel()]
-    return np.array(flat, dtype=np.uint8).reshape(np.shape(vals))
+    codes = np.array([c for c in range(256) if np.isfinite(table[c]) and c != 0x80], np.uint8)
+    order = np.argsort(table[codes], kind="stable")
+    tv, codes = table[codes][order], codes[order]
+    v = np.asarray(vals, dtype=np.float64).ravel()
+    pos = np.clip(np.searchsorted(tv, v), 0, len(tv) - 1)
+    assert np.array_equal(tv[pos], v), "value not representable in E4M3"
+    out = codes[pos]
+    out[(v == 0) & np.signbit(v)] = 0x80
+    return out.reshape(np.shape(vals))
 
 
 def quantize_fp8_blocks(x):
