@@ -51,9 +51,11 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 BURST_CLOCK_FRACTION = 0.95
 
 # the other workloads the default run times after the headline:
-# (name, overrides, flush L2 between steps)
-EXTRA_WORKLOADS = (("large", {}, False), ("large_hot", {}, False), ("mid", {}, False),
-                   ("dispatch", {"T": 8192}, True), ("dispatch", {"T": 65536}, True))
+# (name, overrides, flush L2 between steps, expert FFN in microscaled fp8)
+EXTRA_WORKLOADS = (("large", {}, False, False), ("large", {}, False, True),
+                   ("large_hot", {}, False, False), ("mid", {}, False, False),
+                   ("dispatch", {"T": 8192}, True, False), ("dispatch", {"T": 65536}, True, False))
+FP8_PER_BF16 = 2.0   # dense fp8 tensor rate per bf16 rate (nominal 4.5 / 2.25 PFLOP/s)
 
 # two token counts of the oracle sample per workload (full-step estimate: a
 # straight line through the two timings).  The smaller one already routes to
@@ -81,6 +83,9 @@ def parse(argv=None):
                    help="block-scaled fp8 dispatch (E4M3 + per-128 scales), bf16 combine: "
                         "dispatch workloads dequantise in identity experts; layer workloads "
                         "pass MOE_FP8_DISPATCH (the GEMMs read the dequantised rows)")
+    p.add_argument("--mx", action="store_true",
+                   help="forward-only layer workloads: the expert FFN on the fp8 tensor cores in "
+                        "microscaled fp8 (MOE_FP8_MX; weights quantised once before timing)")
     p.add_argument("--no-prepack", action="store_true",
                    help="forward-only workloads: stream the plain weight layout instead of the "
                         "tiles moe_prepack_weights writes once before timing")
@@ -184,7 +189,7 @@ def parse_clock_samples(lines):
 
 
 # ---------------------------------------------------------------- work model
-def stage_work(wl, fp8=False, shared_fs=0, active_experts=None):
+def stage_work(wl, fp8=False, shared_fs=0, active_experts=None, mx=False):
     """Algorithmic work of one launch of each traced stage.
 
     Returns {stage: {"kind": K, "flops": F, "bytes": B}}.  F counts the
@@ -193,9 +198,11 @@ def stage_work(wl, fp8=False, shared_fs=0, active_experts=None):
     grouped GEMM on the tensor cores), "tensor3" (the gate projection x W_g on
     the tensor cores as three bf16 products, W_g split into hi + mid + lo, so
     the pipe executes 3 F), "alu" (the FP32 FMA gate, d % 64 != 0), "hbm"
-    (data movement only) and "side" (the shared expert's GEMMs, overlapping
-    other stages).  ``active_experts``: experts with at least one row, whose
-    weights the forward and data-gradient GEMMs read (default: all E).
+    (data movement only), "side" (the shared expert's GEMMs, overlapping
+    other stages) and "tensor_fp8" (a grouped GEMM on microscaled fp8
+    operands, ``mx``: one byte per element plus a scale byte per 32).
+    ``active_experts``: experts with at least one row, whose weights the
+    forward and data-gradient GEMMs read (default: all E).
     """
     T, d, E, R, f = wl.T, wl.d, wl.E, wl.R, wl.f
     Ea = E if active_experts is None else active_experts
@@ -234,6 +241,14 @@ def stage_work(wl, fp8=False, shared_fs=0, active_experts=None):
             "bwd_dwg": k("hbm", 0, 2.0 * T * d + 8.0 * N + 4.0 * d * E),
             "bwd_dxc": k("hbm", 0, 2.0 * N * d + 2.0 * T * d + 8.0 * E * d),
         })
+    if f and mx:
+        q = 1.0 + 1.0 / 32                    # a code byte per element, a scale byte per 32
+        w.update({
+            "dispatch": k("hbm", 0, 2.0 * T * d + q * N * d + 12.0 * N),
+            "gateup": k("tensor_fp8", 4.0 * N * d * f, q * N * d + 2.0 * q * Ea * f * d
+                        + q * N * f),
+            "down": k("tensor_fp8", 2.0 * N * d * f, q * N * f + q * Ea * d * f + 2.0 * N * d),
+        })
     if f and shared_fs:
         # the shared expert on the side stream: reported, but its time overlaps
         # other stages, so it stays out of the GEMM summary and the dominant kernel
@@ -252,14 +267,16 @@ def stage_roofline(work, ms, tc_peak, pk, sm_mhz=None):
     s = ms / 1e3
     out = {"ms": round(ms, 4)}
     hbm = pk["hbm_gbs"] * 1e9
-    if kind in ("tensor", "tensor3", "side"):
+    if kind in ("tensor", "tensor3", "side", "tensor_fp8"):
         ex = 3.0 * fl if kind == "tensor3" else fl     # FLOPs the tensor pipe executes
+        rate = FP8_PER_BF16 if kind == "tensor_fp8" else 1.0
+        tc_peak = tc_peak * rate
         out["tflops"] = round(fl / s / 1e12, 1)
         if kind == "tensor3":
             out["tensor_tflops"] = round(ex / s / 1e12, 1)
-        out["frac_burst"] = round(ex / s / 1e12 / pk.get("bf16_tflops", tc_peak), 4)
+        out["frac_burst"] = round(ex / s / 1e12 / (rate * pk.get("bf16_tflops", tc_peak)), 4)
         out["frac_sustained"] = round(
-            ex / s / 1e12 / pk.get("bf16_tflops_sustained", tc_peak), 4)
+            ex / s / 1e12 / (rate * pk.get("bf16_tflops_sustained", tc_peak)), 4)
         if kind == "side":
             out["frac"] = round(ex / s / 1e12 / tc_peak, 4)
             return out
@@ -289,13 +306,17 @@ def dominant_roofline(stages, work, dom, tc_peak, regime, pk, pk_src, traffic, s
     st, w = stages[dom], work[dom]
     r = {"kernel": dom, "traffic": traffic,
          "algorithmic_bytes": w["bytes"] or None}
+    fp8 = w["kind"] == "tensor_fp8"
     if st["bound"] == "tensor":
         r.update(bound="tensor", unit="TFLOP/s",
-                 achieved=st.get("tensor_tflops", st["tflops"]), peak=tc_peak,
+                 achieved=st.get("tensor_tflops", st["tflops"]),
+                 peak=tc_peak * (FP8_PER_BF16 if fp8 else 1.0),
                  frac=st["frac"], frac_burst=st["frac_burst"],
                  frac_sustained=st["frac_sustained"],
-                 peak_source=f"{pk_src} bf16 {regime} (median SM clock "
-                             f"{'within' if regime == 'burst' else 'below'} 5% of max)")
+                 peak_source=(f"{pk_src} bf16 {regime} (median SM clock "
+                              f"{'within' if regime == 'burst' else 'below'} 5% of max)"
+                              + (", x2 for fp8 (derived: nominal dense fp8 / bf16 rate)"
+                                 if fp8 else "")))
     elif st["bound"] == "hbm":
         r.update(bound="hbm", unit="GB/s", achieved=st["gbs"], peak=pk["hbm_gbs"],
                  frac=st["frac"], peak_source=f"{pk_src} HBM copy")
@@ -358,13 +379,14 @@ def alu_peak_tflops(sm_mhz):
 class Opts:
     """What one measured workload runs with."""
 
-    def __init__(self, args, name=None, over=None, flush_l2=None, e2e=None):
+    def __init__(self, args, name=None, over=None, flush_l2=None, e2e=None, mx=None):
         self.name = name or args.workload
         self.over = overrides(args) if over is None else over
         self.flush_l2 = args.flush_l2 if flush_l2 is None else flush_l2
         self.e2e = (not args.no_e2e) if e2e is None else e2e
         self.steps, self.warmup = args.steps, args.warmup
         self.fp8 = args.fp8
+        self.mx = args.mx if mx is None else mx
         self.single_cta = args.single_cta
         self.no_prepack = args.no_prepack
         self.shared_expert = args.shared_expert
@@ -380,6 +402,7 @@ def run_ours(o, rank, world, device):
     wl = synth.workload(o.name, **o.over)
     identity = wl.f == 0
     stream = torch.cuda.current_stream()
+    mxw = None
 
     # ---- inputs, resident in HBM before timing
     if identity:
@@ -416,7 +439,15 @@ def run_ours(o, rank, world, device):
         gemm_flags = B.MOE_SINGLE_CTA_TILES if o.single_cta else 0
         fwd_flags = gemm_flags | (B.MOE_FP8_DISPATCH if o.fp8 else 0)
         weights_note = "plain [E, out, in]"
-        if (not train and not o.no_prepack and wl.d % 256 == 0 and wl.f % 128 == 0):
+        mxw = None
+        if o.mx and not train:
+            # inference in microscaled fp8: the weights are quantised once, outside the timing
+            mxw = B.MxWeights(inp["W1"], inp["W3"], inp["W2"])
+            torch.cuda.synchronize()
+            fwd_flags |= B.MOE_FP8_MX
+            weights_note = ("microscaled fp8 (E4M3 codes + a power-of-two scale per 32 along K; "
+                            "moe_quantize_mx once, before timing)")
+        elif (not train and not o.no_prepack and wl.d % 256 == 0 and wl.f % 128 == 0):
             # inference: the weights are laid out once (like loading a model), outside the timing
             packed = [torch.empty_like(inp[k]) for k in ("W1", "W3", "W2")]
             B.moe_prepack_weights(inp["W1"], inp["W3"], inp["W2"], *packed)
@@ -440,7 +471,7 @@ def run_ours(o, rank, world, device):
                 gemm_flags |= B.MOE_SHARED_SERIAL
                 fwd_flags |= B.MOE_SHARED_SERIAL
         layer = B.Layer(inp["w_gate"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], wl.R, wl.T,
-                        shared=shared)
+                        shared=shared, mx=mxw)
         saved = B.Saved(layer, device, train=train)
         x = inp["x"]
         y = torch.empty_like(x)
@@ -518,7 +549,8 @@ def run_ours(o, rank, world, device):
             stage_ms[name] = stage_ms.get(name, 0.0) + ms / o.steps
     pk, pk_src = load_peaks()
     tc_peak, regime = tensor_peak(pk, clk)
-    work = stage_work(wl, fp8=o.fp8, shared_fs=o.shared_expert, active_experts=active)
+    work = stage_work(wl, fp8=o.fp8, shared_fs=o.shared_expert, active_experts=active,
+                      mx=o.mx and not train)
     if identity:
         ran = ("dispatch", "combine")
     elif train:
@@ -537,30 +569,35 @@ def run_ours(o, rank, world, device):
     # stages' roofline times against the measured step
     step_fl = sum(3.0 * w["flops"] if w["kind"] == "tensor3" else w["flops"]
                   for n, w in work.items() if n in ran and w["kind"] != "side")
+    step_fp8 = any(w["kind"] == "tensor_fp8" for n, w in work.items() if n in ran)
     step_roof_ms = sum(stages[n]["roofline_ms"] for n in stages if "roofline_ms" in stages[n])
     summary = {"tensor_peak_regime": regime, "tensor_peak_tflops": tc_peak,
                "active_experts": active}
     if step_fl:
         step_tf = step_fl / (ms_step / 1e3) / 1e12
         summary["step_tflops"] = round(step_tf, 1)
-        roof["frac_step"] = round(step_tf / tc_peak, 4)
+        roof["frac_step"] = round(step_tf / tc_peak, 4)   # against the bf16 peak
+        if step_fp8:
+            roof["frac_step_note"] = "the step's FLOPs against the bf16 peak; its GEMMs run in fp8"
     summary["step_roofline_ms"] = round(step_roof_ms, 4)
     summary["step_frac_of_roofline"] = round(step_roof_ms / ms_step, 4)
     roof["step_frac_of_roofline"] = summary["step_frac_of_roofline"]
-    gemm = [n for n in stages if work[n]["kind"] == "tensor"]
+    gemm = [n for n in stages if work[n]["kind"] in ("tensor", "tensor_fp8")]
     gemm_ms = sum(stages[n]["ms"] for n in gemm)
     if gemm_ms > 0:
         fl = sum(work[n]["flops"] for n in gemm)
         tf = fl / (gemm_ms / 1e3) / 1e12
+        rate = FP8_PER_BF16 if step_fp8 else 1.0
         summary["grouped_gemm_tflops"] = round(tf, 1)
-        summary["grouped_gemm_frac_burst"] = round(tf / pk.get("bf16_tflops", tc_peak), 4)
+        summary["grouped_gemm_dtype"] = "fp8 (microscaled)" if step_fp8 else "bf16"
+        summary["grouped_gemm_frac_burst"] = round(tf / (rate * pk.get("bf16_tflops", tc_peak)), 4)
         summary["grouped_gemm_frac_sustained"] = round(
-            tf / pk.get("bf16_tflops_sustained", tc_peak), 4)
+            tf / (rate * pk.get("bf16_tflops_sustained", tc_peak)), 4)
         summary["grouped_gemm_frac_of_roofline"] = round(
             sum(stages[n]["roofline_ms"] for n in gemm) / gemm_ms, 4)
         summary["grouped_gemm_bound"] = (
             "hbm" if sum(work[n]["bytes"] for n in gemm) / (pk["hbm_gbs"] * 1e9)
-            > fl / (tc_peak * 1e12) else "tensor")
+            > fl / (rate * tc_peak * 1e12) else "tensor")
     for n in ("dispatch", "combine"):
         if n in stages:
             summary[f"{n}_gbs"] = stages[n]["gbs"]
@@ -641,7 +678,7 @@ def run_ours(o, rank, world, device):
                          "overlapping the layer's compute"}
 
     config = {"workload": synth.describe(wl) + (" fwd+bwd" if train else " fwd")
-              + (" fp8-dispatch" if o.fp8 else ""),
+              + (" fp8-dispatch" if o.fp8 else "") + (" mx-fp8" if mxw is not None else ""),
               "parallelism": f"replicas x{world} (no cross-GPU exchange)",
               "global_batch_tokens": wl.T * world,
               "l2": ("512 MB written between steps (flushes L2; outside the stage events, "
@@ -830,7 +867,7 @@ def want_extras(args):
         return True
     if args.extra_workloads == "off":
         return False
-    return (args.workload == "train" and not overrides(args) and not args.fp8
+    return (args.workload == "train" and not overrides(args) and not args.fp8 and not args.mx
             and not args.single_cta and not args.shared_expert and not args.flush_l2)
 
 
@@ -906,8 +943,8 @@ def main():
     torch.cuda.empty_cache()
     if want_extras(args):
         extras = []
-        for name, over, flush in EXTRA_WORKLOADS:
-            r, _ = run_ours(Opts(args, name, over, flush, e2e=False), rank, world, device)
+        for name, over, flush, mx in EXTRA_WORKLOADS:
+            r, _ = run_ours(Opts(args, name, over, flush, e2e=False, mx=mx), rank, world, device)
             extras.append({"workload": r["config"]["workload"], "value": r["value"],
                            "unit": "tokens/s", "ms_per_step": r["ms_per_step"],
                            "l2": r["config"]["l2"], "weights": r["config"]["weights"],

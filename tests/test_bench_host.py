@@ -141,10 +141,29 @@ def test_extra_workloads_only_with_the_default_headline():
     assert not bench.want_extras(bench.parse(["--tokens", "4096"]))
     assert not bench.want_extras(bench.parse(["--extra-workloads", "off"]))
     assert bench.want_extras(bench.parse(["--workload", "mid", "--extra-workloads", "on"]))
-    names = [n for n, _, _ in bench.EXTRA_WORKLOADS]
-    assert names == ["large", "large_hot", "mid", "dispatch", "dispatch"]
-    assert [o.get("T") for n, o, fl in bench.EXTRA_WORKLOADS if n == "dispatch"] == [8192, 65536]
-    assert all(fl for n, _, fl in bench.EXTRA_WORKLOADS if n == "dispatch")
+    names = [(n, mx) for n, _, _, mx in bench.EXTRA_WORKLOADS]
+    assert names == [("large", False), ("large", True), ("large_hot", False), ("mid", False),
+                     ("dispatch", False), ("dispatch", False)]
+    assert [o.get("T") for n, o, fl, _ in bench.EXTRA_WORKLOADS if n == "dispatch"] == [8192, 65536]
+    assert all(fl for n, _, fl, _ in bench.EXTRA_WORKLOADS if n == "dispatch")
+    assert not bench.want_extras(bench.parse(["--mx"]))
+
+
+def test_microscaled_fp8_gemm_stages_count_bytes_and_the_fp8_peak():
+    wl = synth.workload("large")
+    T, d, E, R, f = wl.T, wl.d, wl.E, wl.R, wl.f
+    N = T * R
+    w = bench.stage_work(wl, mx=True)
+    q = 1 + 1 / 32
+    assert w["gateup"]["kind"] == "tensor_fp8" and w["gateup"]["flops"] == 4.0 * N * d * f
+    # codes and scales of x, W1, W3 and h: half the bf16 weight bytes and a little
+    assert w["gateup"]["bytes"] == q * N * d + 2 * q * E * f * d + q * N * f
+    assert w["down"]["bytes"] == q * N * f + q * E * d * f + 2.0 * N * d
+    st = bench.stage_roofline(w["gateup"], 2.0, 1900.0, PK)
+    assert st["frac_burst"] == pytest.approx(w["gateup"]["flops"] / 2e-3 / 3.8e15, abs=1e-4)
+    assert st["bound"] == "hbm"           # 12.3 GB at 6.8 TB/s outlast 3.85 TFLOP at 3.8 PF
+    roof = bench.dominant_roofline({"gateup": st}, w, "gateup", 1900.0, "burst", PK, "m", None)
+    assert roof["bound"] == "hbm"
 
 
 def test_profiled_traffic_goes_stale_with_the_sources(monkeypatch, tmp_path):
