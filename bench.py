@@ -99,8 +99,8 @@ def parse(argv=None):
                    help="run the shared expert on the caller's stream after the routed path "
                         "(MOE_SHARED_SERIAL), for comparison")
     p.add_argument("--flush-l2", action="store_true",
-                   help="write a 512 MB buffer (4x L2) between timed steps, outside the stage "
-                        "events, so small workloads read HBM; ms_per_step then includes it")
+                   help="write a 512 MB buffer (4x L2) between timed steps, so small workloads "
+                        "read HBM; each step is then timed by its own events, the flush outside them")
     p.add_argument("--extra-workloads", default="auto", choices=["auto", "on", "off"],
                    help="also time large, large_hot, mid and dispatch + combine (auto: only "
                         "with the default headline workload)")
@@ -524,19 +524,27 @@ def run_ours(o, rank, world, device):
     t1 = torch.cuda.Event(enable_timing=True)
     flush = (torch.empty(512 << 20, dtype=torch.uint8, device=device) if o.flush_l2
              else None)
+    # with an L2 flush between steps, each step is timed on its own (the flush
+    # between two steps' events is not part of either)
+    marks = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(o.steps)] if flush is not None else None)
     t0.record(stream)
     for k in range(o.steps):
         if flush is not None:
             flush.fill_(k & 0xff)
+            marks[k][0].record(stream)
         traces[k].arm()
         step()
+        if flush is not None:
+            marks[k][1].record(stream)
     B.StageTrace.disarm()
     t1.record(stream)
     torch.cuda.synchronize()
     launches = B.kernel_launches() - launches0
     clk = clocks.stop()
     world_barrier(world)
-    ms_total = t0.elapsed_time(t1)
+    ms_total = (t0.elapsed_time(t1) if flush is None
+                else sum(a.elapsed_time(b) for a, b in marks))
     ms_total = world_max(ms_total, world, device)
     ms_step = ms_total / o.steps
     tokens_per_step = wl.T
@@ -681,8 +689,8 @@ def run_ours(o, rank, world, device):
               + (" fp8-dispatch" if o.fp8 else "") + (" mx-fp8" if mxw is not None else ""),
               "parallelism": f"replicas x{world} (no cross-GPU exchange)",
               "global_batch_tokens": wl.T * world,
-              "l2": ("512 MB written between steps (flushes L2; outside the stage events, "
-                     "inside ms_per_step)" if o.flush_l2 else
+              "l2": ("512 MB written between steps (flushes L2); each step timed by its own "
+                     "events, the flush outside them" if o.flush_l2 else
                      "inputs larger than L2 every step (no flush)"),
               "weights": weights_note,
               "gemm_tiles": None if identity else
