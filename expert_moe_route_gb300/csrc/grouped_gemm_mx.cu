@@ -12,12 +12,12 @@
 // One CTA per SM, 128-row tiles of an expert's rows (ragged, from the tile
 // list), 256 output columns (GATEUP: 128 of W1 and the same 128 of W3).  Roles
 // (448 threads): warp 0 issues TMA loads of 128-deep k-blocks (A 16 KB, B 32 KB)
-// into four stages, and with the first k-block of every four also the scales
-// of those four (16 bytes per row of A and of B); warp 1 issues the MMAs
-// (four 32-deep steps per k-block) into one 256-column TMEM accumulator;
-// warps 10-13 move each group's scales from shared to tensor memory
-// (tcgen05.st) into one of two buffers; warps 2-9 drain the accumulator and
-// write the outputs.  Every wait is bounded.
+// into four stages, and two groups ahead the scales of each group of four
+// k-blocks (16 bytes per row of A and of B) into a ring of three slots; warp 1
+// issues the MMAs (four 32-deep steps per k-block) into one 256-column TMEM
+// accumulator; warps 10-13 move each group's scales from shared to tensor
+// memory (tcgen05.st) into one of three buffers; warps 2-9 drain the
+// accumulator and write the outputs.  Every wait is bounded.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -29,25 +29,33 @@ namespace {
 constexpr int BM = 128, BK = 128, BN = 256, STAGES = 4;
 constexpr int A_BYTES = BM * BK;              // 16 KB of codes
 constexpr int B_BYTES = BN * BK;              // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SFA_BYTES = BM * 16;            // scales of 4 k-blocks: 16 bytes per row
 constexpr int SFB_BYTES = BN * 16;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
 constexpr int EPI_WARPS = 8, SF_WARPS = 4;
 constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS);
 constexpr int SF_WARP0 = 2 + EPI_WARPS;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
-// tensor-memory columns: accumulator 0-255; per scale buffer b (two), k-block j of
-// its group of four: A scales at 256 + 16b + 4j (+ m/32), B scales at 288 + 32b + 8j
-constexpr uint32_t SFA_COL = 256, SFB_COL = 288;
+// Scale groups: three slots in shared memory and three buffers in tensor memory,
+// so that the scales of a group are loaded two groups ahead of its operands and
+// written while the MMAs of the two groups before it run.
+constexpr uint32_t NBUF = 3;
+// tensor-memory columns: accumulator 0-255; per scale buffer b, k-block j of its
+// group of four: A scales at 256 + 16b + 4j (+ m/32), B scales at 304 + 32b + 8j
+constexpr uint32_t SFA_COL = 256, SFB_COL = 256 + 16 * NBUF;
+static_assert(SFB_COL + 32 * NBUF <= TMEM_COLS, "tensor memory");
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (int)NBUF * SF_BYTES + 256 + 1024;
 
 enum Mode : int { GATEUP = 0, DOWN = 1 };
 
 struct alignas(8) Ctl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t sf_full[2];
-  uint64_t sf_empty[2];
+  uint64_t sfs_full[NBUF];    // a group's scales landed in its shared-memory slot
+  uint64_t sfs_free[NBUF];    // the scale warps have read the slot
+  uint64_t sf_full[NBUF];     // the group's scales are in tensor memory
+  uint64_t sf_empty[NBUF];    // the MMAs that read a tensor-memory scale buffer are done
   uint64_t tfull, tempty, mma_done;
   uint32_t tmem_base;
   int abort;
@@ -81,7 +89,8 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tile_base = (raw_addr + 1023u) & ~1023u;
   uint8_t* tile_ptr = smem_raw + (tile_base - raw_addr);
-  Ctl* ctl = reinterpret_cast<Ctl*>(tile_ptr + STAGES * STAGE_BYTES);
+  const uint32_t sf_base = tile_base + STAGES * STAGE_BYTES;   // the scale slots
+  Ctl* ctl = reinterpret_cast<Ctl*>(tile_ptr + STAGES * STAGE_BYTES + NBUF * SF_BYTES);
   volatile int* abort_flag = &ctl->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -91,7 +100,9 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < (int)NBUF; ++b) {
+      mbar_init(smem_u32(&ctl->sfs_full[b]), 1);
+      mbar_init(smem_u32(&ctl->sfs_free[b]), SF_WARPS);
       mbar_init(smem_u32(&ctl->sf_full[b]), SF_WARPS);
       mbar_init(smem_u32(&ctl->sf_empty[b]), 1);
     }
@@ -127,17 +138,53 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     e = tl.y;
     row_end = g.offsets[e + 1];
   };
+  // B rows of a tile: GATEUP W1 (and W3) rows nt*128..; DOWN W2 rows nt*256..
+  auto b_row = [&](int e, int nt) { return MODE == GATEUP ? e * g.f + nt * 128 : e * g.d + nt * BN; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it_count = 0;
+      // scale group G (four k-blocks) is item blockIdx.x + (G / gpi) * gridDim.x,
+      // k-blocks 4 (G % gpi) ..; groups are loaded kAhead ahead of the operands
+      const int gpi = (nkb + 3) / 4;
+      uint32_t g_sf = 0, g_op = 0;
+      constexpr uint32_t kAhead = 2;
       bool ok = true;
+      auto load_scales = [&](uint32_t G) -> bool {
+        const int item = blockIdx.x + (int)(G / gpi) * gridDim.x;
+        if (item >= total) return true;
+        const uint32_t b = G % NBUF;
+        if (!mbar_wait_bounded(smem_u32(&ctl->sfs_free[b]), ((G / NBUF) & 1u) ^ 1u, abort_flag,
+                               g.err))
+          return false;
+        int row0, e, row_end, nt;
+        decode(item, row0, e, row_end, nt);
+        const int brow = b_row(e, nt);
+        const int x = (int)(G % gpi) * 16;   // bytes 16 (G % gpi) .. of each scale row
+        const uint32_t lb = smem_u32(&ctl->sfs_full[b]);
+        const uint32_t ssa = sf_base + b * SF_BYTES;
+        const uint32_t ssb = ssa + SFA_BYTES;
+        mbar_arrive_expect_tx(lb, SF_BYTES);
+        tma_load_2d(ssa, &tmSA, lb, x, row0);
+        if (MODE == GATEUP) {
+          tma_load_2d(ssb, &tmSB, lb, x, brow);
+          tma_load_2d(ssb + SFB_BYTES / 2, &tmSB2, lb, x, brow);
+        } else {
+          tma_load_2d(ssb, &tmSB, lb, x, brow);
+        }
+        return true;
+      };
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         int row0, e, row_end, nt;
         decode(item, row0, e, row_end, nt);
-        const int brow = MODE == GATEUP ? e * g.f + nt * 128 : e * g.d + nt * BN;
+        const int brow = b_row(e, nt);
         for (int kb = 0; kb < nkb; ++kb, ++it_count) {
+          if ((kb & 3) == 0) {
+            for (; ok && g_sf <= g_op + kAhead; ++g_sf) ok = load_scales(g_sf);
+            ++g_op;
+            if (!ok) break;
+          }
           const int s = it_count % STAGES;
           const uint32_t ph = (it_count / STAGES) & 1u;
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, g.err)) {
@@ -147,25 +194,13 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
           const uint32_t bar = smem_u32(&ctl->full[s]);
           const uint32_t sa = tile_base + s * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          const uint32_t ssa = sb + B_BYTES;
-          const uint32_t ssb = ssa + SFA_BYTES;
-          const bool with_sf = (kb & 3) == 0;   // the scales of k-blocks kb .. kb+3
-          mbar_arrive_expect_tx(bar, A_BYTES + B_BYTES + (with_sf ? SFA_BYTES + SFB_BYTES : 0));
+          mbar_arrive_expect_tx(bar, STAGE_BYTES);
           tma_load_2d(sa, &tmA, bar, kb * BK, row0);
           if (MODE == GATEUP) {
             tma_load_2d(sb, &tmB, bar, kb * BK, brow);
             tma_load_2d(sb + B_BYTES / 2, &tmB2, bar, kb * BK, brow);
           } else {
             tma_load_2d(sb, &tmB, bar, kb * BK, brow);
-          }
-          if (with_sf) {
-            tma_load_2d(ssa, &tmSA, bar, (kb >> 2) * 16, row0);
-            if (MODE == GATEUP) {
-              tma_load_2d(ssb, &tmSB, bar, (kb >> 2) * 16, brow);
-              tma_load_2d(ssb + SFB_BYTES / 2, &tmSB2, bar, (kb >> 2) * 16, brow);
-            } else {
-              tma_load_2d(ssb, &tmSB, bar, (kb >> 2) * 16, brow);
-            }
           }
         }
       }
@@ -175,6 +210,11 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
           const uint32_t c = it_count - 1 - q;
           volatile int never = 0;
           mbar_wait_bounded(smem_u32(&ctl->full[c % STAGES]), (c / STAGES) & 1u, &never, nullptr);
+        }
+        for (uint32_t G = g_sf > NBUF ? g_sf - NBUF : 0; G < g_sf; ++G) {
+          volatile int never = 0;
+          mbar_wait_bounded(smem_u32(&ctl->sfs_full[G % NBUF]), (G / NBUF) & 1u, &never, nullptr,
+                            200000ull);
         }
       }
     }
@@ -195,8 +235,8 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         ok = mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, g.err);
         if (ok && (kb & 3) == 0) {   // this group's scales are in tensor memory
           gcur = grp++;
-          ok = mbar_wait_bounded(smem_u32(&ctl->sf_full[gcur & 1]), (gcur >> 1) & 1u, abort_flag,
-                                 g.err);
+          ok = mbar_wait_bounded(smem_u32(&ctl->sf_full[gcur % NBUF]), (gcur / NBUF) & 1u,
+                                 abort_flag, g.err);
         }
         ok = __all_sync(kFull, ok);
         if (!ok) break;
@@ -204,7 +244,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
           tc_fence_after();
           const uint32_t sa = tile_base + s * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          const uint32_t buf = gcur & 1, jj = kb & 3;
+          const uint32_t buf = gcur % NBUF, jj = kb & 3;
           const uint32_t sfa = tmem_base + SFA_COL + 16 * buf + 4 * jj;
           const uint32_t sfb = tmem_base + SFB_COL + 32 * buf + 8 * jj;
 #pragma unroll
@@ -235,20 +275,20 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
-    uint32_t it_count = 0, grp = 0;
+    uint32_t grp = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       for (int kb0 = 0; kb0 < nkb; kb0 += 4, ++grp) {
-        const uint32_t c = it_count + kb0;
-        const int s = c % STAGES;
-        const uint32_t buf = grp & 1;
-        ok = mbar_wait_bounded(smem_u32(&ctl->full[s]), (c / STAGES) & 1u, abort_flag, g.err);
-        // the MMAs of the group that used this buffer two groups ago are done
-        ok = ok && mbar_wait_bounded(smem_u32(&ctl->sf_empty[buf]), ((grp >> 1) & 1u) ^ 1u,
+        const uint32_t buf = grp % NBUF;
+        // the group's scales landed in their slot, and the MMAs of the group that
+        // used this tensor-memory buffer NBUF groups ago are done
+        ok = mbar_wait_bounded(smem_u32(&ctl->sfs_full[buf]), (grp / NBUF) & 1u, abort_flag,
+                               g.err);
+        ok = ok && mbar_wait_bounded(smem_u32(&ctl->sf_empty[buf]), ((grp / NBUF) & 1u) ^ 1u,
                                      abort_flag, g.err);
         ok = __all_sync(kFull, ok);
         if (!ok) break;
-        const uint8_t* ssa = tile_ptr + s * STAGE_BYTES + A_BYTES + B_BYTES;
+        const uint8_t* ssa = tile_ptr + STAGES * STAGE_BYTES + buf * SF_BYTES;
         const uint8_t* ssb = ssa + SFA_BYTES;
         // A: row m's four k-blocks, each word copied to the four columns of its k-block
         const uint4 wa = *reinterpret_cast<const uint4*>(ssa + m * 16);
@@ -277,9 +317,11 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->sf_full[buf]));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&ctl->sfs_free[buf]));   // the slot may be reloaded
+          mbar_arrive(smem_u32(&ctl->sf_full[buf]));
+        }
       }
-      it_count += nkb;
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2-9)
@@ -296,9 +338,10 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16);
       const int row = row0 + q * 32 + lane;
       const bool valid = row < row_end;
+      const bool any = row0 + q * 32 < row_end;   // warp-uniform: rows of the expert here
       if (MODE == GATEUP) {
         // 64 columns of h (two 32-element scale blocks): a at c, b at 128 + c
-        for (int blk = 0; blk < 2; ++blk) {
+        for (int blk = 0; blk < 2 && any; ++blk) {
           const int c = half * 64 + blk * 32;
           float a[32], b[32];
           tmem_ld16(t_row + c, a);
@@ -326,7 +369,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         }
       } else {
         const float sc = (valid && g.row_scale) ? g.row_scale[row] : 1.f;
-        for (int c = half * 128; c < half * 128 + 128; c += 16) {
+        for (int c = half * 128; c < half * 128 + 128 && any; c += 16) {
           float v[16];
           tmem_ld16(t_row + c, v);
           tmem_ld_wait();

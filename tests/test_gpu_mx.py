@@ -71,7 +71,7 @@ def test_dispatch_mx_bit_exact(lib):
     assert np.array_equal(xs.cpu().numpy()[:, : d // 32], qs[tok])
 
 
-def _ffn_mx_case(B, counts, d, f, seed, row_scale=False, check_weights=True):
+def _ffn_mx_case(B, counts, d, f, seed, row_scale=False, check_weights=True, flags=0):
     E = len(counts)
     offsets = np.zeros(E + 1, dtype=np.int32)
     offsets[1:] = np.cumsum(counts)
@@ -89,7 +89,7 @@ def _ffn_mx_case(B, counts, d, f, seed, row_scale=False, check_weights=True):
         rs = torch.rand(N, generator=torch.Generator().manual_seed(seed + 4)).cuda() + 0.25
     ws = B.workspace(B.grouped_ffn_mx_ws_bytes(N, d, f, E))
     B.moe_grouped_ffn_mx(xq, xs, torch.from_numpy(offsets).cuda(), *q1, *q3, *q2, out, ws,
-                         hq=hq, hs=hs, row_scale=rs, flags=B.MOE_CHECK)
+                         hq=hq, hs=hs, row_scale=rs, flags=flags | B.MOE_CHECK)
     torch.cuda.synchronize()
     # the weights' codes and scales are the oracle's, bit for bit
     for (c, s), w in zip((q1, q3, q2) if check_weights else (), (W1, W3, W2)):
@@ -110,7 +110,7 @@ def _ffn_mx_case(B, counts, d, f, seed, row_scale=False, check_weights=True):
     same = np.mean(npc(hq) == rq)
     assert same > 0.99, f"only {same:.4%} of h codes agree"
     assert_close(f64(out), o, "o")
-    return out
+    return out, hq, hs
 
 
 @pytest.mark.parametrize("counts,d,f", [
@@ -125,8 +125,8 @@ def test_grouped_ffn_mx_matches_oracle(lib, counts, d, f):
 
 
 def test_grouped_ffn_mx_row_scale_and_repeatability(lib):
-    o1 = _ffn_mx_case(lib, [70, 0, 250, 5], 512, 256, seed=9, row_scale=True)
-    o2 = _ffn_mx_case(lib, [70, 0, 250, 5], 512, 256, seed=9, row_scale=True)
+    o1 = _ffn_mx_case(lib, [70, 0, 250, 5], 512, 256, seed=9, row_scale=True)[0]
+    o2 = _ffn_mx_case(lib, [70, 0, 250, 5], 512, 256, seed=9, row_scale=True)[0]
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
 
 
