@@ -674,9 +674,8 @@ static size_t layer_bwd_ws(const moe_layer_t* L) {
   n += align_up(N * 2 * f * 2, 256);    // [da | db]
   n += align_up(N * d * 2, 256);        // dx_perm
   n += align_up(N * 4, 256);            // dlogits per slot (token order)
-  n += align_up(N * 4, 256);            // dlogits per row
   n += align_up(E * d * 4, 256);        // W_g^T
-  n += dwg_ws_bytes((int)d, (int)E);    // router weight-gradient partials
+  n += dwg_ws_bytes((int)T, (int)d, (int)E);   // router weight gradient: S, partials, maps
   if (L->shared) {                      // shared expert: offsets, tiles, [das | dbs], dxs
     const size_t fs = L->shared->fs;
     n += 256 + tiles_ws_bytes((int)T, 1) + align_up(T * 2 * fs * 2, 256) + align_up(T * d * 2, 256);
@@ -742,9 +741,8 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
   uint16_t* dab = static_cast<uint16_t*>(c.take((size_t)N * 2 * f * 2));
   uint16_t* dxp = static_cast<uint16_t*>(c.take((size_t)N * d * 2));
   float* dsel_tok = static_cast<float*>(c.take((size_t)N * 4));
-  float* dsel_row = static_cast<float*>(c.take((size_t)N * 4));
   float* wgT = static_cast<float*>(c.take((size_t)E * d * 4));
-  void* dwg_ws = c.take(dwg_ws_bytes(d, E));
+  void* dwg_ws = c.take(dwg_ws_bytes(T, d, E));
   int32_t* s_off = nullptr;
   void* s_tws = nullptr;
   uint16_t *s_dab = nullptr, *s_dx = nullptr;
@@ -779,14 +777,13 @@ moe_status_t moe_layer_bwd(const moe_layer_t* L, const uint16_t* x, const moe_sa
   }
   {
     Stage st_(s, MOE_STAGE_BWD_ROUTE);
-    MOE_TRY(launch_bwd_route(dy, sv->o, sv->slot_row, sv->topk_w, T, d, R, dO, dsel_tok, dsel_row,
-                             s));
+    MOE_TRY(launch_bwd_route(dy, sv->o, sv->slot_row, sv->topk_w, T, d, R, dO, dsel_tok, s));
   }
   MOE_TRY(launch_ffn_bwd(sv->x_perm, sv->offsets, N, d, f, E, L->W1, L->W3, L->W2, sv->a, sv->b,
                          sv->h, dO, dab, dxp, dW1, dW3, dW2, tws, err, pairs, s));
   {
     Stage st_(s, MOE_STAGE_BWD_DWG);
-    MOE_TRY(launch_dwg(x, sv->row_slot, R, sv->offsets, dsel_row, d, E, dW_gate, dwg_ws, s));
+    MOE_TRY(launch_dwg(x, sv->topk_idx, dsel_tok, T, d, E, R, dW_gate, dwg_ws, err, pairs, s));
   }
   if (SH && !side) MOE_TRY(shared_bwd());
   if (side) MOE_TRY(join.now());

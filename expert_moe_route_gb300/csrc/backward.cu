@@ -3,9 +3,11 @@
 // gate weights the softmax over the chosen logits:
 //   dw_r = <dy_t, o_row>,  do_row = bf16(w_r dy_t)
 //   dlogits at the chosen experts: w_q (dw_q - sum_r w_r dw_r); zero elsewhere
-//   dW_g = x^T dlogits  -> for expert e: sum over its rows of dlogits_row x_perm[row]
+//   dW_g = x^T dlogits  (one dense contraction over the tokens, on the tensor cores)
 //   dx_t = bf16( sum_r dx_perm[row(t,r)] + sum_r dlogits_{t,r} W_g[:, idx[t,r]] )
 // All reductions run in a fixed order, so results are bitwise reproducible.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -19,7 +21,7 @@ constexpr int BW = 8;  // warps per block
 __global__ void __launch_bounds__(BW * 32) bwd_route_kernel(
     const uint16_t* __restrict__ dy, const uint16_t* __restrict__ o,
     const int32_t* __restrict__ slot_row, const float* __restrict__ w, int T, int d, int R, int N,
-    uint16_t* __restrict__ dO, float* __restrict__ dsel_tok, float* __restrict__ dsel_row) {
+    uint16_t* __restrict__ dO, float* __restrict__ dsel_tok) {
   __shared__ int rows_s[BW][32];
   __shared__ float w_s[BW][32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -86,10 +88,60 @@ __global__ void __launch_bounds__(BW * 32) bwd_route_kernel(
     if (lane < R) {
       const float ds = w_s[wid][lane] * (mine - wdw);
       dsel_tok[(size_t)t * R + lane] = ds;
-      const int row = rows_s[wid][lane];
-      if (row >= 0) dsel_row[row] = ds;
     }
     __syncwarp();
+  }
+}
+
+// Router weight gradient on the tensor cores.  dW_g = x^T dlogits is one dense
+// contraction over the T tokens (dlogits [T, E] is zero off each token's chosen
+// experts).  dlogits is split into two bf16 terms, hi = bf16(v) and
+// lo = bf16(v - hi) (v - hi is exact in fp32, so hi + lo carries 16 significant
+// bits of v), laid out side by side as S = [hi | lo] [T, 2 Ep], Ep = E rounded up
+// to 32.  One bf16 GEMM with fp32 accumulation, x^T S over chunks of the tokens,
+// gives both products for every chunk (P[s] [d, 2 Ep]); a last pass adds each
+// chunk's hi and lo columns, chunks in order.
+//
+// Operand pass: warp per token writes the token's row of S (zeros, then, after
+// the warp's zero stores, its R hi and lo values); block 0 also writes the chunk
+// offsets {0, c, 2c, ..., T}.
+__global__ void __launch_bounds__(BW * 32) dwg_operand_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ dsel, int T, int E, int R, int Ep,
+    int chunk, int S, uint16_t* __restrict__ Sm, int32_t* __restrict__ offs) {
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= S; i += blockDim.x) offs[i] = i < S ? min(i * chunk, T) : T;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nv = Ep / 4;   // 16-byte groups in a row of 2 Ep bf16
+  for (int t = blockIdx.x * BW + wid; t < T; t += gridDim.x * BW) {
+    uint4* row = reinterpret_cast<uint4*>(Sm + (size_t)t * 2 * Ep);
+    for (int v = lane; v < nv; v += 32) row[v] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    if (lane < R) {
+      const int e = idx[(size_t)t * R + lane];
+      if ((unsigned)e < (unsigned)E) {
+        const float v = dsel[(size_t)t * R + lane];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+        Sm[(size_t)t * 2 * Ep + e] = __bfloat16_as_ushort(hi);
+        Sm[(size_t)t * 2 * Ep + Ep + e] = __bfloat16_as_ushort(lo);
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// dW_g[k, e] = sum over chunks s (ascending) of (P[s][k][e] + P[s][k][Ep + e]).
+__global__ void dwg_sum_kernel(const float* __restrict__ P, int S, int d, int E, int Ep,
+                               float* __restrict__ dW_gate) {
+  const long long n = (long long)d * E;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int k = (int)(i / E), e = (int)(i % E);
+    const float* p = P + (size_t)k * 2 * Ep + e;
+    const size_t step = (size_t)d * 2 * Ep;
+    float v = 0.f;
+    for (int s = 0; s < S; ++s) v += p[s * step] + p[s * step + Ep];
+    dW_gate[i] = v;
   }
 }
 
@@ -105,76 +157,6 @@ __global__ void wg_transpose_kernel(const float* __restrict__ wg, int d, int E,
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int e = e0 + i, k = k0 + threadIdx.x;
     if (k < d && e < E) wgT[(size_t)e * d + k] = tile[threadIdx.x][i];
-  }
-}
-
-// dW_g[k, e] = sum over expert e's rows (ascending) of dsel_row[row] * x_perm[row, k].
-// Pass 1: block = (1024-column chunk, expert, row chunk s of DWG_SPLIT); thread =
-// 8 consecutive columns (16-byte loads), four rows' loads in flight per step,
-// fp32 accumulation in row order -> part[s][e][k].  Pass 2 adds the DWG_SPLIT
-// partials in s order and writes dW_g transposed through shared memory.
-constexpr int DWG_THREADS = 128;
-constexpr int DWG_SPLIT = 4;
-// dW_g column e, split over DWG_SPLIT row ranges: sum over the expert's rows of
-// dsel_row[row] * x[token(row)].  The rows are read from x through row_slot
-// (x_perm[row] == x[row_slot[row] / R]): every expert walks its tokens in
-// ascending order, so the R reads of a token's row come close together and
-// mostly hit L2 -- x (T*d) is read from HBM about once instead of x_perm (N*d).
-__global__ void __launch_bounds__(DWG_THREADS) dwg_partial_kernel(
-    const uint16_t* __restrict__ x, const int32_t* __restrict__ row_slot, int R,
-    const int32_t* __restrict__ offsets, const float* __restrict__ dsel_row, int d, int E,
-    float* __restrict__ part) {
-  const int e = blockIdx.y, sp = blockIdx.z;
-  const int k0 = (blockIdx.x * DWG_THREADS + threadIdx.x) * 8;
-  if (k0 >= d) return;
-  const int e0 = offsets[e], n = offsets[e + 1] - e0;
-  const int r0 = e0 + (int)((long long)n * sp / DWG_SPLIT);
-  const int r1 = e0 + (int)((long long)n * (sp + 1) / DWG_SPLIT);
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  int row = r0;
-  for (; row + 4 <= r1; row += 4) {
-    uint4 q[4];
-    float s[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      q[u] = ldg_nc_v4(x + (size_t)(row_slot[row + u] / R) * d + k0);
-      s[u] = dsel_row[row + u];
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float xv[8];
-      unpack8(q[u], xv);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = fmaf(s[u], xv[j], acc[j]);
-    }
-  }
-  for (; row < r1; ++row) {
-    float xv[8];
-    unpack8(ldg_nc_v4(x + (size_t)(row_slot[row] / R) * d + k0), xv);
-    const float s = dsel_row[row];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = fmaf(s, xv[j], acc[j]);
-  }
-  float4* dst = reinterpret_cast<float4*>(part + ((size_t)sp * E + e) * d + k0);
-  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-}
-
-__global__ void dwg_reduce_kernel(const float* __restrict__ part, int d, int E,
-                                  float* __restrict__ dW_gate) {
-  __shared__ float tile[32][33];
-  const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {      // i: expert in tile, x: column
-    const int e = e0 + i, k = k0 + threadIdx.x;
-    float v = 0.f;
-    if (e < E && k < d)
-      for (int sp = 0; sp < DWG_SPLIT; ++sp) v += part[((size_t)sp * E + e) * d + k];
-    tile[i][threadIdx.x] = v;
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {      // i: column in tile, x: expert
-    const int k = k0 + i, e = e0 + threadIdx.x;
-    if (k < d && e < E) dW_gate[(size_t)k * E + e] = tile[threadIdx.x][i];
   }
 }
 
@@ -258,14 +240,37 @@ int grid_for(int T, int per_block) {
   const int b = ceil_div(T, per_block);
   return b < 152 * 8 ? b : 152 * 8;
 }
+
+// Chunks of the router weight-gradient GEMM: whole 64-row k-blocks, about two
+// waves of 76 CTA-pair items, at least 256 rows each.
+DwgPlan plan_dwg(int T, int d, int E) {
+  DwgPlan p;
+  p.Ep = ceil_div(E, 32) * 32;
+  const int tiles = ceil_div(d, 256) * ceil_div(2 * p.Ep, 256);
+  int S = std::max(1, 152 / tiles);
+  S = std::min(S, std::max(1, ceil_div(T, 256)));
+  S = std::min(S, 64);
+  p.chunk = std::max(64, ceil_div(ceil_div(std::max(T, 1), S), 64) * 64);
+  p.S = std::max(1, ceil_div(T, p.chunk));
+  return p;
+}
+
 }  // namespace
+
+DwgPlan dwg_plan(int T, int d, int E) { return plan_dwg(T, d, E); }
+
+size_t dwg_ws_bytes(int T, int d, int E) {
+  const DwgPlan p = plan_dwg(T, d, E);
+  return align_up((size_t)T * 2 * p.Ep * 2, 256) + align_up((size_t)p.S * d * 2 * p.Ep * 4, 256) +
+         align_up((size_t)(p.S + 1) * 4, 256) + align_up((size_t)4 * p.S * 128, 256);
+}
 
 cudaError_t launch_bwd_route(const uint16_t* dy, const uint16_t* o, const int32_t* slot_row,
                              const float* w, int T, int d, int R, uint16_t* dO, float* dsel_tok,
-                             float* dsel_row, cudaStream_t s) {
+                             cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   bwd_route_kernel<<<grid_for(T, BW), BW * 32, 0, s>>>(dy, o, slot_row, w, T, d, R, T * R, dO,
-                                                      dsel_tok, dsel_row);
+                                                      dsel_tok);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -277,17 +282,28 @@ cudaError_t launch_wg_transpose(const float* wg, int d, int E, float* wgT, cudaS
   return cudaGetLastError();
 }
 
-size_t dwg_ws_bytes(int d, int E) { return align_up((size_t)DWG_SPLIT * E * d * 4, 256); }
-
-cudaError_t launch_dwg(const uint16_t* x, const int32_t* row_slot, int R, const int32_t* offsets,
-                       const float* dsel_row, int d, int E, float* dW_gate, void* ws,
+cudaError_t launch_dwg(const uint16_t* x, const int32_t* idx, const float* dsel_tok, int T, int d,
+                       int E, int R, float* dW_gate, void* ws, int* err, bool cta_pairs,
                        cudaStream_t s) {
-  float* part = static_cast<float*>(ws);
-  dim3 grid(ceil_div(d, DWG_THREADS * 8), E, DWG_SPLIT);
-  dwg_partial_kernel<<<grid, DWG_THREADS, 0, s>>>(x, row_slot, R, offsets, dsel_row, d, E, part);
-  dwg_reduce_kernel<<<dim3(ceil_div(d, 32), ceil_div(E, 32)), dim3(32, 8), 0, s>>>(part, d, E,
-                                                                                  dW_gate);
-  count_launches(2);
+  const DwgPlan p = plan_dwg(T, d, E);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* Sm = reinterpret_cast<uint16_t*>(w);
+  w += align_up((size_t)T * 2 * p.Ep * 2, 256);
+  float* P = reinterpret_cast<float*>(w);
+  w += align_up((size_t)p.S * d * 2 * p.Ep * 4, 256);
+  int32_t* offs = reinterpret_cast<int32_t*>(w);
+  w += align_up((size_t)(p.S + 1) * 4, 256);
+  void* maps = w;
+  dwg_operand_kernel<<<std::max(1, grid_for(T, BW)), BW * 32, 0, s>>>(idx, dsel_tok, T, E, R,
+                                                                      p.Ep, p.chunk, p.S, Sm, offs);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_dwg_gemm(x, Sm, offs, T, d, 2 * p.Ep, p.S, P, maps, err, cta_pairs, s);
+  if (e != cudaSuccess) return e;
+  dwg_sum_kernel<<<std::min(ceil_div(d * E, 256), 152 * 8), 256, 0, s>>>(P, p.S, d, E, p.Ep,
+                                                                        dW_gate);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -87,6 +87,13 @@ __device__ __forceinline__ uint32_t mx_codes4(const float* v, int k) {
   return (uint32_t)p0 | ((uint32_t)p1 << 16);
 }
 
+// 32-byte store of eight fp32 values (p must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(float* p, const float* v) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]),
+               "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

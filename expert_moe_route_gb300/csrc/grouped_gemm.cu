@@ -55,7 +55,9 @@ template <int M, bool C2 = false> struct Traits {
   static constexpr bool b_mn = (M == DH || M == DX || M == WG2 || M == WG13);
   static constexpr bool wgrad = (M == WG2 || M == WG13);
   // one 32-row x 128-B staging box per epilogue warp (all modes but the gate)
-  static constexpr int epi_bytes = (M == GATE) ? 0 : EPI_BYTES;
+  // (the weight-gradient modes on pairs store from registers: their 32 KB go to
+  // a seventh pipeline stage instead)
+  static constexpr int epi_bytes = (M == GATE || (C2 && (M == WG2 || M == WG13))) ? 0 : EPI_BYTES;
   // GATE: 128-column tiles with four partial accumulators (K-blocks rotate over
   // them; the epilogue adds them in IEEE fp32), so each accumulator takes a
   // quarter of the tensor core's accumulation steps.
@@ -74,7 +76,7 @@ template <int M, bool C2 = false> struct Traits {
   // C2: the CTA pair computes 256-row tiles; each CTA stages 128 rows of A
   // and half of B (128 of the 256 columns), so a stage is 32 KB and six fit.
   static constexpr int tile_m = C2 ? 2 * BM : BM;
-  static constexpr int stages = pair ? 3 : (C2 ? 6 : STAGES);
+  static constexpr int stages = pair ? 3 : (C2 ? ((M == WG2 || M == WG13) ? 7 : 6) : STAGES);
   static constexpr int a_bytes = pair ? 2 * A_BYTES : A_BYTES;
   static constexpr int b_bytes = C2 ? B_BYTES / 2 : B_BYTES;
   static constexpr int stage_bytes = a_bytes + b_bytes;
@@ -85,7 +87,7 @@ template <int M, bool C2 = false> struct Traits {
   static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + CTL_BYTES + 1024;
 };
 
-constexpr int MAX_STAGES = 6;
+constexpr int MAX_STAGES = 7;
 
 struct alignas(8) SharedCtl {
   uint64_t full[MAX_STAGES];
@@ -646,10 +648,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             store_bf16x16(g.out_bf16 + o2 + g.f, db, g.f - col);
           }
         }
-      } else {  // WG2 / WG13: fp32 weight gradients, staged and written by TMA stores
+      } else {  // WG2 / WG13: fp32 weight gradients
         // This warp owns output rows m0 .. m0+31 of expert e and half of the
-        // columns.  Each 32-column chunk goes TMEM -> registers -> a
-        // 128-B-swizzled 32x32 fp32 box in shared memory -> one bulk tensor store.
+        // columns.  Each 32-column chunk goes TMEM -> registers -> (pairs) each
+        // lane's 128 contiguous bytes of its row by plain 16-byte stores, or (one
+        // CTA) a 128-B-swizzled 32x32 fp32 box in shared memory -> one bulk
+        // tensor store.
         const int m0 = it.mt * Tr::tile_m + rrow + q * 32;
         const int mrows = (MODE == WG2) ? g.d : 2 * g.f;
         const int ncols = (MODE == WG2) ? g.f : g.d;
@@ -673,6 +677,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
           const int col = it.nt * BN + c;
           if (m0 >= mrows || col >= ncols) continue;          // warp-uniform
+          if (C2) {   // pairs: the lane's 32 values straight to its output row
+            float* base = (MODE == WG13 && m0 >= g.f) ? g.out_f32b : g.out_f32;
+            const int rows_e = (MODE == WG2) ? g.d : g.f;
+            float* dst = base + ((size_t)it.e * rows_e + mrow + lane) * ncols + col;
+            // a row starts 256-B aligned relative to base (ncols % 64 == 0), so
+            // base's alignment decides, uniformly: whole 32-byte sectors when it
+            // allows (twice fewer, full-sector L2 writes), else 16-byte stores
+            if ((reinterpret_cast<uintptr_t>(base) & 31u) == 0) {
+#pragma unroll
+              for (int q8 = 0; q8 < 4; ++q8) st_global_v8(dst + 8 * q8, v + 8 * q8);
+            } else {
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                reinterpret_cast<float4*>(dst)[q4] =
+                    make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            }
+            continue;
+          }
           if (lane == 0) bulk_wait_read_0();                  // the box's last store has read it
           __syncwarp();
           uint8_t* bp = box_ptr;
@@ -1230,6 +1252,39 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
                 : launch_mode<WG13>(mt.m[2], mt.m[3], mt.m[3], mc, mc2, mc2, g, wg13_items, s);
   trace_end(MOE_STAGE_BWD_WG13, s);
   return e;
+}
+
+// The router weight gradient's GEMM: the weight-gradient kernel (mode WG2) with
+// one "expert" per chunk of tokens, A = x [T, d] and B = S [T, n2], both
+// MN-major, K = the chunk's tokens; each chunk's maps end at its last token.
+cudaError_t launch_dwg_gemm(const uint16_t* x, const uint16_t* Sm, const int32_t* offs, int T,
+                            int d, int n2, int S, float* P, void* maps_ws, int* err,
+                            bool cta_pairs, cudaStream_t s) {
+  if (T == 0 || S == 0) return cudaSuccess;
+  const int tile_m = cta_pairs ? 2 * BM : BM;
+  MapTemplates mt;
+  if (!make_map(&mt.m[0], x, T, d, 64) || !make_map(&mt.m[1], Sm, T, n2, 64))
+    return cudaErrorInvalidValue;
+  mt.m[2] = mt.m[0];
+  mt.m[3] = mt.m[1];
+  CUtensorMap* emaps = static_cast<CUtensorMap*>(maps_ws);
+  expert_maps_kernel<<<ceil_div(4 * S, 256), 256, 0, s>>>(mt, offs, S, emaps);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  GemmArgs g{};
+  g.E = S; g.N = T; g.d = d; g.f = n2;
+  g.offsets = offs;
+  g.err = err;
+  g.n_tiles_m = ceil_div(d, tile_m);
+  g.n_tiles_n = ceil_div(n2, BN);
+  g.out_f32 = P;
+  g.emaps = emaps;
+  CUtensorMap mc;
+  if (!make_map_f32_3d(&mc, P, S, d, n2)) return cudaErrorInvalidValue;
+  const long long items = (long long)S * g.n_tiles_m * g.n_tiles_n;
+  return cta_pairs ? launch_mode<WG2, true>(mt.m[0], mt.m[1], mt.m[1], mc, mc, mc, g, items, s)
+                   : launch_mode<WG2>(mt.m[0], mt.m[1], mt.m[1], mc, mc, mc, g, items, s);
 }
 
 }  // namespace moe

@@ -140,12 +140,26 @@ cudaError_t launch_ffn_bwd(const uint16_t* x_perm, const int32_t* offsets, int N
 // backward of routing / dispatch / combine
 cudaError_t launch_bwd_route(const uint16_t* dy, const uint16_t* o, const int32_t* slot_row,
                              const float* w, int T, int d, int R, uint16_t* dO, float* dsel_tok,
-                             float* dsel_row, cudaStream_t s);
-cudaError_t launch_wg_transpose(const float* wg, int d, int E, float* wgT, cudaStream_t s);
-size_t dwg_ws_bytes(int d, int E);
-cudaError_t launch_dwg(const uint16_t* x, const int32_t* row_slot, int R, const int32_t* offsets,
-                       const float* dsel_row, int d, int E, float* dW_gate, void* ws,
+                             cudaStream_t s);
+// dW_g = x^T dlogits on the tensor cores: dlogits split into bf16 hi and lo
+// columns, S = [hi | lo] [T, 2 Ep], and the weight-gradient GEMM run over S
+// chunks of the tokens (one partial [d, 2 Ep] per chunk), then summed.
+struct DwgPlan {
+  int Ep;      // E rounded up to 32
+  int chunk;   // tokens per chunk (a multiple of 64)
+  int S;       // chunks
+};
+DwgPlan dwg_plan(int T, int d, int E);
+size_t dwg_ws_bytes(int T, int d, int E);
+cudaError_t launch_dwg(const uint16_t* x, const int32_t* idx, const float* dsel_tok, int T, int d,
+                       int E, int R, float* dW_gate, void* ws, int* err, bool cta_pairs,
                        cudaStream_t s);
+// P[s] = x[rows of chunk s]^T S[rows of chunk s] for the chunks in offs[0..S]
+// (S [T, n2] bf16, P [S, d, n2] fp32); maps_ws holds 4 * S tensor maps.
+cudaError_t launch_dwg_gemm(const uint16_t* x, const uint16_t* Sm, const int32_t* offs, int T,
+                            int d, int n2, int S, float* P, void* maps_ws, int* err,
+                            bool cta_pairs, cudaStream_t s);
+cudaError_t launch_wg_transpose(const float* wg, int d, int E, float* wgT, cudaStream_t s);
 cudaError_t launch_dx_combine(const uint16_t* dx_perm, const int32_t* slot_row,
                               const int32_t* idx, const float* dsel_tok, const float* wgT, int T,
                               int d, int E, int R, uint16_t* dx, cudaStream_t s,

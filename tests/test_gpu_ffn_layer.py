@@ -112,14 +112,17 @@ def test_layer_forward(lib, name, T):
     assert_close(f64(y)[same], ref["y"][same], "y")
 
 
-@pytest.mark.parametrize("name,T,E,f", [("tiny", None, None, None), ("train", 512, None, None),
-                                        ("mid", 1024, None, 448), ("mid", None, None, None)])
-def test_layer_backward(lib, name, T, E, f):
+@pytest.mark.parametrize("name,T,E,f,d", [
+    ("tiny", None, None, None, None), ("train", 512, None, None, None),
+    ("mid", 1024, None, 448, None), ("mid", None, None, None, None),
+    # dW_g's padding of E to a multiple of 32 (E = 40 -> 64), a d that is not a
+    # multiple of the 256-row tile, and E > 256 (S's 2 Ep columns span four tiles)
+    ("tiny", 300, 40, 128, 192), ("tiny", 200, 448, 64, 256)])
+def test_layer_backward(lib, name, T, E, f, d):
     over = {}
-    if T is not None:
-        over["T"] = T
-    if f is not None:
-        over["f"] = f
+    for k, v in (("T", T), ("E", E), ("f", f), ("d", d)):
+        if v is not None:
+            over[k] = v
     wl = synth.workload(name, **over)
     inp = synth.layer_inputs(wl, with_grad=True)
     dev, layer, saved, y = _layer_run(lib, wl, inp, train=True)
@@ -204,3 +207,28 @@ def test_row_scaled_outputs_combine_unweighted(lib):
                        bits(inp["W2"]), row_scale=f64(w_row))[3]
     ref = O.combine(o_s, saved.slot_row.cpu().numpy(), None, wl.T, wl.R)
     assert_close(f64(y2), ref, "y (weights on the expert side)")
+
+
+def test_layer_backward_gradient_buffers_16b_aligned(lib):
+    """Weight-gradient buffers that are 16- but not 32-byte aligned (the API asks
+    for 16) give the same bits as 256-byte aligned ones."""
+    wl = synth.workload("tiny", T=300)
+    inp = synth.layer_inputs(wl, with_grad=True)
+    dev, layer, saved, _ = _layer_run(lib, wl, inp, train=True)
+    ws = lib.workspace(lib.layer_bwd_ws_bytes(layer))
+
+    def grads(offset):
+        def buf(shape):
+            n = int(np.prod(shape))
+            return torch.zeros(n + 8, dtype=torch.float32, device="cuda")[offset:offset + n].view(shape)
+        out = dict(dx=torch.empty_like(dev["x"]), dWg=buf((wl.d, wl.E)),
+                   dW1=buf((wl.E, wl.f, wl.d)), dW3=buf((wl.E, wl.f, wl.d)),
+                   dW2=buf((wl.E, wl.d, wl.f)))
+        lib.moe_layer_bwd(layer, dev["x"], saved, dev["g"], out["dx"], out["dWg"], out["dW1"],
+                          out["dW3"], out["dW2"], ws, flags=lib.MOE_CHECK)
+        return out
+
+    a, b = grads(0), grads(4)
+    assert b["dW1"].data_ptr() % 32 == 16
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
