@@ -60,7 +60,9 @@ template <int M, bool C2 = false> struct Traits {
   static constexpr int epi_bytes = (M == GATE || (C2 && (M == WG2 || M == WG13))) ? 0 : EPI_BYTES;
   // GATE: 128-column tiles with four partial accumulators (K-blocks rotate over
   // them; the epilogue adds them in IEEE fp32), so each accumulator takes a
-  // quarter of the tensor core's accumulation steps.
+  // quarter of the tensor core's accumulation steps.  A stage holds one
+  // 64-deep block of x and the same block of the three bf16 terms of W_g
+  // (hi, mid, lo), so x is loaded once for the three products.
   static constexpr bool partials = (M == GATE);
   static constexpr int bn = partials ? 128 : BN;
   // GATEUP2 / DOWN2: each item is a 256-row block of one expert, computed as
@@ -76,13 +78,14 @@ template <int M, bool C2 = false> struct Traits {
   // C2: the CTA pair computes 256-row tiles; each CTA stages 128 rows of A
   // and half of B (128 of the 256 columns), so a stage is 32 KB and six fit.
   static constexpr int tile_m = C2 ? 2 * BM : BM;
-  static constexpr int stages = pair ? 3 : (C2 ? ((M == WG2 || M == WG13) ? 7 : 6) : STAGES);
+  static constexpr int stages =
+      (pair || partials) ? 3 : (C2 ? ((M == WG2 || M == WG13) ? 7 : 6) : STAGES);
   static constexpr int a_bytes = pair ? 2 * A_BYTES : A_BYTES;
-  static constexpr int b_bytes = C2 ? B_BYTES / 2 : B_BYTES;
+  static constexpr int b_bytes = partials ? 3 * 128 * BK * 2 : (C2 ? B_BYTES / 2 : B_BYTES);
   static constexpr int stage_bytes = a_bytes + b_bytes;
   // bytes the full barrier expects per stage (rank 0's barrier counts both CTAs' loads)
   static constexpr uint32_t stage_tx =
-      partials ? A_BYTES + 128 * BK * 2 : (uint32_t)(C2 ? 2 * stage_bytes : stage_bytes);
+      (uint32_t)(C2 ? 2 * stage_bytes : stage_bytes);
   // stages | epilogue staging | control block, plus slack for 1024-B alignment
   static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + CTL_BYTES + 1024;
 };
@@ -278,9 +281,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               }
             }
           } else if (MODE == GATE) {
-            // A repeats x for the hi, mid and lo thirds of K
-            tma_load_2d(sa, &tmA, bar, kx % g.d, it.row0);
-            tma_load_2d(sb, &tmB, bar, kx, it.nt * Tr::bn);
+            // x's k-block, then W_g's hi, mid and lo terms of it (thirds of B's K)
+            tma_load_2d(sa, &tmA, bar, kx, it.row0);
+#pragma unroll
+            for (int t = 0; t < 3; ++t)
+              tma_load_2d(sb + t * 128 * BK * 2, &tmB, bar, t * g.d + kx, it.nt * Tr::bn);
           } else if (Tr::is_down) {
             ld2(sa, &tmA, bar, kx, it.row0 + rrow);
             if (g.prepacked) {   // one contiguous 32 KB tile (C2: each CTA its 128 rows)
@@ -372,6 +377,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t d_tmem = Tr::partials ? tmem_base + (kb & 3) * 128 : d_base;
         const bool first = Tr::partials ? kb < 4 : kb == 0;
         auto issue = [&](int kk0, int kk1) {   // 16-deep K groups kk0 .. kk1-1 (one lane)
+          if (Tr::partials) {   // the three W_g terms against the same x block
+#pragma unroll
+            for (int t = 0; t < 3; ++t)
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk)
+                tc_mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32, 16, 1024),
+                            smem_desc_sw128(sb + t * 128 * BK * 2 + kk * 32, 16, 1024), idesc,
+                            (!first || t > 0 || kk > 0) ? 1u : 0u);
+            return;
+          }
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             if (kk < kk0) continue;
@@ -999,7 +1014,7 @@ cudaError_t launch_gate_tc(const uint16_t* x, const float* wg, const float* bias
     return cudaErrorInvalidValue;
   GemmArgs g{};
   g.E = E; g.N = T; g.d = d; g.f = 0;
-  g.kblocks = 3 * d / BK;
+  g.kblocks = d / BK;
   g.n_tiles_m = ceil_div(T, BM);
   g.n_tiles_n = ceil_div(E, 128);
   g.out_f32 = logits;
