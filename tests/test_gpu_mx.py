@@ -71,7 +71,21 @@ def test_dispatch_mx_bit_exact(lib):
     assert np.array_equal(xs.cpu().numpy()[:, : d // 32], qs[tok])
 
 
-def _ffn_mx_case(B, counts, d, f, seed, row_scale=False, check_weights=True, flags=0):
+def _host_mx(w):
+    """The oracle's codes and scales of a bf16 tensor [..., K], quantised along K."""
+    K = w.shape[-1]
+    c, s = O.quantize_mx(bits(w).reshape(-1, K))
+    return c.reshape(w.shape), s.reshape(w.shape[:-1] + (K // 32,))
+
+
+def _assert_codes(dev, host, what):
+    """The device's codes and (unpadded) scales equal the oracle's, bit for bit."""
+    (dc, ds), (hc, hs) = dev, host
+    assert np.array_equal(dc.cpu().numpy(), hc), f"{what}: codes"
+    assert np.array_equal(ds.cpu().numpy()[..., : hs.shape[-1]], hs), f"{what}: scales"
+
+
+def _ffn_mx_case(B, counts, d, f, seed, row_scale=False, flags=0):
     E = len(counts)
     offsets = np.zeros(E + 1, dtype=np.int32)
     offsets[1:] = np.cumsum(counts)
@@ -86,26 +100,21 @@ def _ffn_mx_case(B, counts, d, f, seed, row_scale=False, check_weights=True, fla
     hs = torch.zeros((N, B.mx_scale_row_bytes(f)), dtype=torch.uint8, device="cuda")
     rs = None
     if row_scale:
-        rs = torch.rand(N, generator=torch.Generator().manual_seed(seed + 4)).cuda() + 0.25
+        rs = torch.rand(N, generator=torch.Generator().manual_seed(seed + 4)) + 0.25
     ws = B.workspace(B.grouped_ffn_mx_ws_bytes(N, d, f, E))
     B.moe_grouped_ffn_mx(xq, xs, torch.from_numpy(offsets).cuda(), *q1, *q3, *q2, out, ws,
-                         hq=hq, hs=hs, row_scale=rs, flags=flags | B.MOE_CHECK)
+                         hq=hq, hs=hs, row_scale=None if rs is None else rs.cuda(),
+                         flags=flags | B.MOE_CHECK)
     torch.cuda.synchronize()
-    # the weights' codes and scales are the oracle's, bit for bit
-    for (c, s), w in zip((q1, q3, q2) if check_weights else (), (W1, W3, W2)):
-        K = w.shape[-1]
-        wc, wsc = O.quantize_mx(bits(w).reshape(-1, K))
-        assert np.array_equal(c.cpu().numpy().reshape(-1, K), wc)
-        assert np.array_equal(s.cpu().numpy().reshape(-1, s.shape[-1])[:, : K // 32], wsc)
+    # the oracle quantises the same bf16 inputs itself; the device's codes and
+    # scales must equal its own, bit for bit
+    hx, h1, h3, h2 = _host_mx(x), _host_mx(W1), _host_mx(W3), _host_mx(W2)
+    for dev, host, what in (((xq, xs), hx, "x"), (q1, h1, "W1"), (q3, h3, "W3"), (q2, h2, "W2")):
+        _assert_codes(dev, host, what)
+    a, b, hv, rq, rsc, h, o = O.expert_ffn_mx(*hx, offsets, *h1, *h3, *h2,
+                                              row_scale=None if rs is None else rs.numpy())
     npc = lambda t: t.cpu().numpy()
-    sk_d, sk_f = d // 32, f // 32
-    W1s = npc(q1[1])[..., :sk_d]
-    W3s = npc(q3[1])[..., :sk_d]
-    W2s = npc(q2[1])[..., :sk_f]
-    a, b, hv, rq, rsc, h, o = O.expert_ffn_mx(npc(xq), npc(xs)[:, :sk_d], offsets, npc(q1[0]), W1s,
-                                              npc(q3[0]), W3s, npc(q2[0]), W2s,
-                                              row_scale=None if rs is None else npc(rs))
-    got_h = O.dequantize_mx(npc(hq), npc(hs)[:, :sk_f])
+    got_h = O.dequantize_mx(npc(hq), npc(hs)[:, : f // 32])
     assert_close(got_h, h, "h (dequantised)")
     same = np.mean(npc(hq) == rq)
     assert same > 0.99, f"only {same:.4%} of h codes agree"
@@ -133,14 +142,15 @@ def test_grouped_ffn_mx_row_scale_and_repeatability(lib):
 def test_grouped_ffn_mx_large_shape_sampled_experts(lib):
     """The large workload's widths (d=7168, f=2048) on three experts' rows."""
     # (the quantiser itself is checked bit for bit at d = 7168 above)
-    _ffn_mx_case(lib, [21, 0, 300, 133], 7168, 2048, seed=77, check_weights=False)
+    _ffn_mx_case(lib, [21, 0, 300, 133], 7168, 2048, seed=77)
 
 
-@pytest.mark.parametrize("name,over", [("tiny", {}), ("mid", dict(T=1024)), ("large", dict(T=256, E=32))])
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("mid", dict(T=1024)), ("large", dict(T=128, E=8))])
 def test_layer_forward_mx(lib, name, over):
-    """moe_layer_fwd with MOE_FP8_MX: routing as the bf16 layer, then the oracle's
-    dispatch, microscaled fp8 expert FFN (on the device-quantised weights, checked
-    bit for bit above) and combine."""
+    """moe_layer_fwd with MOE_FP8_MX against the oracle's whole MX forward: its
+    own routing, dispatch, quantisation of x and of the weights (the device's
+    weight codes must equal its own), microscaled fp8 expert FFN and combine.
+    Rows and tokens are compared where the two routings agree (near ties aside)."""
     from workloads import synth
     wl = synth.workload(name, **over)
     inp = synth.layer_inputs(wl)
@@ -153,21 +163,66 @@ def test_layer_forward_mx(lib, name, over):
     lib.moe_layer_fwd(layer, dev["x"], y, saved, lib.workspace(lib.layer_fwd_ws_bytes(layer, flags)),
                       flags=flags | lib.MOE_CHECK)
     torch.cuda.synchronize()
+    h1, h3, h2 = _host_mx(inp["W1"]), _host_mx(inp["W3"]), _host_mx(inp["W2"])
+    for dev_q, host, what in (((mxw.W1q, mxw.W1s), h1, "W1"), ((mxw.W3q, mxw.W3s), h3, "W3"),
+                              ((mxw.W2q, mxw.W2s), h2, "W2")):
+        _assert_codes(dev_q, host, what)
     bias = None if inp["bias"] is None else inp["bias"].numpy()
     logits = O.gate_logits(bits(inp["x"]), inp["w_gate"].numpy(), bias)
     idx, w = O.route_topk(logits, wl.R)
     gidx = saved.topk_idx.cpu().numpy()
     same = (gidx == idx).all(axis=1)
     assert (same | near_tie_tokens(logits, wl.R)).all(), "routing differs without a near tie"
-    # the rest of the layer on the device's routing (exact where the routing agrees)
-    counts, offsets, row_slot, slot_row = O.dispatch_plan(gidx, wl.E)
-    assert np.array_equal(saved.offsets.cpu().numpy(), offsets)
+    counts, offsets, row_slot, slot_row = O.dispatch_plan(idx, wl.E)
     xq, xs = O.quantize_mx(bits(inp["x"]))
     tok = row_slot // wl.R
-    npc = lambda t: t.cpu().numpy()
-    kd, kf = wl.d // 32, wl.f // 32
-    *_, o = O.expert_ffn_mx(xq[tok], xs[tok], offsets, npc(mxw.W1q), npc(mxw.W1s)[..., :kd],
-                            npc(mxw.W3q), npc(mxw.W3s)[..., :kd], npc(mxw.W2q), npc(mxw.W2s)[..., :kf])
-    assert_close(f64(saved.o), o, "o")
-    yr = O.combine(o, slot_row, saved.topk_w.cpu().numpy(), wl.T, wl.R)
-    assert_close(f64(y), yr, "y")
+    *_, o = O.expert_ffn_mx(xq[tok], xs[tok], offsets, *h1, *h3, *h2)
+    yr = O.combine(o, slot_row, w, wl.T, wl.R)
+    # a row's o depends only on its token and expert: every row of every token routed alike
+    gsr = saved.slot_row.cpu().numpy().reshape(wl.T, wl.R)[same].reshape(-1)
+    rsr = slot_row.reshape(wl.T, wl.R)[same].reshape(-1)
+    assert_close(f64(saved.o)[gsr], o[rsr], "o (rows of tokens routed alike)")
+    assert_close(f64(y)[same], yr[same], "y (tokens routed alike)")
+
+
+def test_layer_forward_mx_full_size_sampled_experts(lib):
+    """The large workload (T=8192, d=7168, E=384, R=8, f=2048) as bench.py times it
+    with the microscaled fp8 FFN: weights quantised once on the device, then
+    moe_layer_fwd with MOE_FP8_MX.  The oracle recomputes every row of three
+    experts (the fewest rows, the most, one drawn at random) from its own
+    routing and its own quantisation of x and of those experts' weights."""
+    from workloads import synth
+    wl = synth.workload("large")
+    inp = synth.layer_inputs(wl, device="cuda")
+    mxw = lib.MxWeights(inp["W1"], inp["W3"], inp["W2"])
+    layer = lib.Layer(inp["w_gate"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], wl.R, wl.T,
+                      mx=mxw)
+    saved = lib.Saved(layer, "cuda", train=False)
+    y = torch.empty_like(inp["x"])
+    flags = lib.MOE_FP8_MX
+    lib.moe_layer_fwd(layer, inp["x"], y, saved, lib.workspace(lib.layer_fwd_ws_bytes(layer, flags)),
+                      flags=flags | lib.MOE_CHECK)
+    torch.cuda.synchronize()
+    xb = bits(inp["x"])
+    logits = O.gate_logits(xb, inp["w_gate"].cpu().numpy(), None)
+    idx, _ = O.route_topk(logits, wl.R)
+    gidx = saved.topk_idx.cpu().numpy()
+    same = (gidx == idx).all(axis=1)
+    assert (same | near_tie_tokens(logits, wl.R)).all()
+    counts = np.bincount(idx[same].reshape(-1), minlength=wl.E)
+    live = np.nonzero(counts)[0]
+    rng = np.random.default_rng(5)
+    experts = sorted({int(live[np.argmin(counts[live])]), int(np.argmax(counts)),
+                      int(rng.choice(live))})
+    dev_slot_row = saved.slot_row.cpu().numpy().reshape(wl.T, wl.R)
+    for e in experts:
+        t_e, r_e = np.nonzero((idx == e) & same[:, None])       # the expert's tokens, ascending
+        host = [O.quantize_mx(bits(inp[k][e])) for k in ("W1", "W3", "W2")]
+        for (c, sc), (dq, ds), what in zip(host, ((mxw.W1q, mxw.W1s), (mxw.W3q, mxw.W3s),
+                                                  (mxw.W2q, mxw.W2s)), ("W1", "W3", "W2")):
+            _assert_codes((dq[e], ds[e]), (c, sc), f"{what}[{e}]")
+        xq, xs = O.quantize_mx(xb[t_e])
+        *_, o = O.expert_ffn_mx(xq, xs, np.array([0, len(t_e)]),
+                                *(a[None] for pair in host for a in pair))
+        rows = torch.from_numpy(dev_slot_row[t_e, r_e]).long().cuda()
+        assert_close(f64(saved.o[rows]), o, f"o rows of expert {e} ({len(t_e)} rows)")
