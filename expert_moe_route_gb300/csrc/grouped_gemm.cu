@@ -377,7 +377,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t d_tmem = Tr::partials ? tmem_base + (kb & 3) * 128 : d_base;
         const bool first = Tr::partials ? kb < 4 : kb == 0;
         auto issue = [&](int kk0, int kk1) {   // 16-deep K groups kk0 .. kk1-1 (one lane)
-          if (Tr::partials) {   // the three W_g terms against the same x block
+          if constexpr (Tr::partials) {   // the three W_g terms against the same x block
 #pragma unroll
             for (int t = 0; t < 3; ++t)
 #pragma unroll
@@ -385,21 +385,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 tc_mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32, 16, 1024),
                             smem_desc_sw128(sb + t * 128 * BK * 2 + kk * 32, 16, 1024), idesc,
                             (!first || t > 0 || kk > 0) ? 1u : 0u);
-            return;
-          }
+          } else {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            if (kk < kk0) continue;
-            if (kk >= kk1) break;
-            const uint64_t ad = Tr::a_mn ? smem_desc_sw128(sa + kk * 2048, ATOM_BYTES, 1024)
-                                         : smem_desc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, ATOM_BYTES, 1024)
-                                         : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            if (C2) tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
-            else tc_mma_bf16(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
-            if (Tr::pair && it.row_end - it.row0 > BM)   // rows 128-255 share the B stage
-              tc_mma_bf16(tmem_base + BN, smem_desc_sw128(sa + A_BYTES + kk * 32, 16, 1024), bd,
-                          idesc, (!first || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              if (kk < kk0) continue;
+              if (kk >= kk1) break;
+              const uint64_t ad = Tr::a_mn ? smem_desc_sw128(sa + kk * 2048, ATOM_BYTES, 1024)
+                                           : smem_desc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, ATOM_BYTES, 1024)
+                                           : smem_desc_sw128(sb + kk * 32, 16, 1024);
+              if (C2) tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
+              else tc_mma_bf16(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
+              if (Tr::pair && it.row_end - it.row0 > BM)   // rows 128-255 share the B stage
+                tc_mma_bf16(tmem_base + BN, smem_desc_sw128(sa + A_BYTES + kk * 32, 16, 1024),
+                            bd, idesc, (!first || kk > 0) ? 1u : 0u);
+            }
           }
         };
         if (lane == 0) {
