@@ -339,16 +339,28 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
       const int row = row0 + q * 32 + lane;
       const bool valid = row < row_end;
       const bool any = row0 + q * 32 < row_end;   // warp-uniform: rows of the expert here
+      // the accumulator is released as soon as this warp's last TMEM load has
+      // landed: the math and the stores of its last block then overlap the
+      // next item's MMAs
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty));
+      };
       if (MODE == GATEUP) {
         // 64 columns of h (two 32-element scale blocks): a at c, b at 128 + c
-        for (int blk = 0; blk < 2 && any; ++blk) {
+        for (int blk = 0; blk < 2; ++blk) {
           const int c = half * 64 + blk * 32;
           float a[32], b[32];
-          tmem_ld16(t_row + c, a);
-          tmem_ld16(t_row + c + 16, a + 16);
-          tmem_ld16(t_row + 128 + c, b);
-          tmem_ld16(t_row + 128 + c + 16, b + 16);
-          tmem_ld_wait();
+          if (any) {
+            tmem_ld16(t_row + c, a);
+            tmem_ld16(t_row + c + 16, a + 16);
+            tmem_ld16(t_row + 128 + c, b);
+            tmem_ld16(t_row + 128 + c + 16, b + 16);
+            tmem_ld_wait();
+          }
+          if (blk == 1) release();
+          if (!any) continue;
           float amax = 0.f;
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
@@ -368,26 +380,34 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
           }
         }
       } else {
+        // 128 columns in two batches of 64: four TMEM loads per wait
         const float sc = (valid && g.row_scale) ? g.row_scale[row] : 1.f;
-        for (int c = half * 128; c < half * 128 + 128 && any; c += 16) {
-          float v[16];
-          tmem_ld16(t_row + c, v);
-          tmem_ld_wait();
-          const int col = nt * BN + c;
-          if (valid && col < g.d) {
-            if (g.row_scale) {
+        for (int bt = 0; bt < 2; ++bt) {
+          const int c0 = half * 128 + bt * 64;
+          float v[64];
+          if (any) {
 #pragma unroll
-              for (int u = 0; u < 16; ++u) v[u] *= sc;
+            for (int u = 0; u < 4; ++u) tmem_ld16(t_row + c0 + 16 * u, v + 16 * u);
+            tmem_ld_wait();
+          }
+          if (bt == 1) release();
+          if (!any) continue;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int col = nt * BN + c0 + 16 * u;
+            if (valid && col < g.d) {
+              float* x = v + 16 * u;
+              if (g.row_scale) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) x[t] *= sc;
+              }
+              uint4* dst = reinterpret_cast<uint4*>(g.out + (size_t)row * g.d + col);
+              dst[0] = pack8(x);
+              dst[1] = pack8(x + 8);
             }
-            uint4* dst = reinterpret_cast<uint4*>(g.out + (size_t)row * g.d + col);
-            dst[0] = pack8(v);
-            dst[1] = pack8(v + 8);
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty));
     }
   }
 
