@@ -348,19 +348,10 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty));
       };
       if (MODE == GATEUP) {
-        // 64 columns of h (two 32-element scale blocks): a at c, b at 128 + c
-        for (int blk = 0; blk < 2; ++blk) {
-          const int c = half * 64 + blk * 32;
-          float a[32], b[32];
-          if (any) {
-            tmem_ld16(t_row + c, a);
-            tmem_ld16(t_row + c + 16, a + 16);
-            tmem_ld16(t_row + 128 + c, b);
-            tmem_ld16(t_row + 128 + c + 16, b + 16);
-            tmem_ld_wait();
-          }
-          if (blk == 1) release();
-          if (!any) continue;
+        // 64 columns of h, two 32-element scale blocks: a at c, b at 128 + c.
+        // Block 0 is turned into codes while block 1's loads are in flight; both
+        // blocks' stores come after the release.
+        auto codes = [&](float* a, const float* b, uint32_t* w) {
           float amax = 0.f;
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
@@ -368,44 +359,82 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             amax = fmaxf(amax, fabsf(a[u]));
           }
           const int k = mx_exponent(amax);
-          uint32_t w[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) w[u] = mx_codes4(a + 4 * u, k);
-          if (valid) {
-            const int col = nt * 128 + c;
-            uint4* dst = reinterpret_cast<uint4*>(g.hq + (size_t)row * g.f + col);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            g.hs[(size_t)row * g.hs_stride + col / 32] = (uint8_t)(k + 127);
-          }
+          return k;
+        };
+        auto put = [&](int c, const uint32_t* w, int k) {
+          if (!valid) return;
+          const int col = nt * 128 + c;
+          uint4* dst = reinterpret_cast<uint4*>(g.hq + (size_t)row * g.f + col);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          g.hs[(size_t)row * g.hs_stride + col / 32] = (uint8_t)(k + 127);
+        };
+        const int c0 = half * 64, c1 = c0 + 32;
+        uint32_t w0[8], w1[8];
+        int k0 = 0;
+        float a[32], b[32];
+        if (any) {
+          tmem_ld16(t_row + c0, a);
+          tmem_ld16(t_row + c0 + 16, a + 16);
+          tmem_ld16(t_row + 128 + c0, b);
+          tmem_ld16(t_row + 128 + c0 + 16, b + 16);
+          tmem_ld_wait();
+          k0 = codes(a, b, w0);
+          tmem_ld16(t_row + c1, a);
+          tmem_ld16(t_row + c1 + 16, a + 16);
+          tmem_ld16(t_row + 128 + c1, b);
+          tmem_ld16(t_row + 128 + c1 + 16, b + 16);
+          tmem_ld_wait();
+        }
+        release();
+        if (any) {
+          put(c0, w0, k0);
+          const int k1 = codes(a, b, w1);
+          put(c1, w1, k1);
         }
       } else {
-        // 128 columns in two batches of 64: four TMEM loads per wait
+        // 128 columns in two batches of 64 (four TMEM loads per wait); batch 0
+        // is packed to bf16 while batch 1 loads, and both are stored after the
+        // release
         const float sc = (valid && g.row_scale) ? g.row_scale[row] : 1.f;
-        for (int bt = 0; bt < 2; ++bt) {
-          const int c0 = half * 128 + bt * 64;
-          float v[64];
-          if (any) {
+        const int c0 = half * 128;
+        auto pack64 = [&](float* v, uint32_t* p) {
+          if (g.row_scale) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) tmem_ld16(t_row + c0 + 16 * u, v + 16 * u);
-            tmem_ld_wait();
+            for (int t = 0; t < 64; ++t) v[t] *= sc;
           }
-          if (bt == 1) release();
-          if (!any) continue;
+#pragma unroll
+          for (int t = 0; t < 32; ++t) p[t] = pack_bf16(v[2 * t], v[2 * t + 1]);
+        };
+        auto put64 = [&](int c, const uint32_t* p) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int col = nt * BN + c0 + 16 * u;
+            const int col = nt * BN + c + 16 * u;
             if (valid && col < g.d) {
-              float* x = v + 16 * u;
-              if (g.row_scale) {
-#pragma unroll
-                for (int t = 0; t < 16; ++t) x[t] *= sc;
-              }
               uint4* dst = reinterpret_cast<uint4*>(g.out + (size_t)row * g.d + col);
-              dst[0] = pack8(x);
-              dst[1] = pack8(x + 8);
+              dst[0] = make_uint4(p[8 * u], p[8 * u + 1], p[8 * u + 2], p[8 * u + 3]);
+              dst[1] = make_uint4(p[8 * u + 4], p[8 * u + 5], p[8 * u + 6], p[8 * u + 7]);
             }
           }
+        };
+        uint32_t p0[32], p1[32];
+        float v[64];
+        if (any) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) tmem_ld16(t_row + c0 + 16 * u, v + 16 * u);
+          tmem_ld_wait();
+          pack64(v, p0);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) tmem_ld16(t_row + c0 + 64 + 16 * u, v + 16 * u);
+          tmem_ld_wait();
+        }
+        release();
+        if (any) {
+          put64(c0, p0);
+          pack64(v, p1);
+          put64(c0 + 64, p1);
         }
       }
     }
