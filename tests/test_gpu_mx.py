@@ -226,3 +226,45 @@ def test_layer_forward_mx_full_size_sampled_experts(lib):
                                 *(a[None] for pair in host for a in pair))
         rows = torch.from_numpy(dev_slot_row[t_e, r_e]).long().cuda()
         assert_close(f64(saved.o[rows]), o, f"o rows of expert {e} ({len(t_e)} rows)")
+
+
+@pytest.mark.parametrize("serial", [False, True])
+def test_layer_forward_mx_with_shared_expert(lib, serial):
+    """MOE_FP8_MX with a shared expert: the routed experts on the fp8 tensor cores,
+    the shared one in bf16 (on the side stream, or serially), added with weight 1
+    before y's rounding -- against the oracle's shared expert plus its MX routed
+    path, on the tokens routed alike; side stream and serial give the same bits."""
+    from workloads import synth
+    wl = synth.workload("tiny", T=200)
+    fs = 256
+    inp = synth.layer_inputs(wl)
+    sw = synth.shared_expert_inputs(wl, fs)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    shared = lib.Shared(*(sw[k].cuda() for k in ("W1", "W3", "W2")))
+    mxw = lib.MxWeights(dev["W1"], dev["W3"], dev["W2"])
+    layer = lib.Layer(dev["w_gate"], dev["bias"], dev["W1"], dev["W3"], dev["W2"], wl.R, wl.T,
+                      shared=shared, mx=mxw)
+    flags = lib.MOE_FP8_MX | (lib.MOE_SHARED_SERIAL if serial else 0)
+    ys = []
+    for fl in (flags, flags ^ lib.MOE_SHARED_SERIAL):
+        saved = lib.Saved(layer, "cuda", train=False)
+        y = torch.empty_like(dev["x"])
+        lib.moe_layer_fwd(layer, dev["x"], y, saved,
+                          lib.workspace(lib.layer_fwd_ws_bytes(layer, fl)), flags=fl | lib.MOE_CHECK)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
+    y = ys[0]
+    h1, h3, h2 = _host_mx(inp["W1"]), _host_mx(inp["W3"]), _host_mx(inp["W2"])
+    bias = None if inp["bias"] is None else inp["bias"].numpy()
+    logits = O.gate_logits(bits(inp["x"]), inp["w_gate"].numpy(), bias)
+    idx, w = O.route_topk(logits, wl.R)
+    same = (saved.topk_idx.cpu().numpy() == idx).all(axis=1)
+    assert (same | near_tie_tokens(logits, wl.R)).all(), "routing differs without a near tie"
+    counts, offsets, row_slot, slot_row = O.dispatch_plan(idx, wl.E)
+    xq, xs = O.quantize_mx(bits(inp["x"]))
+    tok = row_slot // wl.R
+    *_, o = O.expert_ffn_mx(xq[tok], xs[tok], offsets, *h1, *h3, *h2)
+    s_out = O.shared_expert_fwd(bits(inp["x"]), bits(sw["W1"]), bits(sw["W3"]), bits(sw["W2"]))[3]
+    yr = O.combine(o, slot_row, w, wl.T, wl.R, add=s_out)
+    assert_close(f64(y)[same], yr[same], "y (routed MX + shared bf16, tokens routed alike)")
