@@ -343,11 +343,13 @@ def kernel_sources_digest(files=None):
     return h.hexdigest()
 
 
-def traffic_key(wl):
-    """The traffic table's key of a workload: its name, plus T when not the default one."""
+def traffic_key(wl, mx=False):
+    """The traffic table's key of a workload: its name, plus T when not the default
+    one, plus "+mx" for the microscaled fp8 expert FFN."""
     from workloads import synth
     default_T = synth.WORKLOADS[wl.name].T
-    return wl.name if wl.T == default_T else f"{wl.name}@T={wl.T}"
+    key = wl.name if wl.T == default_T else f"{wl.name}@T={wl.T}"
+    return key + ("+mx" if mx else "")
 
 
 def profiled_traffic(workload, stage):
@@ -572,7 +574,8 @@ def run_ours(o, rank, world, device):
         stages[name] = stage_roofline(work[name], ms, tc_peak, pk, clk.get("sm_mhz"))
     dom = max((n for n in stages if work[n]["kind"] != "side"), key=lambda n: stages[n]["ms"])
     roof = dominant_roofline(stages, work, dom, tc_peak, regime, pk, pk_src,
-                             profiled_traffic(traffic_key(wl), dom), clk.get("sm_mhz"))
+                             profiled_traffic(traffic_key(wl, mxw is not None), dom),
+                             clk.get("sm_mhz"))
     # the whole step: its FLOPs against the tensor peak, and the sum of the
     # stages' roofline times against the measured step
     step_fl = sum(3.0 * w["flops"] if w["kind"] == "tensor3" else w["flops"]

@@ -206,6 +206,7 @@ def test_traffic_keys_name_a_non_default_token_count():
     assert bench.traffic_key(synth.workload("train")) == "train"
     assert bench.traffic_key(synth.workload("dispatch", T=8192)) == "dispatch"
     assert bench.traffic_key(synth.workload("dispatch", T=65536)) == "dispatch@T=65536"
+    assert bench.traffic_key(synth.workload("large"), mx=True) == "large+mx"
 
 
 def test_committed_traffic_entries_against_their_algorithmic_bytes():
