@@ -214,14 +214,17 @@ def test_committed_traffic_entries_against_their_algorithmic_bytes():
         table = json.load(fh)
     assert table["workloads"], "no entries"
     for key, stages in table["workloads"].items():
-        name, _, t = key.partition("@T=")
+        base, mx = (key[:-3], True) if key.endswith("+mx") else (key, False)
+        name, _, t = base.partition("@T=")
         wl = synth.workload(name, **({"T": int(t)} if t else {}))
-        work = bench.stage_work(wl)
+        work = bench.stage_work(wl, mx=mx)
         for stage, e in stages.items():
             # the algorithmic bytes of the entry are the work model's
             assert e["algorithmic_bytes_per_launch"] == work[stage]["bytes"], (key, stage)
-            # the measured DRAM bytes are that, give or take what stays in L2
-            assert 0.85 <= e["bytes_per_launch"] / e["algorithmic_bytes_per_launch"] <= 1.1
+            # the measured DRAM bytes are that, give or take what stays in L2;
+            # more than 1.1x is waste, and the entry must say where it comes from
+            ratio = e["bytes_per_launch"] / e["algorithmic_bytes_per_launch"]
+            assert 0.85 <= ratio <= 1.1 or (ratio <= 1.25 and e.get("waste")), (key, stage)
             assert os.path.exists(os.path.join(ROOT, e["profile"]))
             assert e["sources"] and len(e["sources_sha256"]) == 64
 
