@@ -188,8 +188,8 @@ moe_status_t moe_selftest_wait_timeout(unsigned limit_us, void* ws, moe_stream_t
   return finish(launch_selftest_wait(limit_us, err, s), err, MOE_CHECK, s);
 }
 
-static size_t gate_ws_bytes(int d, int E) {
-  return gate_tc_supported(d) ? gate_tc_ws_bytes(d, E) : 0;
+static size_t gate_ws_bytes(int T, int d, int E) {
+  return gate_tc_supported(d) ? gate_tc_ws_bytes(T, d, E) : 0;
 }
 
 // Gate projection: tensor-core split path when d % 64 == 0, else fp32 FMA.
@@ -210,7 +210,7 @@ moe_status_t moe_route(const uint16_t* x, const float* w_gate, const float* bias
     moe_status_t st = shape_check(T, d, E, R);
     if (st != MOE_OK) return st;
     if (!ws_bytes) return MOE_ERR_INVALID_ARG;
-    const size_t need = kErrBytes + gate_ws_bytes(d, E);
+    const size_t need = kErrBytes + gate_ws_bytes(T, d, E);
     if (!ws) {
       *ws_bytes = need;
       return MOE_OK;
@@ -531,7 +531,7 @@ static size_t mx_rows_ws(const moe_layer_t* L) {
 static size_t layer_fwd_ws(const moe_layer_t* L, unsigned flags) {
   const int N = L->T * L->R;
   return kErrBytes + align_up(dispatch_ws_bytes(L->T, L->E), 256) + tiles_ws_bytes(N, L->E) +
-         align_up(gate_ws_bytes(L->d, L->E), 256) + shared_fwd_ws(L) +
+         align_up(gate_ws_bytes(L->T, L->d, L->E), 256) + shared_fwd_ws(L) +
          ((flags & MOE_FP8_DISPATCH) ? fp8_rows_ws(L) : 0) +
          ((flags & MOE_FP8_MX) ? mx_rows_ws(L) : 0);
 }
@@ -586,7 +586,7 @@ moe_status_t moe_layer_fwd(const moe_layer_t* L, const uint16_t* x, uint16_t* y,
   int* err = static_cast<int*>(c.take(kErrBytes));
   void* dws = c.take(dispatch_ws_bytes(T, E));
   void* tws = c.take(tiles_ws_bytes(N, E));
-  void* gws = c.take(gate_ws_bytes(d, E));
+  void* gws = c.take(gate_ws_bytes(T, d, E));
   uint8_t* xq = nullptr;
   float* xs = nullptr;
   if (fp8) {

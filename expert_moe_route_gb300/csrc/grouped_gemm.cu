@@ -104,18 +104,25 @@ struct alignas(8) SharedCtl {
 
 struct Item {
   int e, row0, row_end, mt, nt, kblocks, krow0, krows;   // krows: K rows (weight-gradient modes)
+  int kb0 = 0, kstep = 1;   // GATE split over CTAs: this item's k-blocks are kb0, kb0 + kstep, ...
 };
 
 __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int item, Item& it) {
   if (mode == GATE) {  // one group of T rows: 128-row tiles x 128-expert column tiles
-    const int mi = item / g.n_tiles_n;
-    it.nt = item % g.n_tiles_n;
+    // with g.ksplit = 4, four CTAs share a tile: CTA p takes the k-blocks
+    // kb = p (mod 4), i.e. the tile's partial accumulator p
+    const int S = g.ksplit > 1 ? g.ksplit : 1;
+    const int tile = item / S, p = item - tile * S;
+    const int mi = tile / g.n_tiles_n;
+    it.nt = tile % g.n_tiles_n;
     it.row0 = mi * BM;
     it.row_end = g.N;
     it.e = 0;
     it.mt = 0;
     it.krow0 = it.krows = 0;
-    it.kblocks = g.kblocks;
+    it.kb0 = p;
+    it.kstep = S;
+    it.kblocks = (g.kblocks - p + S - 1) / S;
     return true;
   }
   if (mode == WG2 || mode == WG13) {
@@ -144,7 +151,7 @@ __device__ __forceinline__ bool decode_item(const GemmArgs& g, int mode, int ite
 
 __device__ __forceinline__ int total_items(const GemmArgs& g, int mode) {
   if (mode == WG2 || mode == WG13) return g.E * g.n_tiles_m * g.n_tiles_n;
-  if (mode == GATE) return g.n_tiles_m * g.n_tiles_n;
+  if (mode == GATE) return g.n_tiles_m * g.n_tiles_n * (g.ksplit > 1 ? g.ksplit : 1);
   return (*g.tile_count) * g.n_tiles_n;
 }
 
@@ -258,7 +265,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sa = tile_base + s * Tr::stage_bytes;
           const uint32_t sb = sa + Tr::a_bytes;
           if (leader) mbar_arrive_expect_tx(bar_local, Tr::stage_tx);
-          const int kx = kb * BK;
+          const int kx = (it.kb0 + kb * it.kstep) * BK;
           if (Tr::pair) tma_load_2d(sa + A_BYTES, &tmA, bar, kx, it.row0 + BM);   // rows 128-255
           if (Tr::is_gateup) {
             ld2(sa, &tmA, bar, kx, it.row0 + rrow);
@@ -374,8 +381,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const int rem = it.krows - kb * BK;
           if (rem < BK) kk_end = ceil_div(rem, 16);
         }
-        const uint32_t d_tmem = Tr::partials ? tmem_base + (kb & 3) * 128 : d_base;
-        const bool first = Tr::partials ? kb < 4 : kb == 0;
+        const int kbg = it.kb0 + kb * it.kstep;   // the k-block's index in K
+        const uint32_t d_tmem = Tr::partials ? tmem_base + (kbg & 3) * 128 : d_base;
+        const bool first = Tr::partials ? kbg < 4 : kb == 0;
         auto issue = [&](int kk0, int kk1) {   // 16-deep K groups kk0 .. kk1-1 (one lane)
           if constexpr (Tr::partials) {   // the three W_g terms against the same x block
 #pragma unroll
@@ -524,6 +532,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               store_bf16x16(g.save_a + off, a, g.f - col);
               store_bf16x16(g.save_b + off, b, g.f - col);
             }
+          }
+        }
+      } else if (MODE == GATE && g.ksplit > 1) {
+        // this CTA's partial accumulator (k-blocks kb0 (mod 4)) as it is; a
+        // second kernel adds the four partials in order, with the bias
+        const int row = it.row0 + r_local;
+        const bool valid = row < it.row_end;
+        for (int c = half * 64; c < half * 64 + 64; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + it.kb0 * 128 + c, v);
+          tmem_ld_wait();
+          const int col = it.nt * 128 + c;
+          if (valid && col < g.E) {
+            float* dst = g.out_parts + ((size_t)it.kb0 * g.N + row) * g.E + col;
+            const int n = g.E - col < 16 ? g.E - col : 16;
+            for (int u = 0; u < n; ++u) dst[u] = v[u];
           }
         }
       } else if (MODE == GATE) {
@@ -1001,12 +1025,41 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 
 bool gate_tc_supported(int d) { return d % 64 == 0; }
 
-size_t gate_tc_ws_bytes(int d, int E) { return align_up((size_t)E * 3 * d * 2, 256); }
+namespace {
+// The gate splits each tile's K over four CTAs (one per partial accumulator)
+// when the tiles alone would leave most SMs idle: at most 38 tiles (152 / 4)
+// and at least four k-blocks.
+bool gate_split(int T, int d, int E) {
+  const int tiles = ceil_div(T, BM) * ceil_div(E, 128);
+  return tiles * 4 <= 152 && d / BK >= 4;
+}
+
+// logits = ((P0 + P1) + P2) + P3 + bias, fp32, the order of the one-CTA epilogue
+__global__ void gate_sum_kernel(const float* __restrict__ parts, const float* __restrict__ bias,
+                                int T, int E, float* __restrict__ logits) {
+  const long long n = (long long)T * E;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    float v = parts[i];
+#pragma unroll
+    for (int p = 1; p < 4; ++p) v += parts[p * n + i];
+    logits[i] = v + (bias ? bias[i % E] : 0.f);
+  }
+}
+}  // namespace
+
+size_t gate_tc_ws_bytes(int T, int d, int E) {
+  return align_up((size_t)E * 3 * d * 2, 256) +
+         (gate_split(T, d, E) ? align_up((size_t)4 * T * E * 4, 256) : 0);
+}
 
 cudaError_t launch_gate_tc(const uint16_t* x, const float* wg, const float* bias, int T, int d,
                            int E, float* logits, void* ws, int* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   uint16_t* wgs = static_cast<uint16_t*>(ws);
+  const bool split = gate_split(T, d, E);
+  float* parts = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                          align_up((size_t)E * 3 * d * 2, 256));
   cudaError_t e = launch_wg_split(wg, d, E, wgs, s);
   if (e != cudaSuccess) return e;
   CUtensorMap ma, mb;
@@ -1020,7 +1073,16 @@ cudaError_t launch_gate_tc(const uint16_t* x, const float* wg, const float* bias
   g.out_f32 = logits;
   g.bias = bias;
   g.err = err;
-  return launch_mode<GATE>(ma, mb, mb, ma, ma, ma, g, (long long)g.n_tiles_m * g.n_tiles_n, s);
+  g.ksplit = split ? 4 : 1;
+  g.out_parts = parts;
+  e = launch_mode<GATE>(ma, mb, mb, ma, ma, ma, g,
+                        (long long)g.n_tiles_m * g.n_tiles_n * g.ksplit, s);
+  if (e != cudaSuccess || !split) return e;
+  const long long n = (long long)T * E;
+  gate_sum_kernel<<<(int)std::min<long long>((n + 255) / 256, 152 * 8), 256, 0, s>>>(
+      parts, bias, T, E, logits);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 bool prepack_supported(int d, int f) { return d % BN == 0 && f % 128 == 0; }

@@ -46,6 +46,9 @@ struct GemmArgs {
   // weight-gradient modes: per expert e, tensor maps of A (entry 2e) and B
   // (2e+1) whose row extent ends at the expert's last row (CUtensorMap, 64-B aligned)
   const void* emaps;
+  // gate: K split over ksplit (1 or 4) CTAs per tile, partials [4][T][E] fp32
+  int ksplit;
+  float* out_parts;
   int* err;
 };
 
@@ -55,7 +58,7 @@ cudaError_t launch_wg_split(const float* wg, int d, int E, uint16_t* wgs, cudaSt
 // Gate projection on the tensor cores (needs d % 64 == 0): logits = x W_g + bias
 // through the 3-term bf16 split of W_g; ws holds the split weights.
 bool gate_tc_supported(int d);
-size_t gate_tc_ws_bytes(int d, int E);
+size_t gate_tc_ws_bytes(int T, int d, int E);
 cudaError_t launch_gate_tc(const uint16_t* x, const float* wg, const float* bias, int T, int d,
                            int E, float* logits, void* ws, int* err, cudaStream_t s);
 // One block waits (bounded) on an mbarrier that nothing arrives on.

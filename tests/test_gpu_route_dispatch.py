@@ -166,3 +166,19 @@ def test_route_gate_paths(lib, T, d, E, R):
     ridx, _ = O.route_topk(ref_l, R)
     same = (idx.cpu().numpy() == ridx).all(axis=1)
     assert (same | near_tie_tokens(ref_l, R)).all()
+
+
+@pytest.mark.parametrize("d,E", [(2048, 64), (512, 200)])
+def test_gate_split_over_ctas_same_bits(lib, d, E):
+    """With few 128-token tiles the gate splits each tile's K over four CTAs (one
+    per partial accumulator) and adds the partials in a second kernel; a token's
+    logits must be the same bits as when its tile runs on one CTA (a larger T)."""
+    g = torch.Generator().manual_seed(d + E)
+    x = torch.randn((8192, d), generator=g).to(torch.bfloat16)
+    wg = torch.randn((d, E), generator=g) * 0.02
+    bias = torch.randn(E, generator=g)
+    small, _, _ = _route(lib, x[:1024].cuda(), wg.cuda(), bias.cuda(), 1024, E, 2)   # split
+    big, _, _ = _route(lib, x.cuda(), wg.cuda(), bias.cuda(), 8192, E, 2)            # one CTA
+    assert torch.equal(small, big[:1024])
+    ref = O.gate_logits(bits(x[:1024]), wg.numpy(), bias.numpy())
+    assert_close(f64(small), ref, "logits", max_rel=3e-5, mean_rel=1e-5)

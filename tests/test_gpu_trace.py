@@ -28,11 +28,12 @@ def test_trace_events_and_launch_count(lib):
     lib.moe_layer_bwd(layer, dev["x"], saved, dev["g"], dx, dWg, dW1, dW3, dW2, bws)
     lib.StageTrace.disarm()
     torch.cuda.synchronize()
-    # fwd: W_g split, gate GEMM, topk, 4 dispatch, tile list, gate-up (pairs, then
-    #      one CTA for the experts' last tiles of at most 128 rows), down (same), combine
+    # fwd: W_g split, gate GEMM (K over four CTAs at this size) and the partials'
+    #      sum, topk, 4 dispatch, tile list, gate-up (pairs, then one CTA for the
+    #      experts' last tiles of at most 128 rows), down (same), combine
     # bwd: route, tile list, DH (2), DX (2), per-expert weight-gradient maps, WG2, WG13,
     #      dW_g (operand S, per-chunk maps, GEMM, sum), W_g^T, dx
-    assert lib.kernel_launches() - n0 == 13 + 15
+    assert lib.kernel_launches() - n0 == 14 + 15
     ms = tr.elapsed_ms()
     for name in lib.STAGES:
         assert ms[name] > 0.0, name
