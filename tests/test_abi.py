@@ -172,3 +172,44 @@ def test_noalloc_dispatch_argument_checks_match_moe_dispatch():
     assert noalloc(*shape, x=P, x_perm=None) == code["MOE_ERR_INVALID_ARG"]  # x without x_perm
     assert noalloc(*shape, x=P + 8, x_perm=P) == code["MOE_ERR_UNSUPPORTED"]  # x not 16-B aligned
     assert noalloc(*shape, x=P, x_perm=P + 4) == code["MOE_ERR_UNSUPPORTED"]
+
+
+def test_microscaled_fp8_host_checks():
+    """moe_quantize_mx, moe_dispatch_mx and moe_grouped_ffn_mx check their shapes
+    and answer workspace queries on the host."""
+    lib = B.lib()
+    st = {v: k for k, v in B.STATUS.items()}
+    n = ctypes.c_size_t(0)
+    # quantise: K a multiple of 32; no rows is a no-op
+    assert lib.moe_quantize_mx(None, ctypes.c_longlong(4), 48, None, None, None) == \
+        st["MOE_ERR_UNSUPPORTED"]
+    assert lib.moe_quantize_mx(None, ctypes.c_longlong(-1), 64, None, None, None) == \
+        st["MOE_ERR_INVALID_ARG"]
+    assert lib.moe_quantize_mx(None, ctypes.c_longlong(0), 64, None, None, None) == st["MOE_OK"]
+    assert lib.moe_quantize_mx(None, ctypes.c_longlong(4), 64, None, None, None) == \
+        st["MOE_ERR_INVALID_ARG"]
+    # dispatch: d a multiple of 128, the same shape rules as moe_dispatch, a workspace query
+    args = (None, None, 100, 256, 8, 2) + (None,) * 6
+    assert lib.moe_dispatch_mx(*args, None, ctypes.byref(n), 0, None) == st["MOE_OK"]
+    assert n.value > 0
+    bad_d = (None, None, 100, 192, 8, 2) + (None,) * 6
+    assert lib.moe_dispatch_mx(*bad_d, None, ctypes.byref(n), 0, None) == st["MOE_ERR_UNSUPPORTED"]
+    bad_r = (None, None, 100, 256, 8, 9) + (None,) * 6
+    assert lib.moe_dispatch_mx(*bad_r, None, ctypes.byref(n), 0, None) == st["MOE_ERR_INVALID_ARG"]
+    small = ctypes.c_size_t(16)
+    assert lib.moe_dispatch_mx(*args, ctypes.c_void_p(4096), ctypes.byref(small), 0, None) == \
+        st["MOE_ERR_WORKSPACE"]
+    # grouped FFN: d and f multiples of 128, E up to 1024, a workspace query
+    def ffn(N, d, f, E, ws=None, nb=None):
+        return lib.moe_grouped_ffn_mx(*(None,) * 3, N, d, f, E, *(None,) * 10, ws,
+                                      ctypes.byref(nb if nb is not None else n), 0, None)
+    assert ffn(1000, 256, 384, 8) == st["MOE_OK"] and n.value > 0
+    assert ffn(1000, 256, 320, 8) == st["MOE_ERR_UNSUPPORTED"]
+    assert ffn(1000, 192, 384, 8) == st["MOE_ERR_UNSUPPORTED"]
+    assert ffn(1000, 256, 384, 2000) == st["MOE_ERR_UNSUPPORTED"]
+    assert ffn(-1, 256, 384, 8) == st["MOE_ERR_INVALID_ARG"]
+    assert ffn(1000, 256, 384, 8, ctypes.c_void_p(4096), ctypes.c_size_t(16)) == \
+        st["MOE_ERR_WORKSPACE"]
+    # workspace present but no weights
+    big = ctypes.c_size_t(1 << 30)
+    assert ffn(1000, 256, 384, 8, ctypes.c_void_p(1 << 20), big) == st["MOE_ERR_INVALID_ARG"]
